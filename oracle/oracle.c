@@ -1,0 +1,335 @@
+/*
+ * ORACLE — test infrastructure only.
+ *
+ * A plain, slow fp64 CPU statement of the Flux-style attention call:
+ *     O = softmax(scale * RoPE(RMSNorm_q(q)) RoPE(RMSNorm_k(k))^T + mask) V
+ * and its gradients. Every step materialises its full intermediate (the whole
+ * S_q x S_kv score, probability and gradient matrices of a head); nothing is
+ * tiled, fused or reordered. It shares no code with the CUDA library and is
+ * only ever loaded by the test-suite, by the smoke check and by the benchmark's
+ * CPU-baseline leg.
+ *
+ * Sources (page titles and sections):
+ *  - "Flux-family attention: flash-attn and other backends fail in an autocast
+ *    context" (diffusers issue 14104), "Root cause" list: q and k pass through
+ *    norm_q / norm_k (torch.nn.RMSNorm over the head dimension), then the
+ *    rotary embedding, then attention; v goes straight to attention.
+ *  - "Metal Flash Attention" (SimpleTuner docs), section "Fused RoPE + SDPA":
+ *    interleaved-pair rotation of Q and K, one angle per pair (pair-duplicated
+ *    cos/sin tables), gradients returned w.r.t. the pre-RoPE Q/K through the
+ *    inverse rotation (the same rotation with sin negated).
+ *  - same page, section "Enable In SimpleTuner": bool masks (True = attend),
+ *    additive float masks, batched [B,H,S_q,S_kv] and broadcast [B,1,1,S_kv]
+ *    masks; causal calls.
+ * Readings where the pages are silent (frequency formula, rotation sign,
+ * fully-masked rows, causal alignment) are stated beside the code below.
+ *
+ * Layouts: q, dq, o, do are [B, S_q, H, D]; k, v, dk, dv are [B, S_kv, H, D];
+ * all contiguous fp64. Angles phi are [Bp, S, D/2] with Bp in {1, B}.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+/* Multi-axis rotary angles ("Fused RoPE + SDPA": one angle per interleaved
+ * pair). Reading: axis a owns head dims [o_a, o_a + d_a) with o_a the sum of
+ * the earlier axes' widths; inside axis a, pair j (dims o_a+2j, o_a+2j+1) has
+ * frequency theta^(-2j/d_a), j restarting at 0 in every axis, and angle
+ * id[a] * frequency.
+ *   ids: [n_tok, n_axes] (position ids of each token), phi: [n_tok, D/2]. */
+void oracle_rope_angles(const double* ids, int64_t n_tok, int n_axes, const int* axes_dim, double theta,
+                        double* phi) {
+  int D = 0;
+  for (int a = 0; a < n_axes; ++a) D += axes_dim[a];
+  for (int64_t t = 0; t < n_tok; ++t) {
+    int pair = 0;
+    for (int a = 0; a < n_axes; ++a) {
+      const int d_a = axes_dim[a];
+      for (int j = 0; j < d_a / 2; ++j) {
+        const double freq = pow(theta, -2.0 * (double)j / (double)d_a);
+        phi[t * (D / 2) + pair] = ids[t * n_axes + a] * freq;
+        ++pair;
+      }
+    }
+  }
+}
+
+/* RMSNorm of one row (torch.nn.RMSNorm over the head dimension, eps inside
+ * the square root): r = 1/sqrt(mean(x^2) + eps), y = x * r * w. */
+static double rmsnorm_row(const double* x, const double* w, int D, double eps, double* y) {
+  double ss = 0.0;
+  for (int d = 0; d < D; ++d) ss += x[d] * x[d];
+  const double r = 1.0 / sqrt(ss / (double)D + eps);
+  for (int d = 0; d < D; ++d) y[d] = x[d] * r * w[d];
+  return r;
+}
+
+/* Interleaved-pair rotation (counter-clockwise):
+ *   y0 = x0 cos(phi) - x1 sin(phi),  y1 = x0 sin(phi) + x1 cos(phi). */
+static void rope_row(const double* x, const double* phi, int D, double* y) {
+  for (int p = 0; p < D / 2; ++p) {
+    const double c = cos(phi[p]), s = sin(phi[p]);
+    y[2 * p] = x[2 * p] * c - x[2 * p + 1] * s;
+    y[2 * p + 1] = x[2 * p] * s + x[2 * p + 1] * c;
+  }
+}
+
+/* Inverse rotation: the same pairwise rotation with sin negated. */
+static void rope_row_inverse(const double* g, const double* phi, int D, double* y) {
+  for (int p = 0; p < D / 2; ++p) {
+    const double c = cos(phi[p]), s = -sin(phi[p]);
+    y[2 * p] = g[2 * p] * c - g[2 * p + 1] * s;
+    y[2 * p + 1] = g[2 * p] * s + g[2 * p + 1] * c;
+  }
+}
+
+/* Pre-attention transform of one head: out[s][:] = RoPE(RMSNorm(x[b,s,h,:])).
+ * r_out[s] receives the RMSNorm reciprocal root of each row. */
+static void transform_head(const double* x, int S, int H, int D, int b, int h, const double* w, double eps,
+                           const double* phi, double* out, double* r_out) {
+#pragma omp parallel for schedule(static)
+  for (int s = 0; s < S; ++s) {
+    double tmp[1024];
+    const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
+    r_out[s] = rmsnorm_row(xr, w, D, eps, tmp);
+    rope_row(tmp, phi + (int64_t)s * (D / 2), D, out + (int64_t)s * D);
+  }
+}
+
+/* Exported for the pins: rows x [n_rows][D] -> RoPE(RMSNorm(x)) with one
+ * angle row phi [n_rows][D/2] per input row. */
+void oracle_qk_transform(const double* x, int64_t n_rows, int D, const double* w, double eps, const double* phi,
+                         double* out) {
+  for (int64_t s = 0; s < n_rows; ++s) {
+    double tmp[1024];
+    rmsnorm_row(x + s * D, w, D, eps, tmp);
+    rope_row(tmp, phi + s * (D / 2), D, out + s * D);
+  }
+}
+
+/* Mask value at (b, h, i, j): returns 0 for "attend unchanged", -inf for a
+ * bool False, or the additive value. kind: 0 none, 1 bool (uint8), 2 additive. */
+static double mask_value(int kind, const void* mask, const int64_t* ms, int b, int h, int i, int j) {
+  if (kind == 0) return 0.0;
+  const int64_t off = (int64_t)b * ms[0] + (int64_t)h * ms[1] + (int64_t)i * ms[2] + (int64_t)j * ms[3];
+  if (kind == 1) return ((const uint8_t*)mask)[off] ? 0.0 : -INFINITY;
+  return ((const double*)mask)[off];
+}
+
+/* Scores and probabilities of one head, both [Sq][Skv]:
+ *   s_ij = scale * q'_i . k'_j + mask_ij   (-inf where a bool mask is False
+ *          or, when causal, where j > i — top-left aligned, as torch's
+ *          is_causal);
+ *   P = row softmax, lse_i = ln sum_j exp(s_ij).
+ * A row whose every entry is -inf gets P = 0 and lse = -inf (reading: the
+ * pages define no output there; zero output, zero gradient). */
+static void head_probs(const double* qp, const double* kp, int Sq, int Skv, int D, double scale, int kind,
+                       const void* mask, const int64_t* ms, int causal, int b, int h, double* P, double* lse) {
+#pragma omp parallel for schedule(static)
+  for (int i = 0; i < Sq; ++i) {
+    double* row = P + (int64_t)i * Skv;
+    double m = -INFINITY;
+    for (int j = 0; j < Skv; ++j) {
+      double s = 0.0;
+      for (int d = 0; d < D; ++d) s += qp[(int64_t)i * D + d] * kp[(int64_t)j * D + d];
+      s = scale * s + mask_value(kind, mask, ms, b, h, i, j);
+      if (causal && j > i) s = -INFINITY;
+      row[j] = s;
+      if (s > m) m = s;
+    }
+    if (m == -INFINITY) {
+      for (int j = 0; j < Skv; ++j) row[j] = 0.0;
+      lse[i] = -INFINITY;
+      continue;
+    }
+    double l = 0.0;
+    for (int j = 0; j < Skv; ++j) {
+      row[j] = exp(row[j] - m);
+      l += row[j];
+    }
+    for (int j = 0; j < Skv; ++j) row[j] /= l;
+    lse[i] = m + log(l);
+  }
+}
+
+/* out[r][:] = sum_c M[r][c] * Y[c][:]   (M is [R][C], Y is [C][D]) */
+static void mat_ab(const double* M, int R, int C, const double* Y, int D, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int r = 0; r < R; ++r) {
+    double* o = out + (int64_t)r * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int c = 0; c < C; ++c) {
+      const double a = M[(int64_t)r * C + c];
+      if (a == 0.0) continue;
+      for (int d = 0; d < D; ++d) o[d] += a * Y[(int64_t)c * D + d];
+    }
+  }
+}
+
+/* out[c][:] = sum_r M[r][c] * X[r][:]   (M is [R][C], X is [R][D]) */
+static void mat_atb(const double* M, int R, int C, const double* X, int D, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int c = 0; c < C; ++c) {
+    double* o = out + (int64_t)c * D;
+    for (int d = 0; d < D; ++d) o[d] = 0.0;
+    for (int r = 0; r < R; ++r) {
+      const double a = M[(int64_t)r * C + c];
+      if (a == 0.0) continue;
+      for (int d = 0; d < D; ++d) o[d] += a * X[(int64_t)r * D + d];
+    }
+  }
+}
+
+/* Copy head h of batch b of x [B,S,H,D] into a [S][D] matrix. */
+static void gather_head(const double* x, int S, int H, int D, int b, int h, double* out) {
+  for (int s = 0; s < S; ++s)
+    memcpy(out + (int64_t)s * D, x + (((int64_t)b * S + s) * H + h) * D, sizeof(double) * D);
+}
+static void scatter_head(const double* m, int S, int H, int D, int b, int h, double* x) {
+  for (int s = 0; s < S; ++s)
+    memcpy(x + (((int64_t)b * S + s) * H + h) * D, m + (int64_t)s * D, sizeof(double) * D);
+}
+
+/* Forward for the heads listed in `bh` (flattened b*H + h; NULL = all).
+ * phi_q: [Bpq, Sq, D/2], phi_k: [Bpk, Skv, D/2] (Bp* in {1, B}).
+ * Writes o [B,Sq,H,D] and lse [B,H,Sq] at the listed heads only.
+ * Returns 0, or -1 when a work buffer cannot be allocated. */
+int oracle_fwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
+               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+               const int* bh, int n_bh, double* o, double* lse) {
+  double* qp = malloc(sizeof(double) * (size_t)Sq * D);
+  double* kp = malloc(sizeof(double) * (size_t)Skv * D);
+  double* vh = malloc(sizeof(double) * (size_t)Skv * D);
+  double* oh = malloc(sizeof(double) * (size_t)Sq * D);
+  double* rq = malloc(sizeof(double) * (size_t)Sq);
+  double* rk = malloc(sizeof(double) * (size_t)Skv);
+  double* P = malloc(sizeof(double) * (size_t)Sq * Skv);
+  int rc = 0;
+  if (!qp || !kp || !vh || !oh || !rq || !rk || !P) { rc = -1; goto done; }
+  const int n = bh ? n_bh : B * H;
+  for (int t = 0; t < n; ++t) {
+    const int idx = bh ? bh[t] : t;
+    const int b = idx / H, h = idx % H;
+    transform_head(q, Sq, H, D, b, h, wq, eps, phi_q + (int64_t)(bpq > 1 ? b : 0) * Sq * (D / 2), qp, rq);
+    transform_head(k, Skv, H, D, b, h, wk, eps, phi_k + (int64_t)(bpk > 1 ? b : 0) * Skv * (D / 2), kp, rk);
+    gather_head(v, Skv, H, D, b, h, vh);
+    head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P,
+               lse + ((int64_t)b * H + h) * Sq);
+    mat_ab(P, Sq, Skv, vh, D, oh);
+    scatter_head(oh, Sq, H, D, b, h, o);
+  }
+done:
+  free(qp); free(kp); free(vh); free(oh); free(rq); free(rk); free(P);
+  return rc;
+}
+
+/* RMSNorm + RoPE backward of one head. gp: gradient w.r.t. the rotated,
+ * normalised rows [S][D]; x: raw input [B,S,H,D]. Writes dx into [B,S,H,D]
+ * and adds sum_s (R^T gp) * x * r into dw.
+ *   dy = R^T gp (inverse rotation), g = w * dy,
+ *   dx = r g - (r^3 / D) x (x . g),   dw += dy * x * r. */
+static void transform_head_bwd(const double* gp, const double* x, int S, int H, int D, int b, int h,
+                               const double* w, const double* phi, const double* r, double* dx, double* dw) {
+  double* dy_all = malloc(sizeof(double) * (size_t)S * D);
+#pragma omp parallel for schedule(static)
+  for (int s = 0; s < S; ++s) {
+    double g[1024];
+    double* dy = dy_all + (int64_t)s * D;
+    const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
+    double* dxr = dx + (((int64_t)b * S + s) * H + h) * D;
+    rope_row_inverse(gp + (int64_t)s * D, phi + (int64_t)s * (D / 2), D, dy);
+    double xg = 0.0;
+    for (int d = 0; d < D; ++d) {
+      g[d] = w[d] * dy[d];
+      xg += xr[d] * g[d];
+    }
+    const double rs = r[s];
+    for (int d = 0; d < D; ++d) dxr[d] = rs * g[d] - (rs * rs * rs / (double)D) * xr[d] * xg;
+  }
+  for (int s = 0; s < S; ++s) {
+    const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
+    for (int d = 0; d < D; ++d) dw[d] += dy_all[(int64_t)s * D + d] * xr[d] * r[s];
+  }
+  free(dy_all);
+}
+
+/* Backward for the listed heads, given dO [B,Sq,H,D]:
+ *   dV = P^T dO, dP = dO V^T, Delta_i = sum_j P_ij dP_ij, dS = P (dP - Delta),
+ *   dQ' = scale dS K', dK' = scale dS^T Q', then the RoPE/RMSNorm backward.
+ * dwq/dwk [D] receive the sums over the listed heads only.
+ * Returns 0, or -1 when a work buffer cannot be allocated. */
+int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
+               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+               const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
+               double* dwk) {
+  double* qp = malloc(sizeof(double) * (size_t)Sq * D);
+  double* kp = malloc(sizeof(double) * (size_t)Skv * D);
+  double* vh = malloc(sizeof(double) * (size_t)Skv * D);
+  double* doh = malloc(sizeof(double) * (size_t)Sq * D);
+  double* rq = malloc(sizeof(double) * (size_t)Sq);
+  double* rk = malloc(sizeof(double) * (size_t)Skv);
+  double* lse = malloc(sizeof(double) * (size_t)Sq);
+  double* P = malloc(sizeof(double) * (size_t)Sq * Skv);
+  double* dS = malloc(sizeof(double) * (size_t)Sq * Skv);
+  double* dvh = malloc(sizeof(double) * (size_t)Skv * D);
+  double* gq = malloc(sizeof(double) * (size_t)Sq * D);
+  double* gk = malloc(sizeof(double) * (size_t)Skv * D);
+  int rc = 0;
+  if (!qp || !kp || !vh || !doh || !rq || !rk || !lse || !P || !dS || !dvh || !gq || !gk) { rc = -1; goto done; }
+  for (int d = 0; d < D; ++d) { dwq[d] = 0.0; dwk[d] = 0.0; }
+  const int n = bh ? n_bh : B * H;
+  for (int t = 0; t < n; ++t) {
+    const int idx = bh ? bh[t] : t;
+    const int b = idx / H, h = idx % H;
+    const double* pq = phi_q + (int64_t)(bpq > 1 ? b : 0) * Sq * (D / 2);
+    const double* pk = phi_k + (int64_t)(bpk > 1 ? b : 0) * Skv * (D / 2);
+    transform_head(q, Sq, H, D, b, h, wq, eps, pq, qp, rq);
+    transform_head(k, Skv, H, D, b, h, wk, eps, pk, kp, rk);
+    gather_head(v, Skv, H, D, b, h, vh);
+    gather_head(dout, Sq, H, D, b, h, doh);
+    head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P, lse);
+    /* dV = P^T dO */
+    mat_atb(P, Sq, Skv, doh, D, dvh);
+    scatter_head(dvh, Skv, H, D, b, h, dv);
+    /* dP = dO V^T, Delta, dS = P (dP - Delta) */
+#pragma omp parallel for schedule(static)
+    for (int i = 0; i < Sq; ++i) {
+      double delta = 0.0;
+      for (int j = 0; j < Skv; ++j) {
+        double dp = 0.0;
+        for (int d = 0; d < D; ++d) dp += doh[(int64_t)i * D + d] * vh[(int64_t)j * D + d];
+        dS[(int64_t)i * Skv + j] = dp;
+        delta += P[(int64_t)i * Skv + j] * dp;
+      }
+      for (int j = 0; j < Skv; ++j) {
+        const int64_t ij = (int64_t)i * Skv + j;
+        dS[ij] = P[ij] * (dS[ij] - delta);
+      }
+    }
+    /* dQ' = scale dS K', dK' = scale dS^T Q' */
+    mat_ab(dS, Sq, Skv, kp, D, gq);
+    mat_atb(dS, Sq, Skv, qp, D, gk);
+    for (int64_t e = 0; e < (int64_t)Sq * D; ++e) gq[e] *= scale;
+    for (int64_t e = 0; e < (int64_t)Skv * D; ++e) gk[e] *= scale;
+    transform_head_bwd(gq, q, Sq, H, D, b, h, wq, pq, rq, dq, dwq);
+    transform_head_bwd(gk, k, Skv, H, D, b, h, wk, pk, rk, dk, dwk);
+  }
+done:
+  free(qp); free(kp); free(vh); free(doh); free(rq); free(rk); free(lse);
+  free(P); free(dS); free(dvh); free(gq); free(gk);
+  return rc;
+}
