@@ -1,0 +1,459 @@
+"""Benchmark of the fused QK-RMSNorm + multi-axis RoPE + attention call.
+
+One step = the whole hot path over one batch: st_rope_attn_fwd (rotary table,
+mask tile classes, forward attention) followed by st_rope_attn_bwd (table,
+mask classes, Delta, backward attention, dq post-pass, norm-weight gradient
+reduction). Default workload: Flux1 1024px, B=1 H=24 S=4608 D=128 bf16, 3-axis
+RoPE (16,56,56) theta 1e4, all-True bool mask [1,1,1,4608], forward+backward.
+
+Metric: TFLOP/s with nominal FLOPs 4*B*H*S_q*S_kv*D forward (halved when
+causal) and 2.5x that backward. L2 (129 MB) is flushed by writing a 256 MB
+buffer before every timed step, outside the timed events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 oracle on the host cores
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+path shards over independent (b, h) heads; there is no exchange step), the
+timed region is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "fused norm+RoPE+attention fwd/bwd TFLOP/s and % of GB300 dense BF16 peak"
+DENSE_BF16_PEAK_TFLOPS = 2250.0
+FLUSH_BYTES = 256 << 20
+
+
+def nominal_flops(inp):
+    B, Sq, H, D = inp.q.shape
+    Skv = inp.k.shape[1]
+    f = 4.0 * B * H * Sq * Skv * D
+    if inp.causal:
+        f *= 0.5
+    return f, 2.5 * f
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def describe(name, inp):
+    B, Sq, H, D = inp.q.shape
+    m = "none" if inp.mask is None else f"{inp.mask.dtype} mask {list(inp.mask.shape)}"
+    if inp.meta.get("mask_per_head"):
+        m = f"fp32 additive mask [{B},{H},{Sq},{inp.k.shape[1]}]"
+    return (f"{name} fwd+bwd: B={B} H={H} S_q={Sq} S_kv={inp.k.shape[1]} D={D} q/k {str(inp.q.dtype)[6:]} "
+            f"v {str(inp.v.dtype)[6:]}, RoPE axes {list(inp.axes)} theta {inp.theta:g}, {m}, causal={inp.causal}")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_traffic(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
+    was captured from the current kernel source (matching hash)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "qk_norm_rope_gb300", "csrc", f"st_{kernel}.cu")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for ln in open(path):
+            f = ln.split()
+            if len(f) >= 4 and f[0] == kernel and f[1] == h:
+                return float(f[2]), f[3]
+    except OSError:
+        pass
+    return None, None
+
+
+def run_ours(args, rank, world, dev):
+    from qk_norm_rope_gb300 import api
+
+    inp = wl.make(args.workload)
+    B, Sq, H, D = inp.q.shape
+    f_fwd, f_bwd = nominal_flops(inp)
+    step_flops = f_fwd + f_bwd
+    g = lambda t: None if t is None else t.to(dev)
+    q, k, v, do, wq, wk, ids = (g(t) for t in (inp.q, inp.k, inp.v, inp.do, inp.wq, inp.wk, inp.ids))
+    mask = g(inp.mask)
+    if inp.meta.get("mask_per_head"):
+        mask = torch.empty(B, H, Sq, inp.k.shape[1], dtype=torch.float32, device=dev)
+        for b in range(B):
+            for h in range(H):
+                mask[b, h].copy_(wl.additive_mask_head(args.workload, b, h))
+    o = torch.empty(B, Sq, H, D, dtype=v.dtype, device=dev)
+    lse = torch.empty(B, H, Sq, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dwq, dwk = torch.empty_like(wq), torch.empty_like(wk)
+    ws_f = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal),
+                       dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal,
+                                                       for_backward=True), dtype=torch.uint8, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step(q=q, k=k, v=v, do=do, wq=wq, wk=wk, ids=ids, mask=mask):
+        api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal,
+                             o=o, lse=lse, workspace=ws_f)
+        api.st_rope_attn_bwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o, lse, do, mask=mask,
+                             causal=inp.causal, workspace=ws_b, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    def timed(n, fn):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            fn()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    for _ in range(args.warmup):
+        step()
+    api.st_check_status()
+
+    # ---- timed region (device time, L2 flushed before every step)
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[torch.cuda.current_device()] if vis else torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.2)
+    barrier()
+    launches0 = api.st_get_stats()["kernel_launches"]
+    ms = timed(args.steps, step)
+    launches = api.st_get_stats()["kernel_launches"] - launches0
+    barrier()
+    clk = clocks.stop()
+    api.st_check_status()
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_max = float(t.item())
+    ms_per_step = ms_max / args.steps
+    value = world * step_flops * args.steps / (ms_max * 1e-3) / 1e12
+
+    # ---- per-kernel device time (events on the launching stream, inside the library)
+    api.st_timing_enable(True)
+    api.st_timing_read()
+    timed(args.steps, step)
+    kt = api.st_timing_read()
+    api.st_timing_enable(False)
+    per_kernel = {n: {"launches": c, "avg_us": (m / c * 1e3 if c else None), "share": None} for n, (c, m) in kt.items()}
+    tot = sum(m for _, m in kt.values()) or 1.0
+    for n, (c, m) in kt.items():
+        per_kernel[n]["share"] = round(m / tot, 4)
+    dominant = max(kt, key=lambda n: kt[n][1])
+    peaks = measured_peaks()
+    kflops = {"fwd": f_fwd, "bwd": f_bwd}
+    roof = None
+    if dominant in kflops and kt[dominant][0]:
+        avg_s = kt[dominant][1] / kt[dominant][0] * 1e-3
+        achieved = kflops[dominant] / avg_s / 1e12
+        traffic, _ = load_traffic(dominant)
+        roof = {"kernel": f"st_{dominant}", "bound": "tensor", "achieved": round(achieved, 2),
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+                "peak_source": f"{peaks['source']} bf16 burst (cuBLAS 8192^3)", "traffic": traffic,
+                "frac_of_dense_2250": round(achieved / DENSE_BF16_PEAK_TFLOPS, 4)}
+    fwd_us = per_kernel["fwd"]["avg_us"]
+    bwd_us = per_kernel["bwd"]["avg_us"]
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda t: None if t is None else t.cpu().pin_memory()
+        hq, hk, hv, hdo, hwq, hwk, hids = (pin(t) for t in (q, k, v, do, wq, wk, ids))
+        hmask = pin(mask) if (mask is not None and mask.numel() * mask.element_size() < (1 << 30)) else None
+        dmask = mask if hmask is None else torch.empty_like(mask)
+        dbuf = [torch.empty_like(t) for t in (q, k, v, do, wq, wk, ids)]
+        outs = [o, lse, dq, dk, dv, dwq, dwk]
+        houts = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo, hwq, hwk, hids))
+        if hmask is not None:
+            h2d += hmask.numel() * hmask.element_size()
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+
+        def e2e_step():
+            for dst, src in zip(dbuf, (hq, hk, hv, hdo, hwq, hwk, hids)):
+                dst.copy_(src, non_blocking=True)
+            if hmask is not None:
+                dmask.copy_(hmask, non_blocking=True)
+            step(*dbuf, mask=dmask)
+            for dst, src in zip(houts, outs):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 20))
+        ms_e = timed(n_e2e, e2e_step)
+        te = torch.tensor([ms_e], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": round(world * step_flops * n_e2e / (float(te.item()) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+               "ms_per_step": round(float(te.item()) / n_e2e, 4)}
+        if hmask is None and mask is not None:
+            e2e["note"] = "mask stays resident on the device (over 1 GB)"
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(inp, args.workload, budget_s=args.cpu_seconds)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) inputs, norm weights 1+N(0,0.1))",
+        "config": {"workload": describe(args.workload, inp), "global_batch": B * world, "seq_len": Sq,
+                   "heads": H, "head_dim": D, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed (256 MB write) before every timed step",
+                   "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd},
+        "pct_of_dense_bf16_peak": round(100 * value / world / DENSE_BF16_PEAK_TFLOPS, 2),
+        "pct_of_measured_bf16": round(100 * value / world / peaks["bf16_tflops"], 2),
+        "fwd_tflops": round(f_fwd / (fwd_us * 1e-6) / 1e12, 2) if fwd_us else None,
+        "bwd_tflops": round(f_bwd / (bwd_us * 1e-6) / 1e12, 2) if bwd_us else None,
+        "roofline": roof, "kernels": per_kernel, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def oracle_step_flops(Sq_rows, Skv, D, causal=False):
+    f = 4.0 * Sq_rows * Skv * D
+    if causal:
+        f *= 0.5
+    return 3.5 * f
+
+
+def oracle_sample(inp, b, h, r0, rows, mask_head=None):
+    """The oracle's fwd+bwd on head (b, h), query rows [r0, r0+rows), all keys."""
+    import oracle
+    f64 = lambda t: t.double().numpy()
+    sl_q = lambda t: f64(t[b:b + 1, r0:r0 + rows, h:h + 1])
+    sl_k = lambda t: f64(t[b:b + 1, :, h:h + 1])
+    ids = inp.ids[min(b, inp.ids.shape[0] - 1):][:1]
+    m = None
+    if mask_head is not None:
+        m = mask_head[r0:r0 + rows].double().numpy()[None, None]
+    elif inp.mask is not None:
+        mm = inp.mask[min(b, inp.mask.shape[0] - 1):][:1][:, min(h, inp.mask.shape[1] - 1):][:, :1]
+        if mm.shape[2] > 1:
+            mm = mm[:, :, r0:r0 + rows]
+        m = mm.numpy() if mm.dtype == torch.bool else mm.double().numpy()
+    args = (sl_q(inp.q), sl_k(inp.k), sl_k(inp.v), f64(inp.wq), f64(inp.wk), inp.eps,
+            ids[:, r0:r0 + rows].numpy(), inp.axes, inp.theta)
+    kw = dict(mask=m, causal=False, ids_k=ids.numpy())
+    oracle.fwd(*args, **kw)
+    oracle.bwd(*args, sl_q(inp.do), **kw)
+
+
+def cpu_baseline(inp, name, budget_s=15.0):
+    """The fp64 oracle, as it stands, on the host cores: whole heads of the
+    workload (all query rows, all keys), forward + backward, until the time
+    budget is used (at least one head)."""
+    import oracle
+    oracle.build()
+    B, Sq, H, D = inp.q.shape
+    Skv = inp.k.shape[1]
+    if inp.causal:
+        return {"value": None, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": "skipped: causal sample needs whole heads; see --impl reference"}
+    t0 = time.time()
+    heads = 0
+    while True:
+        b, h = divmod(heads, H)
+        mh = wl.additive_mask_head(name, b, h) if inp.meta.get("mask_per_head") else None
+        oracle_sample(inp, b % B, h, 0, Sq, mh)
+        heads += 1
+        if time.time() - t0 >= budget_s or heads >= B * H:
+            break
+    dt = time.time() - t0
+    fl = heads * oracle_step_flops(Sq, Skv, D)
+    return {"value": round(fl / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{heads} whole head(s) of {name} (fwd+bwd, S_q={Sq}, S_kv={Skv}) in {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    """The oracle (plain fp64 C + OpenMP) timed on the host cores on this
+    workload: every step is a bounded sample of it, the fwd+bwd of one head
+    restricted to a block of query rows against all keys, sized so that the
+    whole run stays within a few minutes."""
+    import oracle
+    oracle.build()
+    inp = wl.make(args.workload)
+    B, Sq, H, D = inp.q.shape
+    Skv = inp.k.shape[1]
+    causal = inp.causal
+    target = max(0.3, min(3.0, 150.0 / (args.steps + args.warmup)))
+    # calibrate the query-row block on one small sample
+    rows = min(Sq, 128)
+    t0 = time.time()
+    oracle_sample(inp, 0, 0, 0, rows)
+    per_row = (time.time() - t0) / rows
+    if not causal:
+        rows = int(max(64, min(Sq, target / max(per_row, 1e-9))) // 64 * 64) or min(Sq, 64)
+    else:
+        rows = Sq
+    mask_cache = {}
+
+    def one(i):
+        b, h = divmod(i % (B * H), H)
+        r0 = 0 if causal else ((i * rows) % max(1, Sq - rows + 1))
+        mh = None
+        if inp.meta.get("mask_per_head"):
+            if (b, h) not in mask_cache:
+                mask_cache.clear()
+                mask_cache[(b, h)] = wl.additive_mask_head(args.workload, b, h)
+            mh = mask_cache[(b, h)]
+        if causal:
+            import oracle as orc
+            f64 = lambda t: t.double().numpy()
+            sl = lambda t: f64(t[b:b + 1, :, h:h + 1])
+            a = (sl(inp.q), sl(inp.k), sl(inp.v), f64(inp.wq), f64(inp.wk), inp.eps, inp.ids.numpy(), inp.axes,
+                 inp.theta)
+            orc.fwd(*a, causal=True)
+            orc.bwd(*a, sl(inp.do), causal=True)
+        else:
+            oracle_sample(inp, b, h, r0, rows, mh)
+
+    for i in range(args.warmup):
+        one(i)
+    t0 = time.time()
+    for i in range(args.steps):
+        one(args.warmup + i)
+    dt = time.time() - t0
+    fl = oracle_step_flops(rows, Skv, D, causal) * args.steps
+    value = fl / dt / 1e12
+    sample = (f"each step: oracle fwd+bwd of one (b,h) head of {args.workload}, "
+              + ("all rows (causal)" if causal else f"{rows} query rows x {Skv} keys"))
+    return {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(args.workload, inp), "global_batch": B, "seq_len": Sq, "heads": H,
+                   "head_dim": D, "parallelism": "host cores (OpenMP)"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="flux1_1024", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    line = run_ours(args, rank, world, dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,645 @@
+// C-ABI host layer: argument validation, workspace planning, kernel launches
+// and the dispatch counters. Nothing here allocates device memory or
+// synchronises a stream, except st_get_stats and st_check_status.
+#include <atomic>
+#include <mutex>
+#include <vector>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+
+#include "../../include/st_rope_attn.h"
+#include "st_aux.h"
+#include "st_kernels.h"
+
+namespace st {
+__device__ unsigned g_status = 0;
+__device__ unsigned long long g_counters[kNumCounters];
+}  // namespace st
+
+namespace {
+
+using namespace st;
+
+thread_local std::string t_err;
+std::atomic<uint64_t> h_fwd_calls{0}, h_bwd_calls{0}, h_mixed{0}, h_launches{0};
+
+// ---- optional per-kernel event timing (measurement only)
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_tmu;
+std::atomic<bool> g_timing{false};
+std::vector<TimedLaunch> g_pending;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launches one kernel through `fn`, counting it and, when timing is on,
+// bracketing it with events on its stream.
+template <class F>
+cudaError_t launch_counted(int kind, cudaStream_t stream, F&& fn) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (g_timing.load(std::memory_order_relaxed)) {
+    std::lock_guard<std::mutex> lk(g_tmu);
+    a = take_event();
+    b = take_event();
+    if (a) cudaEventRecord(a, stream);
+  }
+  cudaError_t e = fn();
+  if (e == cudaSuccess) ++h_launches;
+  if (a && b) {
+    cudaEventRecord(b, stream);
+    std::lock_guard<std::mutex> lk(g_tmu);
+    g_pending.push_back({kind, a, b});
+  }
+  return e;
+}
+
+st_status fail(st_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return s;
+}
+
+int elem_bytes(int dt) {
+  switch (dt) {
+    case ST_BF16: case ST_F16: return 2;
+    case ST_F32: case ST_I32: return 4;
+    case ST_BOOL: return 1;
+    default: return 0;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long wait_budget() {
+  static long long v = [] {
+    const char* e = std::getenv("ST_WAIT_BUDGET");
+    long long b = e ? std::atoll(e) : 0;
+    return b > 0 ? b : (1ll << 31);  // ~1 s of clock64 at GB300 clocks
+  }();
+  return v;
+}
+
+struct Dev {
+  unsigned* status = nullptr;
+  unsigned long long* counters = nullptr;
+};
+
+st_status device_globals(Dev* d) {
+  static Dev cache[64];
+  static std::atomic<bool> ready[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return fail(ST_ERR_CUDA, "cudaGetDevice failed");
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    Dev v;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&v.status), g_status) != cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void**>(&v.counters), g_counters) != cudaSuccess)
+      return fail(ST_ERR_CUDA, "cudaGetSymbolAddress failed: %s", cudaGetErrorString(cudaGetLastError()));
+    cache[dev] = v;
+    ready[dev].store(true, std::memory_order_release);
+  }
+  *d = cache[dev];
+  return ST_OK;
+}
+
+// ------------------------------------------------------------- validation
+struct Shape {
+  int B = 0, Sq = 0, Skv = 0, H = 0, D = 0;
+};
+
+st_status check_bshd(const st_tensor* t, const char* name, int B, int S, int H, int D, int dt_a, int dt_b,
+                     RowTensor* out) {
+  if (!t) return fail(ST_ERR_INVALID_ARG, "%s is NULL", name);
+  if (t->ndim != 4) return fail(ST_ERR_SHAPE, "%s must be 4-D [B,S,H,D], got ndim=%d", name, t->ndim);
+  if (t->shape[0] != B || t->shape[1] != S || t->shape[2] != H || t->shape[3] != D)
+    return fail(ST_ERR_SHAPE, "%s has shape [%lld,%lld,%lld,%lld], expected [%d,%d,%d,%d]", name,
+                (long long)t->shape[0], (long long)t->shape[1], (long long)t->shape[2], (long long)t->shape[3], B,
+                S, H, D);
+  if (t->dtype != dt_a && t->dtype != dt_b) return fail(ST_ERR_DTYPE, "%s has unsupported dtype %d", name, t->dtype);
+  const int64_t n = (int64_t)B * S * H;
+  if (n > 0) {
+    if (!t->data) return fail(ST_ERR_INVALID_ARG, "%s data is NULL", name);
+    const int eb = elem_bytes(t->dtype);
+    if (t->stride[3] != 1) return fail(ST_ERR_ALIGN, "%s must have unit stride on D", name);
+    if (!aligned16(t->data)) return fail(ST_ERR_ALIGN, "%s data pointer is not 16-byte aligned", name);
+    for (int a = 0; a < 3; ++a)
+      if (t->shape[a] > 1 && ((t->stride[a] * eb) % 16) != 0)
+        return fail(ST_ERR_ALIGN, "%s stride[%d]=%lld elements is not a multiple of 16 bytes", name, a,
+                    (long long)t->stride[a]);
+  }
+  if (out) {
+    out->p = t->data;
+    out->sb = t->shape[0] > 1 ? t->stride[0] : 0;
+    out->ss = t->shape[1] > 1 ? t->stride[1] : 0;
+    out->sh = t->shape[2] > 1 ? t->stride[2] : 0;
+    out->is_f32 = t->dtype == ST_F32;
+  }
+  return ST_OK;
+}
+
+st_status check_vec(const st_tensor* t, const char* name, int D) {
+  if (!t || !t->data) return fail(ST_ERR_INVALID_ARG, "%s is NULL", name);
+  if (t->ndim != 1 || t->shape[0] != D) return fail(ST_ERR_SHAPE, "%s must be [%d]", name, D);
+  if (t->dtype != ST_F32) return fail(ST_ERR_DTYPE, "%s must be fp32", name);
+  if (t->stride[0] != 1) return fail(ST_ERR_ALIGN, "%s must be contiguous", name);
+  if (!aligned16(t->data)) return fail(ST_ERR_ALIGN, "%s data pointer is not 16-byte aligned", name);
+  return ST_OK;
+}
+
+struct Ids {
+  const st_tensor* t;
+  int Bt, S;
+};
+
+st_status check_ids(const st_tensor* t, const char* name, int B, int S, int n_axes, Ids* out) {
+  if (!t || (!t->data && S > 0)) return fail(ST_ERR_INVALID_ARG, "%s is NULL", name);
+  if (t->ndim != 3) return fail(ST_ERR_SHAPE, "%s must be 3-D [B|1, S, n_axes]", name);
+  if (!(t->shape[0] == 1 || t->shape[0] == B) || t->shape[1] != S || t->shape[2] != n_axes)
+    return fail(ST_ERR_SHAPE, "%s has shape [%lld,%lld,%lld], expected [%d|1,%d,%d]", name, (long long)t->shape[0],
+                (long long)t->shape[1], (long long)t->shape[2], B, S, n_axes);
+  if (t->dtype != ST_I32 && t->dtype != ST_F32) return fail(ST_ERR_DTYPE, "%s must be int32 or fp32", name);
+  out->t = t;
+  out->Bt = static_cast<int>(t->shape[0]);
+  out->S = S;
+  return ST_OK;
+}
+
+struct Plan {
+  Shape sh;
+  RowTensor q, k, v;
+  Ids ids_q{}, ids_k{};
+  bool separate_k_table = false;
+  int mask_kind = kMaskNone;
+  int Bm = 1, Hm = 1, Sqm = 1;
+  int64_t m_sb = 0, m_sh = 0, m_sq = 0;
+  int nQt = 0, nKt = 0, nQtm = 1;
+  // workspace offsets
+  size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
+         off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
+  int n_dwq = 0, n_dwk = 0;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* mask, int causal,
+                    const st_rope* rope, int for_backward, Plan* P) {
+  if (!q || !k || !v) return fail(ST_ERR_INVALID_ARG, "q, k and v must not be NULL");
+  if (q->ndim != 4 || k->ndim != 4) return fail(ST_ERR_SHAPE, "q and k must be 4-D [B,S,H,D]");
+  Shape s;
+  s.B = static_cast<int>(q->shape[0]);
+  s.Sq = static_cast<int>(q->shape[1]);
+  s.H = static_cast<int>(q->shape[2]);
+  s.D = static_cast<int>(q->shape[3]);
+  s.Skv = static_cast<int>(k->shape[1]);
+  if (q->shape[0] < 0 || q->shape[1] < 0 || q->shape[2] < 0 || k->shape[1] < 0 || q->shape[1] > (1ll << 30) ||
+      k->shape[1] > (1ll << 30) || q->shape[0] > 65535 || q->shape[2] > 65535)
+    return fail(ST_ERR_SHAPE, "sizes out of range");
+  if (s.D != kD) return fail(ST_ERR_UNSUPPORTED, "head dimension %d is not supported (this build handles D=128)", s.D);
+  st_status st;
+  if ((st = check_bshd(q, "q", s.B, s.Sq, s.H, s.D, ST_BF16, ST_F32, &P->q)) != ST_OK) return st;
+  if ((st = check_bshd(k, "k", s.B, s.Skv, s.H, s.D, ST_BF16, ST_F32, &P->k)) != ST_OK) return st;
+  if ((st = check_bshd(v, "v", s.B, s.Skv, s.H, s.D, ST_BF16, ST_BF16, &P->v)) != ST_OK) return st;
+  if (!rope) return fail(ST_ERR_INVALID_ARG, "rope is NULL");
+  if (rope->n_axes < 1 || rope->n_axes > 8) return fail(ST_ERR_INVALID_ARG, "rope.n_axes must be 1..8");
+  int dsum = 0;
+  for (int a = 0; a < rope->n_axes; ++a) {
+    if (rope->axes_dim[a] <= 0 || (rope->axes_dim[a] & 1))
+      return fail(ST_ERR_INVALID_ARG, "rope.axes_dim[%d]=%d must be positive and even", a, rope->axes_dim[a]);
+    dsum += rope->axes_dim[a];
+  }
+  if (dsum != s.D) return fail(ST_ERR_INVALID_ARG, "rope axes sum to %d, expected D=%d", dsum, s.D);
+  if (!(rope->theta > 0.0) || !std::isfinite(rope->theta)) return fail(ST_ERR_INVALID_ARG, "rope.theta must be > 0");
+  if ((st = check_ids(rope->ids, "rope.ids", s.B, s.Sq, rope->n_axes, &P->ids_q)) != ST_OK) return st;
+  if (rope->ids_k) {
+    if ((st = check_ids(rope->ids_k, "rope.ids_k", s.B, s.Skv, rope->n_axes, &P->ids_k)) != ST_OK) return st;
+    P->separate_k_table = true;
+  } else {
+    if (s.Sq != s.Skv) return fail(ST_ERR_INVALID_ARG, "rope.ids_k is required when S_q != S_kv");
+    P->ids_k = P->ids_q;
+  }
+  if (mask && causal) return fail(ST_ERR_INVALID_ARG, "mask and causal cannot be combined");
+  if (mask) {
+    if (mask->ndim != 4) return fail(ST_ERR_SHAPE, "mask must be 4-D [B|1,H|1,S_q|1,S_kv]");
+    const int64_t want[4] = {s.B, s.H, s.Sq, s.Skv};
+    for (int a = 0; a < 3; ++a)
+      if (!(mask->shape[a] == 1 || mask->shape[a] == want[a]))
+        return fail(ST_ERR_SHAPE, "mask dim %d is %lld, expected 1 or %lld", a, (long long)mask->shape[a],
+                    (long long)want[a]);
+    if (mask->shape[3] != s.Skv) return fail(ST_ERR_SHAPE, "mask last dim must equal S_kv=%d", s.Skv);
+    if (mask->dtype == ST_BOOL) P->mask_kind = kMaskBool;
+    else if (mask->dtype == ST_F32) P->mask_kind = kMaskF32;
+    else if (mask->dtype == ST_BF16) P->mask_kind = kMaskBF16;
+    else return fail(ST_ERR_DTYPE, "mask must be bool, fp32 or bf16");
+    if (s.Skv > 1 && mask->stride[3] != 1) return fail(ST_ERR_ALIGN, "mask must have unit stride on S_kv");
+    if (!mask->data && (int64_t)s.B * s.H * s.Sq * s.Skv > 0) return fail(ST_ERR_INVALID_ARG, "mask data is NULL");
+    P->Bm = static_cast<int>(mask->shape[0]);
+    P->Hm = static_cast<int>(mask->shape[1]);
+    P->Sqm = static_cast<int>(mask->shape[2]);
+    P->m_sb = P->Bm > 1 ? mask->stride[0] : 0;
+    P->m_sh = P->Hm > 1 ? mask->stride[1] : 0;
+    P->m_sq = P->Sqm > 1 ? mask->stride[2] : 0;
+  }
+  P->sh = s;
+  P->nQt = (s.Sq + kTile - 1) / kTile;
+  P->nKt = (s.Skv + kTile - 1) / kTile;
+  P->nQtm = P->Sqm > 1 ? P->nQt : 1;
+
+  size_t off = 0;
+  P->off_ctrl = off;
+  off += 256;
+  P->off_tab_q = off;
+  off = align_up(off + (size_t)P->ids_q.Bt * s.Sq * kPairs * sizeof(float2), 256);
+  P->off_tab_k = P->off_tab_q;
+  if (P->separate_k_table) {
+    P->off_tab_k = off;
+    off = align_up(off + (size_t)P->ids_k.Bt * s.Skv * kPairs * sizeof(float2), 256);
+  }
+  if (P->mask_kind == kMaskBool) {
+    P->off_flags = off;
+    off = align_up(off + (size_t)P->Bm * P->Hm * P->nQtm * P->nKt, 256);
+  }
+  if (for_backward) {
+    P->off_delta = off;
+    off = align_up(off + (size_t)s.B * s.H * s.Sq * sizeof(float), 256);
+    P->off_dqacc = off;
+    off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * sizeof(float), 256);
+    P->n_dwk = s.B * s.H * P->nKt;
+    P->off_dwk = off;
+    off = align_up(off + (size_t)P->n_dwk * kD * sizeof(float), 256);
+    P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kTile - 1) / kTile);
+    P->off_dwq = off;
+    off = align_up(off + (size_t)P->n_dwq * kD * sizeof(float), 256);
+    P->off_dwscratch = off;
+    off = align_up(off + (size_t)2 * dw_reduce_blocks(P->n_dwq, P->n_dwk) * kD * sizeof(float), 256);
+  }
+  P->total = off;
+  return ST_OK;
+}
+
+void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float eps, int causal, float scale,
+                 uint8_t* ws, const Dev& dev, Common* c) {
+  memset(c, 0, sizeof(*c));
+  c->q = P.q;
+  c->k = P.k;
+  c->v = P.v;
+  c->wq = static_cast<const float*>(qw->data);
+  c->wk = static_cast<const float*>(kw->data);
+  c->eps = eps;
+  c->tab_q = reinterpret_cast<const float2*>(ws + P.off_tab_q);
+  c->tab_k = reinterpret_cast<const float2*>(ws + P.off_tab_k);
+  c->tab_q_sb = P.ids_q.Bt > 1 ? (int64_t)P.sh.Sq * kPairs : 0;
+  c->tab_k_sb = P.ids_k.Bt > 1 ? (int64_t)P.sh.Skv * kPairs : 0;
+  c->mask_kind = P.mask_kind;
+  c->m_sb = P.m_sb;
+  c->m_sh = P.m_sh;
+  c->m_sq = P.m_sq;
+  if (P.mask_kind == kMaskBool) {
+    c->flags = ws + P.off_flags;
+    c->f_sb = P.Bm > 1 ? (int64_t)P.Hm * P.nQtm * P.nKt : 0;
+    c->f_sh = P.Hm > 1 ? (int64_t)P.nQtm * P.nKt : 0;
+    c->f_sq = P.nQtm > 1 ? P.nKt : 0;
+  }
+  c->causal = causal ? 1 : 0;
+  const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(kD));
+  c->scale = sc;
+  c->scale_log2 = sc * kLog2e;
+  c->B = P.sh.B;
+  c->H = P.sh.H;
+  c->Sq = P.sh.Sq;
+  c->Skv = P.sh.Skv;
+  c->nQt = P.nQt;
+  c->nKt = P.nKt;
+  c->status = dev.status;
+  c->counters = dev.counters;
+  c->wait_budget = wait_budget();
+}
+
+void fill_table(const Ids& ids, const st_rope* rope, float2* out, unsigned* ctrl, TableParams* t) {
+  memset(t, 0, sizeof(*t));
+  t->ids = ids.t->data;
+  t->ids_f32 = ids.t->dtype == ST_F32;
+  t->i_sb = ids.t->stride[0];
+  t->i_ss = ids.t->stride[1];
+  t->i_sa = ids.t->stride[2];
+  t->Bt = ids.Bt;
+  t->S = ids.S;
+  int pair = 0;
+  for (int a = 0; a < rope->n_axes; ++a) {
+    const int da = rope->axes_dim[a];
+    for (int j = 0; j < da / 2; ++j, ++pair) {
+      t->omega[pair] = std::pow(rope->theta, -2.0 * j / static_cast<double>(da));
+      t->axis_of[pair] = a;
+    }
+  }
+  t->out = out;
+  t->ctrl = ctrl;
+}
+
+st_status cuda_check(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(ST_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return ST_OK;
+}
+
+// Rotary tables and mask tile classes: the first launches of a call.
+st_status launch_prelude(const Plan& P, const st_rope* rope, const st_tensor* mask, uint8_t* ws, const Dev& dev,
+                         cudaStream_t stream) {
+  unsigned* ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
+  TableParams t;
+  fill_table(P.ids_q, rope, reinterpret_cast<float2*>(ws + P.off_tab_q), ctrl, &t);
+  st_status st = cuda_check(launch_counted(ST_K_TABLE, stream, [&] { return launch_table(t, stream); }), "table kernel launch");
+  if (st != ST_OK) return st;
+  if (P.separate_k_table) {
+    fill_table(P.ids_k, rope, reinterpret_cast<float2*>(ws + P.off_tab_k), nullptr, &t);
+    if ((st = cuda_check(launch_counted(ST_K_TABLE, stream, [&] { return launch_table(t, stream); }), "table kernel launch")) != ST_OK) return st;
+  }
+  if (P.mask_kind == kMaskBool && P.nKt > 0 && P.nQt > 0) {
+    ClassifyParams cp;
+    memset(&cp, 0, sizeof(cp));
+    cp.mask = static_cast<const uint8_t*>(mask->data);
+    cp.m_sb = P.m_sb;
+    cp.m_sh = P.m_sh;
+    cp.m_sq = P.m_sq;
+    cp.Bm = P.Bm;
+    cp.Hm = P.Hm;
+    cp.Sqm = P.Sqm > 1 ? P.sh.Sq : 1;
+    cp.Skv = P.sh.Skv;
+    cp.nQtm = P.nQtm;
+    cp.nKt = P.nKt;
+    cp.flags = ws + P.off_flags;
+    cp.ctrl = ctrl;
+    cp.counters = dev.counters;
+    if ((st = cuda_check(launch_counted(ST_K_CLASSIFY, stream, [&] { return launch_classify(cp, stream); }), "mask classify launch")) != ST_OK) return st;
+  }
+  return ST_OK;
+}
+
+st_status check_workspace(const Plan& P, void* ws, size_t bytes) {
+  if (bytes < P.total) return fail(ST_ERR_WORKSPACE, "workspace of %zu bytes is smaller than the %zu required", bytes, P.total);
+  if (P.total > 0 && !ws) return fail(ST_ERR_WORKSPACE, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return fail(ST_ERR_ALIGN, "workspace must be 256-byte aligned");
+  return ST_OK;
+}
+
+st_status check_out(const st_tensor* t, const char* name, int B, int S, int H, int dtype, RowTensor* rt) {
+  return check_bshd(t, name, B, S, H, kD, dtype, dtype, rt);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k, const st_tensor* v,
+                                   const st_tensor* mask, int causal, const st_rope* rope, int for_backward) {
+  Plan P;
+  if (plan_call(q, k, v, mask, causal, rope, for_backward, &P) != ST_OK) return 0;
+  return P.total;
+}
+
+st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* q_norm_w,
+                           const st_tensor* k_norm_w, float eps, const st_rope* rope, const st_tensor* mask,
+                           int causal, float scale, st_tensor* o, st_tensor* lse, void* workspace,
+                           size_t workspace_bytes, void* stream_) {
+  t_err.clear();
+  Plan P;
+  st_status st = plan_call(q, k, v, mask, causal, rope, 0, &P);
+  if (st != ST_OK) return st;
+  const Shape& s = P.sh;
+  if ((st = check_vec(q_norm_w, "q_norm_w", kD)) != ST_OK) return st;
+  if ((st = check_vec(k_norm_w, "k_norm_w", kD)) != ST_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ST_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (!std::isfinite(scale)) return fail(ST_ERR_INVALID_ARG, "scale must be finite");
+  RowTensor ro;
+  if ((st = check_out(o, "o", s.B, s.Sq, s.H, v->dtype, &ro)) != ST_OK) return st;
+  if (!lse || lse->ndim != 3 || lse->shape[0] != s.B || lse->shape[1] != s.H || lse->shape[2] != s.Sq)
+    return fail(ST_ERR_SHAPE, "lse must be [B,H,S_q] = [%d,%d,%d]", s.B, s.H, s.Sq);
+  if (lse->dtype != ST_F32) return fail(ST_ERR_DTYPE, "lse must be fp32");
+  if ((int64_t)s.B * s.H * s.Sq > 0 &&
+      (!lse->data || lse->stride[2] != 1 || lse->stride[1] != s.Sq || lse->stride[0] != (int64_t)s.H * s.Sq))
+    return fail(ST_ERR_ALIGN, "lse must be contiguous");
+  if ((st = check_workspace(P, workspace, workspace_bytes)) != ST_OK) return st;
+  if ((int64_t)s.B * s.H * s.Sq == 0) {
+    ++h_fwd_calls;
+    return ST_OK;
+  }
+  Dev dev;
+  if ((st = device_globals(&dev)) != ST_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
+  fp.c.mask = mask ? mask->data : nullptr;
+  fp.o = o->data;
+  fp.o_sb = ro.sb;
+  fp.o_ss = ro.ss;
+  fp.o_sh = ro.sh;
+  fp.o_f32 = ro.is_f32;
+  fp.lse = static_cast<float*>(lse->data);
+  if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch")) != ST_OK) return st;
+  ++h_fwd_calls;
+  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  return ST_OK;
+}
+
+st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* q_norm_w,
+                           const st_tensor* k_norm_w, float eps, const st_rope* rope, const st_tensor* mask,
+                           int causal, float scale, const st_tensor* o, const st_tensor* lse, const st_tensor* d_o,
+                           st_tensor* dq, st_tensor* dk, st_tensor* dv, st_tensor* d_q_norm_w,
+                           st_tensor* d_k_norm_w, void* workspace, size_t workspace_bytes, void* stream_) {
+  t_err.clear();
+  Plan P;
+  st_status st = plan_call(q, k, v, mask, causal, rope, 1, &P);
+  if (st != ST_OK) return st;
+  const Shape& s = P.sh;
+  if ((st = check_vec(q_norm_w, "q_norm_w", kD)) != ST_OK) return st;
+  if ((st = check_vec(k_norm_w, "k_norm_w", kD)) != ST_OK) return st;
+  if ((st = check_vec(d_q_norm_w, "d_q_norm_w", kD)) != ST_OK) return st;
+  if ((st = check_vec(d_k_norm_w, "d_k_norm_w", kD)) != ST_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ST_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (!std::isfinite(scale)) return fail(ST_ERR_INVALID_ARG, "scale must be finite");
+  RowTensor ro, rdo, rdq, rdk, rdv;
+  if ((st = check_out(o, "o", s.B, s.Sq, s.H, v->dtype, &ro)) != ST_OK) return st;
+  if ((st = check_out(d_o, "d_o", s.B, s.Sq, s.H, v->dtype, &rdo)) != ST_OK) return st;
+  if ((st = check_out(dq, "dq", s.B, s.Sq, s.H, q->dtype, &rdq)) != ST_OK) return st;
+  if ((st = check_out(dk, "dk", s.B, s.Skv, s.H, k->dtype, &rdk)) != ST_OK) return st;
+  if ((st = check_out(dv, "dv", s.B, s.Skv, s.H, v->dtype, &rdv)) != ST_OK) return st;
+  if (!lse || lse->ndim != 3 || lse->shape[0] != s.B || lse->shape[1] != s.H || lse->shape[2] != s.Sq)
+    return fail(ST_ERR_SHAPE, "lse must be [B,H,S_q] = [%d,%d,%d]", s.B, s.H, s.Sq);
+  if (lse->dtype != ST_F32) return fail(ST_ERR_DTYPE, "lse must be fp32");
+  if ((int64_t)s.B * s.H * s.Sq > 0 &&
+      (!lse->data || lse->stride[2] != 1 || lse->stride[1] != s.Sq || lse->stride[0] != (int64_t)s.H * s.Sq))
+    return fail(ST_ERR_ALIGN, "lse must be contiguous");
+  if ((st = check_workspace(P, workspace, workspace_bytes)) != ST_OK) return st;
+  if ((int64_t)s.B * s.H == 0) {
+    ++h_bwd_calls;
+    return ST_OK;
+  }
+  Dev dev;
+  if ((st = device_globals(&dev)) != ST_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+
+  float* delta = reinterpret_cast<float*>(ws + P.off_delta);
+  float* dq_acc = reinterpret_cast<float*>(ws + P.off_dqacc);
+  if ((int64_t)s.B * s.Sq * s.H > 0) {
+    PreParams pp;
+    memset(&pp, 0, sizeof(pp));
+    pp.o = o->data;
+    pp.o_sb = ro.sb; pp.o_ss = ro.ss; pp.o_sh = ro.sh; pp.o_f32 = ro.is_f32;
+    pp.dout = d_o->data;
+    pp.do_sb = rdo.sb; pp.do_ss = rdo.ss; pp.do_sh = rdo.sh;
+    pp.delta = delta;
+    pp.dq_acc = dq_acc;
+    pp.B = s.B; pp.H = s.H; pp.Sq = s.Sq;
+    if ((st = cuda_check(launch_counted(ST_K_BWD_PRE, stream, [&] { return launch_bwd_pre(pp, stream); }), "backward pre launch")) != ST_OK) return st;
+  }
+  if (P.nKt > 0) {
+    BwdParams bp;
+    memset(&bp, 0, sizeof(bp));
+    fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &bp.c);
+    bp.c.mask = mask ? mask->data : nullptr;
+    bp.dout = d_o->data;
+    bp.do_sb = rdo.sb; bp.do_ss = rdo.ss; bp.do_sh = rdo.sh;
+    bp.lse = static_cast<const float*>(lse->data);
+    bp.delta = delta;
+    bp.dq_acc = dq_acc;
+    bp.dk = dk->data; bp.dk_sb = rdk.sb; bp.dk_ss = rdk.ss; bp.dk_sh = rdk.sh; bp.dk_f32 = rdk.is_f32;
+    bp.dv = dv->data; bp.dv_sb = rdv.sb; bp.dv_ss = rdv.ss; bp.dv_sh = rdv.sh; bp.dv_f32 = rdv.is_f32;
+    bp.dwk_part = reinterpret_cast<float*>(ws + P.off_dwk);
+    if ((st = cuda_check(launch_counted(ST_K_BWD, stream, [&] { return launch_bwd(bp, stream); }), "backward kernel launch")) != ST_OK) return st;
+  }
+  if ((int64_t)s.B * s.Sq * s.H > 0) {
+    PostParams pq;
+    memset(&pq, 0, sizeof(pq));
+    pq.dq_acc = dq_acc;
+    pq.q = P.q;
+    pq.tab_q = reinterpret_cast<const float2*>(ws + P.off_tab_q);
+    pq.tab_q_sb = P.ids_q.Bt > 1 ? (int64_t)s.Sq * kPairs : 0;
+    pq.wq = static_cast<const float*>(q_norm_w->data);
+    pq.eps = eps;
+    pq.dq = dq->data; pq.dq_sb = rdq.sb; pq.dq_ss = rdq.ss; pq.dq_sh = rdq.sh; pq.dq_f32 = rdq.is_f32;
+    pq.dwq_part = reinterpret_cast<float*>(ws + P.off_dwq);
+    pq.B = s.B; pq.H = s.H; pq.Sq = s.Sq;
+    if ((st = cuda_check(launch_counted(ST_K_DQ_POST, stream, [&] { return launch_dq_post(pq, stream); }), "dq post launch")) != ST_OK) return st;
+  }
+  DwParams dp;
+  memset(&dp, 0, sizeof(dp));
+  dp.dwq_part = reinterpret_cast<const float*>(ws + P.off_dwq);
+  dp.dwk_part = reinterpret_cast<const float*>(ws + P.off_dwk);
+  dp.n_q = (int64_t)s.B * s.Sq * s.H > 0 ? P.n_dwq : 0;
+  dp.n_k = P.nKt > 0 ? P.n_dwk : 0;
+  dp.scratch = reinterpret_cast<float*>(ws + P.off_dwscratch);
+  dp.ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
+  dp.dwq = static_cast<float*>(d_q_norm_w->data);
+  dp.dwk = static_cast<float*>(d_k_norm_w->data);
+  if ((st = cuda_check(launch_counted(ST_K_DW, stream, [&] { return launch_dw_reduce(dp, stream); }), "weight-gradient reduce launch")) != ST_OK) return st;
+  ++h_bwd_calls;
+  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  return ST_OK;
+}
+
+const char* st_last_error(void) { return t_err.c_str(); }
+
+st_status st_get_stats(st_stats* out) {
+  if (!out) return fail(ST_ERR_INVALID_ARG, "out is NULL");
+  memset(out, 0, sizeof(*out));
+  out->fwd_calls = h_fwd_calls.load();
+  out->bwd_calls = h_bwd_calls.load();
+  out->mixed_dtype_calls = h_mixed.load();
+  Dev dev;
+  st_status st = device_globals(&dev);
+  if (st != ST_OK) return st;
+  unsigned long long c[kNumCounters];
+  if ((st = cuda_check(cudaDeviceSynchronize(), "cudaDeviceSynchronize")) != ST_OK) return st;
+  if ((st = cuda_check(cudaMemcpy(c, dev.counters, sizeof(c), cudaMemcpyDeviceToHost), "read counters")) != ST_OK)
+    return st;
+  out->mask_all_true_skipped = c[kCtrMaskAllTrue];
+  out->tiles_skipped = c[kCtrTilesSkipped];
+  out->tiles_total = c[kCtrTilesTotal];
+  out->timeouts = c[kCtrTimeouts];
+  out->kernel_launches = h_launches.load();
+  return ST_OK;
+}
+
+st_status st_timing_enable(int on) {
+  g_timing.store(on != 0);
+  return ST_OK;
+}
+
+st_status st_timing_read(st_kernel_times* out) {
+  if (!out) return fail(ST_ERR_INVALID_ARG, "out is NULL");
+  memset(out, 0, sizeof(*out));
+  std::vector<TimedLaunch> done;
+  {
+    std::lock_guard<std::mutex> lk(g_tmu);
+    done.swap(g_pending);
+  }
+  st_status st = ST_OK;
+  for (const TimedLaunch& t : done) {
+    float ms = 0.f;
+    cudaError_t e = cudaEventSynchronize(t.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, t.a, t.b);
+    if (e != cudaSuccess && st == ST_OK) st = fail(ST_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+    if (t.kind >= 0 && t.kind < ST_K_COUNT) {
+      out->launches[t.kind] += 1;
+      out->ms[t.kind] += ms;
+    }
+  }
+  std::lock_guard<std::mutex> lk(g_tmu);
+  for (const TimedLaunch& t : done) {
+    g_event_pool.push_back(t.a);
+    g_event_pool.push_back(t.b);
+  }
+  return st;
+}
+
+void st_reset_stats(void) {
+  h_launches = 0;
+  h_fwd_calls = 0;
+  h_bwd_calls = 0;
+  h_mixed = 0;
+  Dev dev;
+  if (device_globals(&dev) != ST_OK) return;
+  unsigned long long z[kNumCounters] = {};
+  cudaDeviceSynchronize();
+  cudaMemcpy(dev.counters, z, sizeof(z), cudaMemcpyHostToDevice);
+}
+
+st_status st_check_status(void* stream_) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  st_status st = cuda_check(cudaStreamSynchronize(stream), "cudaStreamSynchronize");
+  if (st != ST_OK) return st;
+  Dev dev;
+  if ((st = device_globals(&dev)) != ST_OK) return st;
+  unsigned s = 0, z = 0;
+  if ((st = cuda_check(cudaMemcpy(&s, dev.status, sizeof(s), cudaMemcpyDeviceToHost), "read status")) != ST_OK)
+    return st;
+  if (s & kStatusTimeout) {
+    cudaMemcpy(dev.status, &z, sizeof(z), cudaMemcpyHostToDevice);
+    return fail(ST_ERR_TIMEOUT, "a kernel's bounded wait ran out");
+  }
+  return ST_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,205 @@
+// Small kernels around the two attention kernels:
+//  - rotary table:   position ids -> (cos, sin) per token and pair (fp32);
+//  - mask classify:  bool mask tiles -> {all True, all False, mixed}, plus the
+//                    "whole mask is all True" counter;
+//  - backward pre:   Delta_i = sum_d dO_id O_id, zero the fp32 dQ accumulator;
+//  - dq post:        dQ accumulator -> inverse rotation -> RMSNorm backward -> dq,
+//                    per-block partial sums of the q-norm weight gradient;
+//  - dw reduce:      fixed-order sums of the weight-gradient partials.
+#include "st_aux.h"
+
+namespace st {
+
+namespace {
+
+// (cos, sin) of id * omega_p, the angle reduced to [-pi, pi] in fp64 before
+// the fp32 sincosf so that large ids keep full fp32 accuracy.
+__global__ void table_kernel(const __grid_constant__ TableParams p) {
+  if (blockIdx.x == 0 && threadIdx.x < kCtrlWords && p.ctrl) p.ctrl[threadIdx.x] = 0u;
+  const int64_t n = (int64_t)p.Bt * p.S * kPairs;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+    const int pr = static_cast<int>(e % kPairs);
+    const int64_t tok = e / kPairs;
+    const int s = static_cast<int>(tok % p.S);
+    const int bt = static_cast<int>(tok / p.S);
+    const int a = p.axis_of[pr];
+    const int64_t off = bt * p.i_sb + (int64_t)s * p.i_ss + (int64_t)a * p.i_sa;
+    const double id = p.ids_f32 ? static_cast<double>(static_cast<const float*>(p.ids)[off])
+                                : static_cast<double>(static_cast<const int32_t*>(p.ids)[off]);
+    const double phi = id * p.omega[pr];
+    const double k = rint(phi * 0.15915494309189535);  // 1 / (2 pi)
+    const double red = fma(-k, 6.283185307179586, phi);
+    float sn, cs;
+    sincosf(static_cast<float>(red), &sn, &cs);
+    p.out[e] = make_float2(cs, sn);
+  }
+}
+
+__global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
+  const int kt = blockIdx.x, qt = blockIdx.y;
+  const int bm = blockIdx.z / p.Hm, hm = blockIdx.z % p.Hm;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rows = (p.Sqm == 1) ? 1 : min(kTile, p.Sqm - qt * kTile);
+  const int keys = min(kTile, p.Skv - kt * kTile);
+  bool any_t = false, any_f = false;
+  for (int r = warp; r < rows; r += blockDim.x / 32) {
+    const uint8_t* row = p.mask + bm * p.m_sb + hm * p.m_sh + (int64_t)(qt * kTile + r) * p.m_sq + kt * kTile;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int jj = 4 * lane + u;
+      if (jj < keys) {
+        if (__ldg(row + jj)) any_t = true; else any_f = true;
+      }
+    }
+  }
+  const int bt = __syncthreads_or(any_t);
+  const int bf = __syncthreads_or(any_f);
+  __shared__ int is_last;
+  if (threadIdx.x == 0) {
+    const uint8_t flag = !bf ? kTileAllTrue : (!bt ? kTileAllFalse : kTileMixed);
+    p.flags[((int64_t)blockIdx.z * p.nQtm + qt) * p.nKt + kt] = flag;
+    if (bf) atomicOr(p.ctrl + kCtrlAnyFalse, 1u);
+    __threadfence();
+    const unsigned total = gridDim.x * gridDim.y * gridDim.z;
+    is_last = (atomicAdd(p.ctrl + kCtrlClassifyDone, 1u) == total - 1);
+  }
+  __syncthreads();
+  if (is_last && threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.ctrl + kCtrlAnyFalse, 0u) == 0u) atomicAdd(p.counters + kCtrMaskAllTrue, 1ull);
+  }
+}
+
+// One warp per (b, i, h) row.
+__global__ void bwd_pre_kernel(const __grid_constant__ PreParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  if (row >= nrows) return;
+  const int h = static_cast<int>(row % p.H);
+  const int i = static_cast<int>((row / p.H) % p.Sq);
+  const int b = static_cast<int>(row / ((int64_t)p.H * p.Sq));
+  float o[4], g[4];
+  const int64_t oo = b * p.o_sb + (int64_t)i * p.o_ss + h * p.o_sh + 4 * lane;
+  const int64_t go = b * p.do_sb + (int64_t)i * p.do_ss + h * p.do_sh + 4 * lane;
+  if (p.o_f32) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.o) + oo));
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+    const float4 w = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.dout) + go));
+    g[0] = w.x; g[1] = w.y; g[2] = w.z; g[3] = w.w;
+  } else {
+    const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.o) + oo));
+    o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.dout) + go));
+    g[0] = bf16_lo(w.x); g[1] = bf16_hi(w.x); g[2] = bf16_lo(w.y); g[3] = bf16_hi(w.y);
+  }
+  float acc = o[0] * g[0] + o[1] * g[1] + o[2] * g[2] + o[3] * g[3];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) p.delta[((int64_t)b * p.H + h) * p.Sq + i] = acc;
+  reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
+// One thread per (b, i, h) row, 128 rows per block.
+constexpr uint32_t kPostSmem = kTile * (kD + 1) * sizeof(float);
+
+__global__ void __launch_bounds__(128) dq_post_kernel(const __grid_constant__ PostParams p) {
+  extern __shared__ float red[];  // [128][129]
+  const int tid = threadIdx.x;
+  const int64_t row = (int64_t)blockIdx.x * kTile + tid;
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  float* my = red + tid * (kD + 1);
+  if (row < nrows) {
+    const int h = static_cast<int>(row % p.H);
+    const int i = static_cast<int>((row / p.H) % p.Sq);
+    const int b = static_cast<int>(row / ((int64_t)p.H * p.Sq));
+    float g[kD];
+    const float4* src = reinterpret_cast<const float4*>(p.dq_acc + row * kD);
+#pragma unroll
+    for (int c = 0; c < kD / 4; ++c) {
+      const float4 v = src[c];
+      g[4 * c] = v.x; g[4 * c + 1] = v.y; g[4 * c + 2] = v.z; g[4 * c + 3] = v.w;
+    }
+    rope_norm_bwd_row(g, p.q.p, b * p.q.sb + (int64_t)i * p.q.ss + h * p.q.sh, p.q.is_f32,
+                      p.tab_q + b * p.tab_q_sb + (int64_t)i * kPairs, p.wq, p.eps, my);
+    store_row(p.dq, b * p.dq_sb + (int64_t)i * p.dq_ss + h * p.dq_sh, p.dq_f32, g);
+  } else {
+    for (int d = 0; d < kD; ++d) my[d] = 0.f;
+  }
+  __syncthreads();
+  float acc = 0.f;
+  for (int r = 0; r < kTile; ++r) acc += red[r * (kD + 1) + tid];
+  p.dwq_part[(int64_t)blockIdx.x * kD + tid] = acc;
+}
+
+// Grid (nblocks, 2): y = 0 reduces the q-weight partials, y = 1 the k-weight
+// partials. Each block sums up to kDwChunk partials in index order; the last
+// block to finish sums the block results in index order.
+__global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ DwParams p) {
+  const int which = blockIdx.y, tid = threadIdx.x;
+  const float* part = which ? p.dwk_part : p.dwq_part;
+  const int n = which ? p.n_k : p.n_q;
+  float* scratch = p.scratch + (int64_t)which * gridDim.x * kD;
+  const int p0 = blockIdx.x * kDwChunk;
+  float acc = 0.f;
+  for (int q = p0; q < min(n, p0 + kDwChunk); ++q) acc += part[(int64_t)q * kD + tid];
+  scratch[(int64_t)blockIdx.x * kD + tid] = acc;
+  __threadfence();
+  __syncthreads();
+  __shared__ int is_last;
+  if (tid == 0) is_last = (atomicAdd(p.ctrl + kCtrlDwDone + which, 1u) == gridDim.x - 1);
+  __syncthreads();
+  if (is_last) {
+    __threadfence();
+    float tot = 0.f;
+    for (int b = 0; b < (int)gridDim.x; ++b) tot += __ldcg(scratch + (int64_t)b * kD + tid);
+    (which ? p.dwk : p.dwq)[tid] = tot;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_table(const TableParams& p, cudaStream_t stream) {
+  const int64_t n = (int64_t)p.Bt * p.S * kPairs;
+  const int threads = 256;
+  int blocks = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 152 * 16));
+  if (blocks < 1) blocks = 1;
+  table_kernel<<<blocks, threads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
+  dim3 grid(p.nKt, p.nQtm, p.Bm * p.Hm);
+  classify_kernel<<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream) {
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  const int64_t blocks = (nrows * 32 + 255) / 256;
+  bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  const int64_t blocks = (nrows + kTile - 1) / kTile;
+  static unsigned configured = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(configured & (1u << (dev & 31)))) {
+    cudaError_t e = cudaFuncSetAttribute(dq_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPostSmem);
+    if (e != cudaSuccess) return e;
+    configured |= 1u << (dev & 31);
+  }
+  dq_post_kernel<<<static_cast<unsigned>(blocks), kTile, kPostSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream) {
+  dim3 grid(dw_reduce_blocks(p.n_q, p.n_k), 2);
+  dw_reduce_kernel<<<grid, kD, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace st

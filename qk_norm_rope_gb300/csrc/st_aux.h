@@ -1,0 +1,80 @@
+// Parameter blocks and launchers of the auxiliary kernels.
+#pragma once
+#include <algorithm>
+#include <cuda_runtime.h>
+#include "st_common.cuh"
+
+namespace st {
+
+// Control words at the start of the workspace, zeroed by the table kernel
+// (always the first launch of a call).
+enum { kCtrlAnyFalse = 0, kCtrlClassifyDone = 1, kCtrlDwDone = 2 /* +0 q, +1 k */, kCtrlWords = 8 };
+constexpr int kDwChunk = 32;  // weight-gradient partials summed per block
+
+inline int dw_reduce_blocks(int n_q, int n_k) {
+  const int a = (n_q + kDwChunk - 1) / kDwChunk, b = (n_k + kDwChunk - 1) / kDwChunk;
+  return std::max(1, std::max(a, b));
+}
+
+struct TableParams {
+  const void* ids;
+  int ids_f32;
+  int64_t i_sb, i_ss, i_sa;  // element strides of ids [Bt, S, A]
+  int Bt, S;
+  double omega[kPairs];      // frequency of each pair
+  int axis_of[kPairs];       // axis that owns each pair
+  float2* out;               // [Bt, S, 64]
+  unsigned* ctrl;            // zeroed when non-null
+};
+
+struct ClassifyParams {
+  const uint8_t* mask;
+  int64_t m_sb, m_sh, m_sq;  // element strides, 0 on broadcast dims
+  int Bm, Hm, Sqm, Skv, nQtm, nKt;
+  uint8_t* flags;            // [Bm, Hm, nQtm, nKt]
+  unsigned* ctrl;
+  unsigned long long* counters;
+};
+
+struct PreParams {
+  const void* o;
+  int64_t o_sb, o_ss, o_sh;
+  int o_f32;
+  const void* dout;
+  int64_t do_sb, do_ss, do_sh;
+  float* delta;   // [B, H, Sq]
+  float* dq_acc;  // [B, Sq, H, D]
+  int B, H, Sq;
+};
+
+struct PostParams {
+  const float* dq_acc;
+  RowTensor q;
+  const float2* tab_q;
+  int64_t tab_q_sb;
+  const float* wq;
+  float eps;
+  void* dq;
+  int64_t dq_sb, dq_ss, dq_sh;
+  int dq_f32;
+  float* dwq_part;  // [n_blocks, D]
+  int B, H, Sq;
+};
+
+struct DwParams {
+  const float* dwq_part;
+  const float* dwk_part;
+  int n_q, n_k;
+  float* scratch;  // [2, blocks, D]
+  unsigned* ctrl;
+  float* dwq;
+  float* dwk;
+};
+
+cudaError_t launch_table(const TableParams& p, cudaStream_t stream);
+cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream);
+cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream);
+cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream);
+
+}  // namespace st

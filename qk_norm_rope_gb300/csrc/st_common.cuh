@@ -1,0 +1,237 @@
+// Device-side parameter blocks and row helpers shared by the kernels.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include "st_ptx.cuh"
+
+namespace st {
+
+constexpr int kD = 128;        // head dimension handled by the kernels
+constexpr int kTile = 128;     // rows of a query tile and of a key tile
+constexpr int kPairs = kD / 2; // rotation pairs per row
+constexpr uint32_t kTileBytes = kTile * kD * 2;  // one bf16 operand tile (two 128B-swizzled halves)
+constexpr uint32_t kHalfBytes = kTileBytes / 2;  // one 64-column half: 128 rows x 128 B
+
+// Tile classes of a bool mask, one byte per (b|1, h|1, q-tile|1, k-tile).
+enum : uint8_t { kTileMixed = 0, kTileAllTrue = 1, kTileAllFalse = 2 };
+enum MaskKind : int { kMaskNone = 0, kMaskBool = 1, kMaskF32 = 2, kMaskBF16 = 3 };
+
+// Device status word bits.
+enum : unsigned { kStatusTimeout = 1u };
+
+// Device-side counters (indices into a uint64 array).
+enum { kCtrMaskAllTrue = 0, kCtrTilesSkipped = 1, kCtrTilesTotal = 2, kCtrTimeouts = 3, kNumCounters = 8 };
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct RowTensor {  // [B, S, H, D] view with unit stride on D
+  const void* p;
+  int64_t sb, ss, sh;
+  int is_f32;
+};
+
+struct Common {
+  RowTensor q, k, v;
+  const float* wq;
+  const float* wk;
+  float eps;
+  const float2* tab_q;  // [Bt_q, Sq, 64] (cos, sin)
+  const float2* tab_k;  // [Bt_k, Skv, 64]
+  int64_t tab_q_sb, tab_k_sb;  // batch stride in float2 (0 when shared by the batch)
+  int mask_kind;
+  const void* mask;            // element (b,h,i,j) at b*m_sb + h*m_sh + i*m_sq + j
+  int64_t m_sb, m_sh, m_sq;    // 0 on broadcast dims
+  const uint8_t* flags;        // bool masks: tile classes
+  int64_t f_sb, f_sh, f_sq;    // strides of the flag array (0 on broadcast dims)
+  int causal;
+  float scale;       // softmax scale
+  float scale_log2;  // scale * log2(e)
+  int B, H, Sq, Skv, nQt, nKt;
+  unsigned* status;               // device status word
+  unsigned long long* counters;   // device counters
+  long long wait_budget;          // clock64 cycles per bounded wait
+};
+
+struct FwdParams {
+  Common c;
+  void* o;
+  int64_t o_sb, o_ss, o_sh;
+  int o_f32;
+  float* lse;  // [B, H, Sq]
+};
+
+struct BwdParams {
+  Common c;
+  const void* dout;
+  int64_t do_sb, do_ss, do_sh;
+  const float* lse;    // [B, H, Sq]
+  const float* delta;  // [B, H, Sq]
+  float* dq_acc;       // [B, Sq, H, D] fp32, zeroed
+  void* dk;
+  int64_t dk_sb, dk_ss, dk_sh;
+  int dk_f32;
+  void* dv;
+  int64_t dv_sb, dv_ss, dv_sh;
+  int dv_f32;
+  float* dwk_part;     // [B*H*nKt, D]
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Loads the 128-element row at element offset `off` of a bf16 or fp32 tensor.
+__device__ __forceinline__ void load_row(const void* base, int64_t off, int is_f32, float (&x)[kD]) {
+  if (is_f32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < kD / 4; ++c) {
+      const float4 v = __ldg(p + c);
+      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < kD / 8; ++c) {
+      const uint4 v = __ldg(p + c);
+      x[8 * c + 0] = bf16_lo(v.x); x[8 * c + 1] = bf16_hi(v.x);
+      x[8 * c + 2] = bf16_lo(v.y); x[8 * c + 3] = bf16_hi(v.y);
+      x[8 * c + 4] = bf16_lo(v.z); x[8 * c + 5] = bf16_hi(v.z);
+      x[8 * c + 6] = bf16_lo(v.w); x[8 * c + 7] = bf16_hi(v.w);
+    }
+  }
+}
+
+// Reciprocal RMS of a row: 1 / sqrt(mean(x^2) + eps).
+__device__ __forceinline__ float row_rrms(const float (&x)[kD], float eps) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int d = 0; d < kD; d += 4) {
+    a0 = fmaf(x[d], x[d], a0); a1 = fmaf(x[d + 1], x[d + 1], a1);
+    a2 = fmaf(x[d + 2], x[d + 2], a2); a3 = fmaf(x[d + 3], x[d + 3], a3);
+  }
+  return rsqrtf(((a0 + a1) + (a2 + a3)) * (1.0f / kD) + eps);
+}
+
+// RMSNorm + interleaved-pair rotation of one row, rounded to bf16 and written
+// as row `row` of a K-major 128B-swizzled operand tile (two 64-column halves,
+// kHalfBytes apart). tab: the row's 64 (cos, sin) pairs.
+__device__ __forceinline__ void norm_rope_store(const float (&x)[kD], const float* __restrict__ w, float eps,
+                                                const float2* __restrict__ tab, uint8_t* tile, int row) {
+  const float r = row_rrms(x, eps);
+  const float4* t4 = reinterpret_cast<const float4*>(tab);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {  // 8 elements = 4 pairs = one 16-byte chunk
+    uint32_t packed[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float4 cs = __ldg(t4 + 2 * c + h);  // (cos, sin) of two pairs
+      const float4 ww = __ldg(w4 + 2 * c + h);
+      const int d = 8 * c + 4 * h;
+      const float n0 = x[d] * r * ww.x, n1 = x[d + 1] * r * ww.y;
+      const float n2 = x[d + 2] * r * ww.z, n3 = x[d + 3] * r * ww.w;
+      packed[2 * h] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+      packed[2 * h + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+    }
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+// Raw bf16 row copy into a 128B-swizzled tile (used for v and dO).
+__device__ __forceinline__ void copy_row_bf16(const void* base, int64_t off, uint8_t* tile, int row) {
+  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c)
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) = __ldg(p + c);
+}
+
+__device__ __forceinline__ void zero_row(uint8_t* tile, int row) {
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c)
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) = make_uint4(0, 0, 0, 0);
+}
+
+// Stores a 128-element fp32 row to a bf16 or fp32 destination.
+__device__ __forceinline__ void store_row(void* base, int64_t off, int is_f32, const float (&y)[kD]) {
+  if (is_f32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < kD / 4; ++c) p[c] = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
+  } else {
+    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
+#pragma unroll
+    for (int c = 0; c < kD / 8; ++c)
+      p[c] = make_uint4(pack_bf16(y[8 * c], y[8 * c + 1]), pack_bf16(y[8 * c + 2], y[8 * c + 3]),
+                        pack_bf16(y[8 * c + 4], y[8 * c + 5]), pack_bf16(y[8 * c + 6], y[8 * c + 7]));
+  }
+}
+
+// Loads elements [8c, 8c+8) of the row at element offset `off`.
+__device__ __forceinline__ void load_chunk8(const void* base, int64_t off, int is_f32, int c, float (&v)[8]) {
+  if (is_f32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off) + 2 * c;
+    const float4 a = __ldg(p), b = __ldg(p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+  } else {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off) + c);
+    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
+    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+  }
+}
+
+// Backward of the rotation and the RMSNorm for one row.
+//   g: gradient w.r.t. the rotated, normalised row (fp32, overwritten with dx);
+//   the raw input row x is re-read from (xbase, xoff) chunk by chunk;
+//   tab: the row's (cos, sin); w: norm weight.
+// With dy = R^T g (inverse rotation, sin negated), g' = w * dy:
+//   dx = r g' - (r^3 / D) x (x . g'); the weight-gradient term dy * x * r of
+// the row goes to contrib[0..127] (shared memory; the caller sums over rows).
+__device__ __forceinline__ void rope_norm_bwd_row(float (&g)[kD], const void* xbase, int64_t xoff, int x_f32,
+                                                  const float2* __restrict__ tab, const float* __restrict__ w,
+                                                  float eps, float* contrib) {
+  float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    float x[8];
+    load_chunk8(xbase, xoff, x_f32, c, x);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) { ss0 = fmaf(x[e], x[e], ss0); ss1 = fmaf(x[e + 1], x[e + 1], ss1); }
+  }
+  const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + eps);
+  float xg = 0.f;
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    float x[8];
+    load_chunk8(xbase, xoff, x_f32, c, x);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const int d = 8 * c + e;
+      const float2 cs = __ldg(tab + d / 2);
+      const float d0 = g[d] * cs.x + g[d + 1] * cs.y;
+      const float d1 = -g[d] * cs.y + g[d + 1] * cs.x;
+      contrib[d] = d0 * (x[e] * r);
+      contrib[d + 1] = d1 * (x[e + 1] * r);
+      const float g0 = d0 * __ldg(w + d), g1 = d1 * __ldg(w + d + 1);
+      g[d] = g0;
+      g[d + 1] = g1;
+      xg = fmaf(x[e], g0, fmaf(x[e + 1], g1, xg));
+    }
+  }
+  const float c3 = r * r * r * xg * (1.0f / kD);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    float x[8];
+    load_chunk8(xbase, xoff, x_f32, c, x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) g[8 * c + e] = r * g[8 * c + e] - c3 * x[e];
+  }
+}
+
+__device__ __forceinline__ void record_timeout(const Common& c) {
+  atomicOr(c.status, kStatusTimeout);
+  atomicAdd(c.counters + kCtrTimeouts, 1ull);
+}
+
+}  // namespace st

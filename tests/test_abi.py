@@ -1,0 +1,160 @@
+"""CPU checks of the C-ABI library: it builds, loads and exports every symbol
+that include/*.h declares, and its host-side validation rejects bad arguments
+with the documented status before touching the GPU."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+from qk_norm_rope_gb300 import api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x7f0000000000  # 256-byte aligned stand-in for a device address (never dereferenced)
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names |= set(re.findall(r"ST_API\s+[\w\s\*]+?\b(st_\w+)\s*\(", src))
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    L = api.lib()
+    names = declared_symbols()
+    assert {"st_rope_attn_fwd", "st_rope_attn_bwd", "st_rope_attn_workspace_size"} <= names
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def T(shape, dtype=api.ST_BF16, data=FAKE, strides=None):
+    t = api.st_tensor()
+    t.data = data
+    t.dtype = dtype
+    t.ndim = len(shape)
+    if strides is None:
+        strides, acc = [], 1
+        for s in reversed(shape):
+            strides.insert(0, acc)
+            acc *= s
+    for a, (s, st) in enumerate(zip(shape, strides)):
+        t.shape[a] = s
+        t.stride[a] = st
+    return t
+
+
+class Call:
+    """A valid forward call on fake device pointers; tests perturb one field."""
+
+    def __init__(self, B=1, S=256, Skv=None, H=2, D=128):
+        Skv = S if Skv is None else Skv
+        self.q = T([B, S, H, D])
+        self.k = T([B, Skv, H, D])
+        self.v = T([B, Skv, H, D])
+        self.wq = T([D], api.ST_F32)
+        self.wk = T([D], api.ST_F32)
+        self.o = T([B, S, H, D])
+        self.lse = T([B, H, S], api.ST_F32)
+        self.ids = T([1, S, 3], api.ST_I32)
+        self.ids_k = None
+        self.axes = [16, 56, 56]
+        self.theta = 1e4
+        self.mask = None
+        self.causal = 0
+        self.ws_bytes = 1 << 30
+        self.ws = FAKE
+
+    def rope(self):
+        r = api.st_rope()
+        r.ids = ctypes.pointer(self.ids)
+        r.ids_k = ctypes.pointer(self.ids_k) if self.ids_k is not None else None
+        r.n_axes = len(self.axes)
+        for a, d in enumerate(self.axes):
+            r.axes_dim[a] = d
+        r.theta = self.theta
+        return r
+
+    def fwd(self):
+        p = lambda t: None if t is None else ctypes.pointer(t)
+        L = api.lib()
+        return L.st_rope_attn_fwd(p(self.q), p(self.k), p(self.v), p(self.wq), p(self.wk), 1e-6,
+                                  ctypes.byref(self.rope()), p(self.mask), self.causal, 0.0, p(self.o), p(self.lse),
+                                  ctypes.c_void_p(self.ws), self.ws_bytes, None)
+
+    def ws_size(self, bwd=0):
+        p = lambda t: None if t is None else ctypes.pointer(t)
+        return api.lib().st_rope_attn_workspace_size(p(self.q), p(self.k), p(self.v), p(self.mask), self.causal,
+                                                     ctypes.byref(self.rope()), bwd)
+
+
+def expect(c, status, pattern=None):
+    st = c.fwd()
+    msg = api.lib().st_last_error().decode()
+    assert st == status, (api.STATUS_NAMES[st], msg)
+    if pattern:
+        assert re.search(pattern, msg), msg
+
+
+def test_workspace_size_valid_and_grows_for_backward():
+    c = Call()
+    f, b = c.ws_size(0), c.ws_size(1)
+    assert 0 < f < b
+    c.mask = T([1, 1, 1, 256], api.ST_BOOL)
+    assert c.ws_size(0) > f
+
+
+def test_valid_call_without_gpu_reports_cuda_error():
+    if torch.cuda.is_available():
+        pytest.skip("only meaningful without a GPU")
+    expect(Call(), api.ST_ERR_CUDA)
+
+
+def test_null_and_shape_errors():
+    c = Call(); c.q = None; expect(c, api.ST_ERR_INVALID_ARG)
+    c = Call(D=64); c.wq = T([64], api.ST_F32); c.wk = T([64], api.ST_F32); expect(c, api.ST_ERR_UNSUPPORTED)
+    c = Call(); c.k = T([1, 256, 3, 128]); expect(c, api.ST_ERR_SHAPE, "k has shape")
+    c = Call(); c.o = T([1, 255, 2, 128]); expect(c, api.ST_ERR_SHAPE, "o has shape")
+    c = Call(); c.lse = T([1, 2, 255], api.ST_F32); expect(c, api.ST_ERR_SHAPE, "lse")
+    c = Call(); c.wq = T([64], api.ST_F32); expect(c, api.ST_ERR_SHAPE, "q_norm_w")
+
+
+def test_dtype_errors():
+    c = Call(); c.q.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "q")
+    c = Call(); c.v.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "v")
+    c = Call(); c.o.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "o")
+    c = Call(); c.wk.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "k_norm_w")
+    c = Call(); c.ids.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "ids")
+    c = Call(); c.mask = T([1, 1, 1, 256], api.ST_I32); expect(c, api.ST_ERR_DTYPE, "mask")
+
+
+def test_alignment_errors():
+    c = Call(); c.q.data = FAKE + 8; expect(c, api.ST_ERR_ALIGN, "aligned")
+    c = Call(); c.k.stride[3] = 2; expect(c, api.ST_ERR_ALIGN, "unit stride")
+    c = Call(); c.v.stride[1] = 2 * 128 + 4; expect(c, api.ST_ERR_ALIGN, "multiple of 16")
+    c = Call(); c.lse.stride[2] = 2; expect(c, api.ST_ERR_ALIGN, "contiguous")
+    c = Call(); c.ws = FAKE + 16; expect(c, api.ST_ERR_ALIGN, "256-byte")
+
+
+def test_rope_and_mask_errors():
+    c = Call(); c.axes = [16, 56, 54]; c.ids = T([1, 256, 3], api.ST_I32); expect(c, api.ST_ERR_INVALID_ARG, "axes")
+    c = Call(); c.axes = [16, 57, 55]; expect(c, api.ST_ERR_INVALID_ARG, "even")
+    c = Call(); c.theta = -1.0; expect(c, api.ST_ERR_INVALID_ARG, "theta")
+    c = Call(); c.ids = T([2, 256, 3], api.ST_I32); expect(c, api.ST_ERR_SHAPE, "ids")
+    c = Call(); c.ids = T([1, 256, 2], api.ST_I32); expect(c, api.ST_ERR_SHAPE, "ids")
+    c = Call(S=256, Skv=200); expect(c, api.ST_ERR_INVALID_ARG, "ids_k")
+    c = Call(); c.mask = T([1, 1, 1, 256], api.ST_BOOL); c.causal = 1; expect(c, api.ST_ERR_INVALID_ARG, "causal")
+    c = Call(); c.mask = T([1, 1, 1, 255], api.ST_BOOL); expect(c, api.ST_ERR_SHAPE, "mask")
+    c = Call(); c.mask = T([1, 3, 1, 256], api.ST_BOOL); expect(c, api.ST_ERR_SHAPE, "mask")
+    c = Call(); c.mask = T([1, 1, 256, 256], api.ST_F32, strides=[1, 1, 1, 256]); expect(c, api.ST_ERR_ALIGN)
+
+
+def test_workspace_errors():
+    c = Call()
+    need = c.ws_size(0)
+    c.ws_bytes = need - 1
+    expect(c, api.ST_ERR_WORKSPACE, "smaller")
+    c = Call(); c.ws = 0; expect(c, api.ST_ERR_WORKSPACE, "NULL")
