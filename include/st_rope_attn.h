@@ -174,6 +174,35 @@ ST_API st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const 
                            st_tensor* dq, st_tensor* dk, st_tensor* dv, st_tensor* d_q_norm_w,
                            st_tensor* d_k_norm_w, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Size of the library's built-in forward scratch, used by
+ * st_rope_attn_fwd_noalloc. */
+#define ST_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Forward without a caller-provided workspace (no counterpart in the paper;
+ * an addition of this library). Some callers cannot allocate device memory:
+ * code running while a CUDA graph is being captured into a fixed memory plan,
+ * plugins hosted by inference runtimes that hand out only input and output
+ * buffers, and serving processes that forbid allocation after start-up to keep
+ * their memory footprint fixed. For them the scratch (rotary tables, mask tile
+ * classes, control words) lives in one static device array of
+ * ST_NOALLOC_SCRATCH_BYTES, held by every GPU that loads the library until the
+ * process exits. Arguments and results are those of st_rope_attn_fwd.
+ *  - A call whose scratch need exceeds ST_NOALLOC_SCRATCH_BYTES returns
+ *    ST_ERR_WORKSPACE and launches nothing (the need is B_ids * S * 512 bytes
+ *    of tables, doubled with separate key ids, plus the mask tile classes).
+ *  - The first call on a device looks up the array's device address (a
+ *    one-time set-up per device, which also loads the library's kernels on
+ *    that device); make that first call before any stream capture begins.
+ *  - Every call on a device shares the one array: calls that overlap on the
+ *    GPU (on different streams, or from several threads without ordering)
+ *    race on it. Calls in stream order are safe; each call re-initialises what
+ *    must start from zero.
+ *  - Nothing here calls cudaMalloc, cudaFree or any allocating routine. */
+ST_API st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const st_tensor* v,
+                                          const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps,
+                                          const st_rope* rope, const st_tensor* mask, int causal, float scale,
+                                          st_tensor* o, st_tensor* lse, void* stream);
+
 /* Message of the last failing call on this thread ("" if none). */
 ST_API const char* st_last_error(void);
 

@@ -87,6 +87,8 @@ def lib():
             L.st_reset_stats.restype = None
             L.st_check_status.argtypes = [vp]
             L.st_check_status.restype = i
+            L.st_rope_attn_fwd_noalloc.argtypes = [T, T, T, T, T, fl, R, T, i, fl, T, T, vp]
+            L.st_rope_attn_fwd_noalloc.restype = i
             L.st_timing_enable.argtypes = [i]
             L.st_timing_enable.restype = i
             L.st_timing_read.argtypes = [ctypes.POINTER(st_kernel_times)]
@@ -198,6 +200,24 @@ def st_rope_attn_bwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, o, 
                                 ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream())
     _check(st)
     return dq, dk, dv, dwq, dwk
+
+
+def st_rope_attn_fwd_noalloc(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mask=None, causal=False,
+                             scale=None, ids_k=None, o=None, lse=None):
+    """Forward on the library's built-in scratch (no workspace, no device
+    allocation inside the call; outputs are allocated here unless given)."""
+    _require_cuda(q, k, v, q_norm_w, k_norm_w, ids, mask, ids_k)
+    B, Sq, H, D = q.shape
+    if o is None:
+        o = torch.empty((B, Sq, H, D), dtype=v.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    r = _rope(ids, axes_dim, theta, ids_k)
+    st = lib().st_rope_attn_fwd_noalloc(_p(_t(q)), _p(_t(k)), _p(_t(v)), _p(_t(q_norm_w)), _p(_t(k_norm_w)),
+                                        float(eps), ctypes.byref(r), _p(_t(mask)), int(bool(causal)),
+                                        float(scale) if scale else 0.0, _p(_t(o)), _p(_t(lse)), _stream())
+    _check(st)
+    return o, lse
 
 
 def st_last_error() -> str:

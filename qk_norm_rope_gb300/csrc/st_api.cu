@@ -559,6 +559,98 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   return ST_OK;
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward with built-in scratch, for callers that cannot allocate device
+// memory (see st_rope_attn_fwd_noalloc in the header). The scratch is this
+// file-scope array; host code never uses its name as an address: the device
+// address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[ST_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+st_status noalloc_scratch_address(void** out) {
+  static void* addr[64];
+  static std::atomic<bool> ready[64];
+  static std::mutex mu;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return fail(ST_ERR_CUDA, "cudaGetDevice failed");
+  if (!ready[dev].load(std::memory_order_acquire)) {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ready[dev].load(std::memory_order_relaxed)) {
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p)
+        return fail(ST_ERR_CUDA, "cudaGetSymbolAddress of the built-in scratch failed: %s", cudaGetErrorString(e));
+      addr[dev] = p;
+      ready[dev].store(true, std::memory_order_release);
+    }
+  }
+  *out = addr[dev];
+  return ST_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const st_tensor* v,
+                                   const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps,
+                                   const st_rope* rope, const st_tensor* mask, int causal, float scale,
+                                   st_tensor* o, st_tensor* lse, void* stream_) {
+  t_err.clear();
+  Plan P;
+  st_status st = plan_call(q, k, v, mask, causal, rope, 0, &P);
+  if (st != ST_OK) return st;
+  if (P.total > ST_NOALLOC_SCRATCH_BYTES)
+    return fail(ST_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch; the built-in scratch holds %u bytes "
+                "(use st_rope_attn_fwd with a caller workspace)",
+                P.total, (unsigned)ST_NOALLOC_SCRATCH_BYTES);
+  const Shape& s = P.sh;
+  if ((st = check_vec(q_norm_w, "q_norm_w", kD)) != ST_OK) return st;
+  if ((st = check_vec(k_norm_w, "k_norm_w", kD)) != ST_OK) return st;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return fail(ST_ERR_INVALID_ARG, "eps must be finite and >= 0");
+  if (!std::isfinite(scale)) return fail(ST_ERR_INVALID_ARG, "scale must be finite");
+  RowTensor ro;
+  if ((st = check_out(o, "o", s.B, s.Sq, s.H, v->dtype, &ro)) != ST_OK) return st;
+  if (!lse || lse->ndim != 3 || lse->shape[0] != s.B || lse->shape[1] != s.H || lse->shape[2] != s.Sq)
+    return fail(ST_ERR_SHAPE, "lse must be [B,H,S_q] = [%d,%d,%d]", s.B, s.H, s.Sq);
+  if (lse->dtype != ST_F32) return fail(ST_ERR_DTYPE, "lse must be fp32");
+  if ((int64_t)s.B * s.H * s.Sq > 0 &&
+      (!lse->data || lse->stride[2] != 1 || lse->stride[1] != s.Sq || lse->stride[0] != (int64_t)s.H * s.Sq))
+    return fail(ST_ERR_ALIGN, "lse must be contiguous");
+  if ((int64_t)s.B * s.H * s.Sq == 0) {
+    ++h_fwd_calls;
+    return ST_OK;
+  }
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch_address(&scratch)) != ST_OK) return st;
+  Dev dev;
+  if ((st = device_globals(&dev)) != ST_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t* ws = static_cast<uint8_t*>(scratch);
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
+  fp.c.mask = mask ? mask->data : nullptr;
+  fp.o = o->data;
+  fp.o_sb = ro.sb;
+  fp.o_ss = ro.ss;
+  fp.o_sh = ro.sh;
+  fp.o_f32 = ro.is_f32;
+  fp.lse = static_cast<float*>(lse->data);
+  if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }),
+                       "forward kernel launch")) != ST_OK)
+    return st;
+  ++h_fwd_calls;
+  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  return ST_OK;
+}
+
 const char* st_last_error(void) { return t_err.c_str(); }
 
 st_status st_get_stats(st_stats* out) {
