@@ -11,6 +11,8 @@
 #include <cstring>
 #include <string>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/st_rope_attn.h"
 #include "st_aux.h"
 #include "st_kernels.h"
@@ -403,6 +405,52 @@ st_status check_out(const st_tensor* t, const char* name, int B, int S, int H, i
   return check_bshd(t, name, B, S, H, kD, dtype, dtype, rt);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// 4-D tiled map over a bf16 [B, S, H, D] tensor for 64-column x 128-row boxes
+// with 128-byte swizzle. The two middle dims are ordered by stride (s before h
+// when the sequence stride is the smaller one, as in a BHSD view).
+st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const int64_t B = t->shape[0], S = t->shape[1], H = t->shape[2];
+  const int64_t eb = 2;
+  // strides in bytes; a size-1 dim gets the packed stride (any valid value works)
+  int64_t ss = S > 1 ? t->stride[1] * eb : H * kD * eb;
+  int64_t sh = H > 1 ? t->stride[2] * eb : kD * eb;
+  int64_t sb = B > 1 ? t->stride[0] * eb : S * H * kD * eb;
+  if (ss == 0) ss = H * kD * eb;
+  if (sh == 0) sh = kD * eb;
+  if (sb == 0) sb = S * H * kD * eb;
+  *s_first = ss < sh;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4] = {64, 1, 1, 1}, es[4] = {1, 1, 1, 1};
+  dims[0] = kD;
+  if (*s_first) {
+    dims[1] = S; dims[2] = H; strides[0] = ss; strides[1] = sh; box[1] = kTile;
+  } else {
+    dims[1] = H; dims[2] = S; strides[0] = sh; strides[1] = ss; box[2] = kTile;
+  }
+  dims[3] = B;
+  strides[2] = sb;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ST_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the layout (error %d)", (int)r);
+  return ST_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -444,7 +492,6 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
   if ((st = device_globals(&dev)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   FwdParams fp;
   memset(&fp, 0, sizeof(fp));
   fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
@@ -455,6 +502,13 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
   fp.o_sh = ro.sh;
   fp.o_f32 = ro.is_f32;
   fp.lse = static_cast<float*>(lse->data);
+  if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
+  fp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+  if (fp.qk_tma) {
+    if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
+    if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
+  }
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch")) != ST_OK) return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
@@ -498,6 +552,19 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   if ((st = device_globals(&dev)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
+  BwdParams bp;
+  memset(&bp, 0, sizeof(bp));
+  if (P.nKt > 0) {
+    if ((st = encode_rows_map(v, &bp.tmap_v, &bp.v_s_first)) != ST_OK) return st;
+    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first)) != ST_OK)
+      return st;
+    bp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+    if (bp.qk_tma) {
+      if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
+      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first)) != ST_OK)
+        return st;
+    }
+  }
   if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
 
   float* delta = reinterpret_cast<float*>(ws + P.off_delta);
@@ -515,8 +582,6 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     if ((st = cuda_check(launch_counted(ST_K_BWD_PRE, stream, [&] { return launch_bwd_pre(pp, stream); }), "backward pre launch")) != ST_OK) return st;
   }
   if (P.nKt > 0) {
-    BwdParams bp;
-    memset(&bp, 0, sizeof(bp));
     fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &bp.c);
     bp.c.mask = mask ? mask->data : nullptr;
     bp.dout = d_o->data;
@@ -632,7 +697,6 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   if ((st = device_globals(&dev)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t* ws = static_cast<uint8_t*>(scratch);
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   FwdParams fp;
   memset(&fp, 0, sizeof(fp));
   fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
@@ -643,6 +707,13 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   fp.o_sh = ro.sh;
   fp.o_f32 = ro.is_f32;
   fp.lse = static_cast<float*>(lse->data);
+  if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
+  fp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+  if (fp.qk_tma) {
+    if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
+    if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
+  }
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }),
                        "forward kernel launch")) != ST_OK)
     return st;
@@ -727,8 +798,9 @@ st_status st_check_status(void* stream_) {
   unsigned s = 0, z = 0;
   if ((st = cuda_check(cudaMemcpy(&s, dev.status, sizeof(s), cudaMemcpyDeviceToHost), "read status")) != ST_OK)
     return st;
-  if (s & kStatusTimeout) {
+  if (s & (kStatusTimeout | kStatusLayout)) {
     cudaMemcpy(dev.status, &z, sizeof(z), cudaMemcpyHostToDevice);
+    if (s & kStatusLayout) return fail(ST_ERR_CUDA, "a kernel found its shared memory misaligned and did nothing");
     return fail(ST_ERR_TIMEOUT, "a kernel's bounded wait ran out");
   }
   return ST_OK;

@@ -17,7 +17,7 @@ enum : uint8_t { kTileMixed = 0, kTileAllTrue = 1, kTileAllFalse = 2 };
 enum MaskKind : int { kMaskNone = 0, kMaskBool = 1, kMaskF32 = 2, kMaskBF16 = 3 };
 
 // Device status word bits.
-enum : unsigned { kStatusTimeout = 1u };
+enum : unsigned { kStatusTimeout = 1u, kStatusLayout = 2u };
 
 // Device-side counters (indices into a uint64 array).
 enum { kCtrMaskAllTrue = 0, kCtrTilesSkipped = 1, kCtrTilesTotal = 2, kCtrTimeouts = 3, kNumCounters = 8 };
@@ -55,6 +55,12 @@ struct Common {
 
 struct FwdParams {
   Common c;
+  CUtensorMap tmap_v;  // V as a 4-D tiled map, 128B swizzle, box 64 x 128 keys
+  CUtensorMap tmap_q;  // raw q / k rows (bf16 only; see qk_tma)
+  CUtensorMap tmap_k;
+  int v_s_first;       // map dims are (d, s, h, b) instead of (d, h, s, b)
+  int q_s_first, k_s_first;
+  int qk_tma;          // 1: q and k are bf16 and staged by TMA, normalised in place
   void* o;
   int64_t o_sb, o_ss, o_sh;
   int o_f32;
@@ -63,6 +69,12 @@ struct FwdParams {
 
 struct BwdParams {
   Common c;
+  CUtensorMap tmap_v;   // V rows, as in FwdParams
+  CUtensorMap tmap_do;  // dO rows
+  CUtensorMap tmap_q;   // raw q / k rows (bf16 only; see qk_tma)
+  CUtensorMap tmap_k;
+  int v_s_first, do_s_first, q_s_first, k_s_first;
+  int qk_tma;
   const void* dout;
   int64_t do_sb, do_ss, do_sh;
   const float* lse;    // [B, H, Sq]
@@ -168,6 +180,21 @@ __device__ __forceinline__ void store_row(void* base, int64_t off, int is_f32, c
   }
 }
 
+// Stores elements [32*q4, 32*q4 + 32) of a row to a bf16 or fp32 destination.
+__device__ __forceinline__ void store_chunk32(void* base, int64_t off, int is_f32, int q4, const float (&y)[32]) {
+  if (is_f32) {
+    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off) + 8 * q4;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) p[c] = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
+  } else {
+    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off) + 4 * q4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      p[c] = make_uint4(pack_bf16(y[8 * c], y[8 * c + 1]), pack_bf16(y[8 * c + 2], y[8 * c + 3]),
+                        pack_bf16(y[8 * c + 4], y[8 * c + 5]), pack_bf16(y[8 * c + 6], y[8 * c + 7]));
+  }
+}
+
 // Loads elements [8c, 8c+8) of the row at element offset `off`.
 __device__ __forceinline__ void load_chunk8(const void* base, int64_t off, int is_f32, int c, float (&v)[8]) {
   if (is_f32) {
@@ -227,6 +254,33 @@ __device__ __forceinline__ void rope_norm_bwd_row(float (&g)[kD], const void* xb
 #pragma unroll
     for (int e = 0; e < 8; ++e) g[8 * c + e] = r * g[8 * c + e] - c3 * x[e];
   }
+}
+
+// Bounded wait on an mbarrier phase that also gives up when another role of
+// the CTA has aborted; a wait that runs out of budget raises the CTA's abort
+// flag.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag, long long budget) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > budget) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// 2^x on the MUFU unit (flushes denormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ void record_timeout(const Common& c) {

@@ -1,24 +1,59 @@
 // Forward kernel: fused RMSNorm + RoPE prologue, tcgen05 QK^T and PV with
 // TMEM accumulators, online base-2 softmax, O and log-sum-exp epilogue.
 //
-// One CTA per (query tile of 128 rows, head, batch); 128 threads, thread t
-// owns query row t of the tile (TMEM lane t). Per key tile:
-//   1. every thread normalises + rotates one key row into the K' operand
-//      tile and copies one value row into the V tile (both 128B-swizzled);
-//   2. one thread issues S = Q' K'^T (8 x tcgen05.mma, K = 16 each) into TMEM;
-//   3. each thread reads its S row from TMEM, applies scale, mask / causal /
-//      bounds, updates the running max and sum, writes P (bf16) back into the
-//      S columns and rescales its O row when the max moved;
-//   4. one thread issues O += P V with P read from TMEM.
+// One CTA per (pair of 128-row query tiles, head, batch), warp-specialised:
+//   warps 0-7   softmax: warp w serves query tile w/4 and TMEM lanes
+//               32*(w%4).. (one thread per query row); two passes over the
+//               row's 128 scores in TMEM: the max of the raw scores, then
+//               P = exp2(s*scale*log2e - max) with the scale folded into one FMA
+//   warps 8-11  operand prologue, one thread per row: Q' for both query tiles,
+//               then K' for every key tile of a kStages-deep ring; bf16 rows
+//               arrive by TMA in the operand layout and are normalised and
+//               rotated in place (fp32 rows are read from global memory)
+//   warp 12     TMEM allocation + tcgen05.mma issue (one thread)
+//   warp 13     TMA: raw Q and K rows, V tiles
+// TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_i (bf16)
+// overwrites the first 64 columns of S_i and feeds PV from TMEM.
+// MMA issue order per key tile n: PV0(n-1), S0(n), PV1(n-1), S1(n), so that
+// while one softmax group works on its scores the tensor core computes the
+// other's.
 #include "st_common.cuh"
 #include "st_kernels.h"
+#include "st_prologue.cuh"
 
 namespace st {
 
 namespace {
 
-constexpr int kFwdThreads = 128;
-constexpr uint32_t kFwdSmem = 3 * kTileBytes + 1024 /*barriers*/ + 1024 /*alignment slack*/;
+constexpr int kStages = 2;
+constexpr int kSoftWarps = 8;
+constexpr int kWarpProl0 = 8, kProlWarps = 4;
+constexpr int kWarpMma = 12, kWarpTma = 13;
+constexpr int kFwdWarps = 14;
+constexpr int kFwdThreads = kFwdWarps * 32;
+// rescale O only when the running max grows by more than 8 (base 2); exact
+// either way since O and l always share the same reference max
+constexpr float kRescaleThreshold = 8.0f;
+
+// shared memory layout (offsets from a 1024-byte aligned base)
+constexpr uint32_t kOffQ = 0;                                  // 2 tiles
+constexpr uint32_t kOffK = 2 * kTileBytes;                     // kStages tiles
+constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;       // kStages tiles
+constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+constexpr uint32_t kFwdSmem = kOffBar + 256 + 1024;
+
+enum {
+  kBarQRaw = 0,                       // raw q rows landed (TMA)
+  kBarQFull,                          // Q' ready (prologue)
+  kBarKRaw,                           // + stage: raw k rows landed (TMA)
+  kBarKFull = kBarKRaw + kStages,     // + stage: K' ready (prologue)
+  kBarVFull = kBarKFull + kStages,    // + stage
+  kBarKVEmpty = kBarVFull + kStages,  // + stage
+  kBarSFull = kBarKVEmpty + kStages,  // + tile (0/1)
+  kBarPFull = kBarSFull + 2,          // + tile, 256 arrivals
+  kBarOFull = kBarPFull + 2,
+  kNumBars = kBarOFull + 1
+};
 
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
@@ -27,217 +62,407 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, kHalfBytes, 1024);
 }
 
-// Adds the mask of keys [j0, j0+128) for query row i to the base-2 scores.
-// Keys at or beyond S_kv are set to -inf (and their mask is not read).
-__device__ __forceinline__ void apply_mask_row(const Common& c, int b, int h, int i, int j0, uint8_t flag,
-                                               float (&s)[kTile]) {
-  const int nvalid = min(kTile, c.Skv - j0);
-  if (i >= c.Sq) return;  // padding row of the last query tile: nothing to read, nothing stored
-  if (c.mask_kind == kMaskBool && flag == kTileMixed) {
-    const uint8_t* mrow = static_cast<const uint8_t*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+__device__ __forceinline__ uint8_t tile_flag(const Common& c, int b, int h, int qt, int kt) {
+  if (qt >= c.nQt) return kTileAllFalse;
+  if (c.mask_kind == kMaskBool) return c.flags[b * c.f_sb + h * c.f_sh + qt * c.f_sq + kt];
+  if (c.mask_kind == kMaskNone) return kTileAllTrue;
+  return kTileMixed;  // additive masks are always applied
+}
+
+// Next key tile at or after kt that at least one of the two query tiles needs.
+__device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0, int kt, int kt_end) {
+  if (c.mask_kind != kMaskBool) return kt;
+  for (; kt < kt_end; ++kt)
+    if (tile_flag(c, b, h, qt0, kt) != kTileAllFalse || tile_flag(c, b, h, qt0 + 1, kt) != kTileAllFalse) break;
+  return kt;
+}
+
+// Base-2 scores of 32 key columns [j0, j0 + 32) of query row i from their raw
+// TMEM values: s * scale * log2(e) (+ mask * log2(e)), -inf where a bool mask
+// is False, beyond the causal diagonal or at keys >= S_kv. Tiles that need no
+// masking take the caller's fast path instead.
+__device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t (&raw)[32], int b, int h, int i,
+                                                int j0, uint8_t flag, uint32_t mbits, float (&s)[32]) {
 #pragma unroll
-    for (int jj = 0; jj < kTile; ++jj)
-      if (jj < nvalid && __ldg(mrow + jj) == 0) s[jj] = -INFINITY;
-  } else if (c.mask_kind == kMaskF32) {
-    const float* mrow = static_cast<const float*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+  for (int t = 0; t < 32; ++t) s[t] = __uint_as_float(raw[t]) * c.scale_log2;
+  if (flag == kTileAllFalse) {
 #pragma unroll
-    for (int jj = 0; jj < kTile; ++jj)
-      if (jj < nvalid) s[jj] = fmaf(__ldg(mrow + jj), kLog2e, s[jj]);
-  } else if (c.mask_kind == kMaskBF16) {
-    const __nv_bfloat16* mrow =
-        static_cast<const __nv_bfloat16*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
-#pragma unroll
-    for (int jj = 0; jj < kTile; ++jj)
-      if (jj < nvalid) s[jj] = fmaf(__bfloat162float(mrow[jj]), kLog2e, s[jj]);
+    for (int t = 0; t < 32; ++t) s[t] = -INFINITY;
+    return;
   }
-  if (nvalid < kTile) {
+  if (c.mask_kind == kMaskBool) {
+    if (flag == kTileMixed) {
 #pragma unroll
-    for (int jj = 0; jj < kTile; ++jj)
-      if (jj >= nvalid) s[jj] = -INFINITY;
+      for (int t = 0; t < 32; ++t)
+        if (!((mbits >> t) & 1u)) s[t] = -INFINITY;
+    }
+  } else if (c.mask_kind == kMaskF32) {
+    if (i < c.Sq) {
+      const float* mrow = static_cast<const float*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (j0 + t < c.Skv) s[t] = fmaf(__ldg(mrow + t), kLog2e, s[t]);
+    }
+  } else if (c.mask_kind == kMaskBF16) {
+    if (i < c.Sq) {
+      const __nv_bfloat16* mrow =
+          static_cast<const __nv_bfloat16*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+#pragma unroll
+      for (int t = 0; t < 32; ++t)
+        if (j0 + t < c.Skv) s[t] = fmaf(__bfloat162float(mrow[t]), kLog2e, s[t]);
+    }
+  }
+  if (c.causal) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (j0 + t > i) s[t] = -INFINITY;
+  }
+  if (j0 + 32 > c.Skv) {
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (j0 + t >= c.Skv) s[t] = -INFINITY;
   }
 }
 
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = sm;
-  uint8_t* sK = sm + kTileBytes;
-  uint8_t* sV = sm + 2 * kTileBytes;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 3 * kTileBytes);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
 
   const Common& c = P.c;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int i = qt * kTile + tid;
+  const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
+  const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qt0 = 2 * pair;
 
-  if (warp == 0) {
-    tmem_alloc(tslot, 256);
+  if (warp == kWarpMma) {
+    tmem_alloc(tslot, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(bar, 1);
+    mbar_init(&bars[kBarQRaw], 1);
+    mbar_init(&bars[kBarQFull], kProlWarps * 32);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars[kBarKRaw + s], 1);
+      mbar_init(&bars[kBarKFull + s], kProlWarps * 32);
+      mbar_init(&bars[kBarVFull + s], 1);
+      mbar_init(&bars[kBarKVEmpty + s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars[kBarSFull + t], 1);
+      mbar_init(&bars[kBarPFull + t], 128);
+    }
+    mbar_init(&bars[kBarOFull], 1);
+    *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (warp == kWarpTma && lane_id == 0) {
+    tma_prefetch_desc(&P.tmap_v);
+    if (P.qk_tma) {
+      tma_prefetch_desc(&P.tmap_q);
+      tma_prefetch_desc(&P.tmap_k);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t lane = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem, tO = tmem + 128;
-
-  if (i < c.Sq) {
-    float x[kD];
-    load_row(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, x);
-    norm_rope_store(x, c.wq, c.eps, c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, sQ, tid);
-  } else {
-    zero_row(sQ, tid);
-  }
 
   int kt_end = c.nKt;
-  if (c.causal) kt_end = min(c.nKt, (qt * kTile + kTile - 1) / kTile + 1);
+  if (c.causal) kt_end = min(c.nKt, (qt0 * kTile + 2 * kTile - 1) / kTile + 1);
+  const long long budget = c.wait_budget;
 
-  const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
-  const uint32_t idesc_pv = idesc_bf16(128, 128, 0, 1);
-  const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-
-  float m_run = -INFINITY, l_run = 0.f;
-  uint32_t phase = 0;
-  bool any = false;
-  bool failed = false;
-  int skipped = c.nKt - kt_end;
-
-  for (int kt = 0; kt < kt_end; ++kt) {
-    uint8_t flag = kTileMixed;
-    if (c.mask_kind == kMaskBool) flag = c.flags[b * c.f_sb + h * c.f_sh + qt * c.f_sq + kt];
-    if (flag == kTileAllFalse) {
-      ++skipped;
-      continue;
-    }
-    const int j = kt * kTile + tid;
-    if (j < c.Skv) {
-      float x[kD];
-      load_row(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, x);
-      norm_rope_store(x, c.wk, c.eps, c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs, sK, tid);
-      copy_row_bf16(c.v.p, b * c.v.sb + (int64_t)j * c.v.ss + h * c.v.sh, sV, tid);
-    } else {
-      zero_row(sK, tid);
-      zero_row(sV, tid);
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
+  if (warp < kSoftWarps) {
+    // ------------------------------------------------------------ softmax
+    const int ti = warp >> 2;                 // query tile of the pair
+    const int r = (warp & 3) * 32 + lane_id;  // row within the tile = TMEM lane
+    const int i = (qt0 + ti) * kTile + r;
+    const uint32_t lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + ti * 128 + lane, tO = tmem + 256 + ti * 128 + lane;
+    const float sc = c.scale_log2;
+    float m_run = -INFINITY, l_run = 0.f;
+    int n = 0, useful = 0;
+    bool ok = true;
+    for (int kt = next_tile(c, b, h, qt0, 0, kt_end); kt < kt_end; kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
+      const uint8_t flag = tile_flag(c, b, h, qt0 + ti, kt);
+      useful += (flag != kTileAllFalse && (!c.causal || kt <= qt0 + ti)) ? 1 : 0;
+      const int j0 = kt * kTile;
+      // plain tiles: no mask values, no causal diagonal, no key bound inside
+      const bool plain = (flag == kTileAllTrue || (c.mask_kind == kMaskNone && flag != kTileAllFalse)) &&
+                         (!c.causal || j0 + kTile - 1 <= (qt0 + ti) * kTile) && j0 + kTile <= c.Skv;
+      uint32_t mbits[4] = {~0u, ~0u, ~0u, ~0u};
+      if (c.mask_kind == kMaskBool && flag == kTileMixed && i < c.Sq) {
+        const uint8_t* mrow = static_cast<const uint8_t*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+        const int nvalid = min(kTile, c.Skv - j0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tS, kmajor_desc(aQ, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
-      mma_commit(bar);
-    }
-    __syncwarp();
-    bool ok = mbar_wait(bar, phase, c.wait_budget);
-    phase ^= 1;
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc_fence_after();
-
-    // ---- online softmax on this thread's row
-    float s[kTile];
-    {
-      uint32_t r32[32];
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t bits = 0;
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        tmem_ld32(tS + lane + 32 * q4, r32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) s[32 * q4 + t] = __uint_as_float(r32[t]) * c.scale_log2;
-      }
-    }
-    apply_mask_row(c, b, h, i, kt * kTile, flag, s);
-    if (c.causal) {
-#pragma unroll
-      for (int jj = 0; jj < kTile; ++jj)
-        if (kt * kTile + jj > i) s[jj] = -INFINITY;
-    }
-    float mt = -INFINITY;
-#pragma unroll
-    for (int jj = 0; jj < kTile; ++jj) mt = fmaxf(mt, s[jj]);
-    const float m_new = fmaxf(m_run, mt);
-    const float corr = (m_new == -INFINITY) ? 1.f : exp2f(m_run - m_new);
-    float lsum = 0.f;
-    {
-      uint32_t pw[32];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-#pragma unroll
-        for (int t = 0; t < 32; ++t) {
-          const int jj = 64 * hh + 2 * t;
-          const float p0 = (m_new == -INFINITY) ? 0.f : exp2f(s[jj] - m_new);
-          const float p1 = (m_new == -INFINITY) ? 0.f : exp2f(s[jj + 1] - m_new);
-          lsum += p0 + p1;
-          pw[t] = pack_bf16(p0, p1);
+          for (int t = 0; t < 32; ++t)
+            if (32 * q4 + t < nvalid && __ldg(mrow + 32 * q4 + t)) bits |= 1u << t;
+          mbits[q4] = bits;
         }
-        tmem_st32(tS + lane + 32 * hh, pw);
       }
-    }
-    l_run = l_run * corr + lsum;
-    m_run = m_new;
-    if (any && __any_sync(0xffffffffu, corr != 1.f)) {  // warp-uniform: tcgen05.ld/st are collective
-      uint32_t r32[32];
+      if (!(ok = wait_bar(&bars[kBarSFull + ti], n & 1, abort_flag, budget))) break;
+      tc_fence_after();
+      // pass 1: row max (raw scores on plain tiles; the scale is positive)
+      float mt = -INFINITY;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        tmem_ld32(tO + lane + 32 * q4, r32);
+        uint32_t raw[32];
+        tmem_ld32(tS + 32 * q4, raw);
+        if (plain) {
+          float m0 = __uint_as_float(raw[0]), m1 = __uint_as_float(raw[1]);
 #pragma unroll
-        for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * corr);
-        tmem_st32(tO + lane + 32 * q4, r32);
+          for (int t = 2; t < 32; t += 2) {
+            m0 = fmaxf(m0, __uint_as_float(raw[t]));
+            m1 = fmaxf(m1, __uint_as_float(raw[t + 1]));
+          }
+          mt = fmaxf(mt, fmaxf(m0, m1) * sc);
+        } else {
+          float sv[32];
+          masked_scores32(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) mt = fmaxf(mt, sv[t]);
+        }
+      }
+      float corr = 1.f;
+      if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
+        corr = ex2(m_run - mt);  // 0 when m_run is -inf
+        m_run = mt;
+      }
+      const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
+      // pass 2: P = exp2(s - m) (bf16 into the first 64 S columns), row sum
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t raw[32], pw[16];
+        tmem_ld32(tS + 32 * q4, raw);
+        if (plain) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float p0 = ex2(fmaf(__uint_as_float(raw[2 * t]), sc, -m_use));
+            const float p1 = ex2(fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use));
+            ls0 += p0;
+            ls1 += p1;
+            pw[t] = pack_bf16(p0, p1);
+          }
+        } else {
+          float sv[32];
+          masked_scores32(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const float p0 = ex2(sv[2 * t] - m_use), p1 = ex2(sv[2 * t + 1] - m_use);
+            ls0 += p0;
+            ls1 += p1;
+            pw[t] = pack_bf16(p0, p1);
+          }
+        }
+        tmem_st16(tS + 16 * q4, pw);
+      }
+      l_run = l_run * corr + (ls0 + ls1);
+      if (n > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // warp-uniform: tcgen05.ld/st are collective
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t r32[32];
+          tmem_ld32(tO + 32 * q4, r32);
+#pragma unroll
+          for (int t = 0; t < 32; ++t) r32[t] = __float_as_uint(__uint_as_float(r32[t]) * corr);
+          tmem_st32(tO + 32 * q4, r32);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarPFull + ti]);
+    }
+    // ---- epilogue: O / l, LSE
+    if (ok && n > 0) ok = wait_bar(&bars[kBarOFull], 0, abort_flag, budget);
+    if (ok) {
+      tc_fence_after();
+      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
+      const int64_t ooff = b * P.o_sb + (int64_t)i * P.o_ss + h * P.o_sh;
+#pragma unroll 1
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r32[32];
+        if (n > 0) {
+          tmem_ld32(tO + 32 * q4, r32);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) r32[t] = 0u;
+        }
+        float y[32];
+#pragma unroll
+        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r32[t]) * inv;
+        if (i < c.Sq) store_chunk32(P.o, ooff, P.o_f32, q4, y);
+      }
+      if (i < c.Sq)
+        P.lse[((int64_t)b * c.H + h) * c.Sq + i] = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      if (r == 0 && qt0 + ti < c.nQt) {  // key tiles this query tile skipped or found fully masked
+        atomicAdd(c.counters + kCtrTilesSkipped, (unsigned long long)(c.nKt - useful));
+        atomicAdd(c.counters + kCtrTilesTotal, (unsigned long long)c.nKt);
       }
     }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tS + kk * 8, mnmajor_desc(aV, kk), idesc_pv, (any || kk > 0) ? 1u : 0u);
-      mma_commit(bar);
+  } else if (warp < kWarpProl0 + kProlWarps) {
+    // ------------------------------------------------------------ operand prologue
+    const int p = tid - kWarpProl0 * 32;  // row of the tile handled by this thread
+    bool ok = true;
+    if (P.qk_tma) ok = wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+    if (ok) {
+#pragma unroll 1
+      for (int ti = 0; ti < 2; ++ti) {
+        const int i = (qt0 + ti) * kTile + p;
+        uint8_t* tile = sm + kOffQ + ti * kTileBytes;
+        const float2* tab = c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs;
+        if (P.qk_tma) {
+          if (i < c.Sq) rope_norm_inplace(tile, p, c.wq, c.eps, tab);  // rows past S_q stay TMA zeros
+        } else if (i < c.Sq) {
+          rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps, tab, tile,
+                           p);
+        } else {
+          zero_row(tile, p);
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kBarQFull]);
     }
-    __syncwarp();
-    ok = mbar_wait(bar, phase, c.wait_budget);
-    phase ^= 1;
-    if (__syncthreads_or(!ok)) { failed = true; break; }
-    tc_fence_after();
-    any = true;
+    int n = 0;
+    for (int kt = next_tile(c, b, h, qt0, 0, kt_end); ok && kt < kt_end;
+         kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
+      const int slot = n % kStages;
+      uint8_t* tile = sm + kOffK + slot * kTileBytes;
+      const int j = kt * kTile + p;
+      const float2* tab = c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs;
+      if (P.qk_tma) {
+        if (!wait_bar(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
+        if (j < c.Skv) rope_norm_inplace(tile, p, c.wk, c.eps, tab);
+      } else {
+        if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
+        if (j < c.Skv)
+          rope_norm_global(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps, tab, tile,
+                           p);
+        else
+          zero_row(tile, p);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars[kBarKFull + slot]);
+    }
+  } else if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA: raw Q, raw K, V
+    if (lane_id == 0) {
+      if (P.qk_tma) {
+        mbar_arrive_expect_tx(&bars[kBarQRaw], 2 * kTileBytes);
+#pragma unroll 1
+        for (int ti = 0; ti < 2; ++ti) {
+          const int row = (qt0 + ti) * kTile;
+          const int y = P.q_s_first ? row : h, z = P.q_s_first ? h : row;
+          uint8_t* tile = sm + kOffQ + ti * kTileBytes;
+          tma_load_4d(tile, &P.tmap_q, &bars[kBarQRaw], 0, y, z, b);
+          tma_load_4d(tile + kHalfBytes, &P.tmap_q, &bars[kBarQRaw], 64, y, z, b);
+        }
+      }
+      int n = 0;
+      for (int kt = next_tile(c, b, h, qt0, 0, kt_end); kt < kt_end;
+           kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
+        const int slot = n % kStages;
+        if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
+        if (P.qk_tma) {
+          uint8_t* ktile = sm + kOffK + slot * kTileBytes;
+          const int y = P.k_s_first ? kt * kTile : h, z = P.k_s_first ? h : kt * kTile;
+          mbar_arrive_expect_tx(&bars[kBarKRaw + slot], kTileBytes);
+          tma_load_4d(ktile, &P.tmap_k, &bars[kBarKRaw + slot], 0, y, z, b);
+          tma_load_4d(ktile + kHalfBytes, &P.tmap_k, &bars[kBarKRaw + slot], 64, y, z, b);
+        }
+        uint8_t* tile = sm + kOffV + slot * kTileBytes;
+        const int y = P.v_s_first ? kt * kTile : h, z = P.v_s_first ? h : kt * kTile;
+        mbar_arrive_expect_tx(&bars[kBarVFull + slot], kTileBytes);
+        tma_load_4d(tile, &P.tmap_v, &bars[kBarVFull + slot], 0, y, z, b);
+        tma_load_4d(tile + kHalfBytes, &P.tmap_v, &bars[kBarVFull + slot], 64, y, z, b);
+      }
+      // every issued load lands before the CTA exits
+      if (P.qk_tma) wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+      for (int m = max(0, n - kStages); m < n; ++m) {
+        wait_bar(&bars[kBarVFull + m % kStages], (m / kStages) & 1, abort_flag, budget);
+        if (P.qk_tma) wait_bar(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, abort_flag, budget);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane_id == 0) {
+      const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
+      const uint32_t idesc_pv = idesc_bf16(128, 128, 0, 1);
+      const uint32_t aQ0 = smem_u32(sm + kOffQ), aQ1 = aQ0 + kTileBytes;
+      const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
+      bool ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
+      int kt = next_tile(c, b, h, qt0, 0, kt_end);
+      int n = 0;
+      bool issued = false;
+      if (ok && kt < kt_end) {
+        ok = wait_bar(&bars[kBarKFull + 0], 0, abort_flag, budget);
+        if (ok) {
+          tc_fence_after();
+          const uint32_t aK = smem_u32(sm + kOffK);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, kmajor_desc(aQ0, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          mma_commit(&bars[kBarSFull + 0]);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, kmajor_desc(aQ1, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          mma_commit(&bars[kBarSFull + 1]);
+          issued = true;
+        }
+      }
+      while (ok && kt < kt_end) {
+        const int slot = n % kStages;
+        const int kt_next = next_tile(c, b, h, qt0, kt + 1, kt_end);
+        const bool has_next = kt_next < kt_end;
+        const int nslot = (n + 1) % kStages;
+        const uint32_t aV = smem_u32(sm + kOffV + slot * kTileBytes);
+        if (!(ok = wait_bar(&bars[kBarVFull + slot], (n / kStages) & 1, abort_flag, budget))) break;
+        if (!(ok = wait_bar(&bars[kBarPFull + 0], n & 1, abort_flag, budget))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, mnmajor_desc(aV, kk), idesc_pv, (n > 0 || kk > 0));
+        if (has_next) {
+          if (!(ok = wait_bar(&bars[kBarKFull + nslot], ((n + 1) / kStages) & 1, abort_flag, budget))) break;
+          tc_fence_after();
+          const uint32_t aK = smem_u32(sm + kOffK + nslot * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, kmajor_desc(aQ0, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          mma_commit(&bars[kBarSFull + 0]);
+        }
+        if (!(ok = wait_bar(&bars[kBarPFull + 1], n & 1, abort_flag, budget))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ts(tO1, tS1 + kk * 8, mnmajor_desc(aV, kk), idesc_pv, (n > 0 || kk > 0));
+        mma_commit(&bars[kBarKVEmpty + slot]);
+        if (has_next) {
+          const uint32_t aK = smem_u32(sm + kOffK + nslot * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, kmajor_desc(aQ1, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          mma_commit(&bars[kBarSFull + 1]);
+        }
+        kt = kt_next;
+        ++n;
+      }
+      if (issued) {
+        // every MMA done (also on abort) before anyone reads O or frees TMEM
+        mma_commit(&bars[kBarOFull]);
+        if (!ok) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(&bars[kBarOFull], 0) && clock64() - t0 < budget) {
+          }
+        }
+      }
+    }
   }
 
-  if (failed) {
-    if (tid == 0) record_timeout(c);
-    // Give the in-flight MMA one more bounded chance to land before TMEM is freed.
-    mbar_wait(bar, phase ^ 1, c.wait_budget);
-  } else {
-    // ---- epilogue: O / l and the log-sum-exp
-    float y[kD];
-    if (any) {
-      const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
-      uint32_t r32[32];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        tmem_ld32(tO + lane + 32 * q4, r32);
-#pragma unroll
-        for (int t = 0; t < 32; ++t) y[32 * q4 + t] = __uint_as_float(r32[t]) * inv;
-      }
-    } else {
-#pragma unroll
-      for (int d = 0; d < kD; ++d) y[d] = 0.f;
-    }
-    if (i < c.Sq) {
-      store_row(P.o, b * P.o_sb + (int64_t)i * P.o_ss + h * P.o_sh, P.o_f32, y);
-      P.lse[((int64_t)b * c.H + h) * c.Sq + i] = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
-    }
-    if (tid == 0) {
-      atomicAdd(c.counters + kCtrTilesSkipped, (unsigned long long)skipped);
-      atomicAdd(c.counters + kCtrTilesTotal, (unsigned long long)c.nKt);
-    }
-  }
+  if (*abort_flag && tid == 0) record_timeout(c);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 256);
+  if (warp == kWarpMma) {
+    __syncwarp();
+    tmem_dealloc(tmem, 512);
+  }
 }
 
 }  // namespace
@@ -251,7 +476,7 @@ cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured |= 1u << (dev & 31);
   }
-  dim3 grid(p.c.nQt, p.c.H, p.c.B);
+  dim3 grid((p.c.nQt + 1) / 2, p.c.H, p.c.B);
   fwd_kernel<<<grid, kFwdThreads, kFwdSmem, stream>>>(p);
   return cudaGetLastError();
 }

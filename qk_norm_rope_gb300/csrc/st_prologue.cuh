@@ -1,0 +1,166 @@
+// Warp-cooperative operand prologue: RMSNorm (fp32) + interleaved-pair RoPE of
+// one 128-row tile of q or k, rounded to bf16 and written as a K-major,
+// 128B-swizzled UMMA operand tile. One warp handles one row at a time; lane l
+// owns head dims 4l..4l+3 (two rotation pairs), so every global load (the raw
+// row, its (cos, sin) table row) is one coalesced request per row, the norm
+// weights stay in registers, and the row's sum of squares is a shuffle
+// reduction.
+#pragma once
+#include "st_common.cuh"
+
+namespace st {
+
+struct RowPrologue {
+  float w0, w1, w2, w3;  // this lane's four norm weights
+  float eps;
+  uint32_t dst;          // this lane's byte offset inside a row (half, chunk, 8-byte sub-chunk)
+  int lane;
+
+  __device__ __forceinline__ RowPrologue(const float* __restrict__ w, float eps_, int lane_)
+      : eps(eps_), lane(lane_) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(w) + lane_);
+    w0 = v.x; w1 = v.y; w2 = v.z; w3 = v.w;
+    dst = (lane_ >> 4) * kHalfBytes;
+  }
+
+  // Rows [row0, row0 + 128) of x (head h, batch b) into `tile`; rows at or
+  // beyond nrows are written as zeros. tab: the (cos, sin) table of batch b,
+  // indexed by row. Warp `wi` of `nw` handles rows wi, wi + nw, ...
+  __device__ __forceinline__ void tile(const RowTensor& x, int b, int h, int row0, int nrows,
+                                       const float2* __restrict__ tab, uint8_t* tile_base, int wi, int nw) const {
+    constexpr int U = 4;  // rows in flight per warp
+    const int64_t base = b * x.sb + h * x.sh + 4 * lane;
+    const uint32_t chunk = (lane & 15) >> 1, sub = (lane & 1) * 8;
+#pragma unroll 1
+    for (int rr = wi; rr < kTile; rr += nw * U) {
+      float v[U][4], cs[U][4];
+      bool valid[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int row = row0 + rr + u * nw;
+        valid[u] = (rr + u * nw < kTile) && row < nrows;
+        if (valid[u]) {
+          const int64_t off = base + (int64_t)row * x.ss;
+          if (x.is_f32) {
+            const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x.p) + off));
+            v[u][0] = a.x; v[u][1] = a.y; v[u][2] = a.z; v[u][3] = a.w;
+          } else {
+            const uint2 a = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(x.p) + off));
+            v[u][0] = bf16_lo(a.x); v[u][1] = bf16_hi(a.x); v[u][2] = bf16_lo(a.y); v[u][3] = bf16_hi(a.y);
+          }
+          const float4 t = __ldg(reinterpret_cast<const float4*>(tab + (int64_t)row * kPairs) + lane);
+          cs[u][0] = t.x; cs[u][1] = t.y; cs[u][2] = t.z; cs[u][3] = t.w;
+        } else {
+          v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
+          cs[u][0] = 1.f; cs[u][1] = 0.f; cs[u][2] = 1.f; cs[u][3] = 0.f;
+        }
+      }
+      float ss[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        ss[u] = fmaf(v[u][0], v[u][0], fmaf(v[u][1], v[u][1], fmaf(v[u][2], v[u][2], v[u][3] * v[u][3])));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (rr + u * nw >= kTile) continue;
+        const int trow = rr + u * nw;
+        uint32_t lo = 0u, hi = 0u;
+        if (valid[u]) {
+          const float r = rsqrtf(ss[u] * (1.0f / kD) + eps);
+          const float n0 = v[u][0] * w0 * r, n1 = v[u][1] * w1 * r;
+          const float n2 = v[u][2] * w2 * r, n3 = v[u][3] * w3 * r;
+          lo = pack_bf16(n0 * cs[u][0] - n1 * cs[u][1], n0 * cs[u][1] + n1 * cs[u][0]);
+          hi = pack_bf16(n2 * cs[u][2] - n3 * cs[u][3], n2 * cs[u][3] + n3 * cs[u][2]);
+        }
+        *reinterpret_cast<uint2*>(tile_base + dst + sw128_off(trow, chunk) + sub) = make_uint2(lo, hi);
+      }
+    }
+  }
+};
+
+// Thread-per-row prologue on a tile that TMA has already filled with the raw
+// bf16 rows (128B-swizzled, the operand layout): the thread reads its row,
+// normalises and rotates it, and writes the bf16 result back in place. The
+// swizzle makes eight consecutive rows hit eight different bank groups, so
+// the 16-byte accesses are conflict-free. tab: the row's 64 (cos, sin).
+__device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const float* __restrict__ w, float eps,
+                                                  const float2* __restrict__ tab) {
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7));
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
+      a0 = fmaf(lo, lo, a0);
+      a1 = fmaf(hi, hi, a1);
+    }
+  }
+  const float r = rsqrtf((a0 + a1) * (1.0f / kD) + eps);
+  const float4* t4 = reinterpret_cast<const float4*>(tab);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll 2
+  for (int c = 0; c < kD / 8; ++c) {
+    uint4* p16 = reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7));
+    const uint4 v = *p16;
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float4 cs = __ldg(t4 + 2 * c + hh);  // (cos, sin) of two pairs
+      const float4 ww = __ldg(w4 + 2 * c + hh);
+      const float n0 = bf16_lo(u[2 * hh]) * ww.x * r, n1 = bf16_hi(u[2 * hh]) * ww.y * r;
+      const float n2 = bf16_lo(u[2 * hh + 1]) * ww.z * r, n3 = bf16_hi(u[2 * hh + 1]) * ww.w * r;
+      out[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+      out[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+    }
+    *p16 = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// Thread-per-row prologue reading the raw row (bf16 or fp32) from global
+// memory; used when q/k are fp32 (no in-place TMA staging) and for rows that
+// a TMA load does not cover. The raw row is read twice (sum of squares, then
+// transform), the second time from L1.
+__device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, int is_f32,
+                                                 const float* __restrict__ w, float eps,
+                                                 const float2* __restrict__ tab, uint8_t* tile, int row) {
+  float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    float x[8];
+    load_chunk8(base, off, is_f32, c, x);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      ss0 = fmaf(x[e], x[e], ss0);
+      ss1 = fmaf(x[e + 1], x[e + 1], ss1);
+    }
+  }
+  const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + eps);
+  const float4* t4 = reinterpret_cast<const float4*>(tab);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) {
+    float x[8];
+    load_chunk8(base, off, is_f32, c, x);
+    uint32_t packed[4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const float4 cs = __ldg(t4 + 2 * c + hh);
+      const float4 ww = __ldg(w4 + 2 * c + hh);
+      const float n0 = x[4 * hh] * ww.x * r, n1 = x[4 * hh + 1] * ww.y * r;
+      const float n2 = x[4 * hh + 2] * ww.z * r, n3 = x[4 * hh + 3] * ww.w * r;
+      packed[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+      packed[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+    }
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
+}  // namespace st
