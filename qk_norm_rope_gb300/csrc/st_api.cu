@@ -13,7 +13,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/st_rope_attn.h"
+#include "st_rope_attn.h"
 #include "st_aux.h"
 #include "st_kernels.h"
 
@@ -195,6 +195,7 @@ struct Plan {
   int64_t m_sb = 0, m_sh = 0, m_sq = 0;
   int nQt = 0, nKt = 0, nQtm = 1;
   // workspace offsets
+  size_t off_tab16_q = 0, off_tab16_k = 0;
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
          off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
   int n_dwq = 0, n_dwk = 0;
@@ -270,10 +271,15 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
   off += 256;
   P->off_tab_q = off;
   off = align_up(off + (size_t)P->ids_q.Bt * s.Sq * kPairs * sizeof(float2), 256);
+  P->off_tab16_q = off;
+  off = align_up(off + (size_t)P->ids_q.Bt * s.Sq * kPairs * sizeof(__half2), 256);
   P->off_tab_k = P->off_tab_q;
+  P->off_tab16_k = P->off_tab16_q;
   if (P->separate_k_table) {
     P->off_tab_k = off;
     off = align_up(off + (size_t)P->ids_k.Bt * s.Skv * kPairs * sizeof(float2), 256);
+    P->off_tab16_k = off;
+    off = align_up(off + (size_t)P->ids_k.Bt * s.Skv * kPairs * sizeof(__half2), 256);
   }
   if (P->mask_kind == kMaskBool) {
     P->off_flags = off;
@@ -308,6 +314,8 @@ void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float 
   c->eps = eps;
   c->tab_q = reinterpret_cast<const float2*>(ws + P.off_tab_q);
   c->tab_k = reinterpret_cast<const float2*>(ws + P.off_tab_k);
+  c->tab16_q = reinterpret_cast<const __half2*>(ws + P.off_tab16_q);
+  c->tab16_k = reinterpret_cast<const __half2*>(ws + P.off_tab16_k);
   c->tab_q_sb = P.ids_q.Bt > 1 ? (int64_t)P.sh.Sq * kPairs : 0;
   c->tab_k_sb = P.ids_k.Bt > 1 ? (int64_t)P.sh.Skv * kPairs : 0;
   c->mask_kind = P.mask_kind;
@@ -335,7 +343,7 @@ void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float 
   c->wait_budget = wait_budget();
 }
 
-void fill_table(const Ids& ids, const st_rope* rope, float2* out, unsigned* ctrl, TableParams* t) {
+void fill_table(const Ids& ids, const st_rope* rope, float2* out, __half2* out16, unsigned* ctrl, TableParams* t) {
   memset(t, 0, sizeof(*t));
   t->ids = ids.t->data;
   t->ids_f32 = ids.t->dtype == ST_F32;
@@ -353,6 +361,7 @@ void fill_table(const Ids& ids, const st_rope* rope, float2* out, unsigned* ctrl
     }
   }
   t->out = out;
+  t->out16 = out16;
   t->ctrl = ctrl;
 }
 
@@ -366,11 +375,13 @@ st_status launch_prelude(const Plan& P, const st_rope* rope, const st_tensor* ma
                          cudaStream_t stream) {
   unsigned* ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
   TableParams t;
-  fill_table(P.ids_q, rope, reinterpret_cast<float2*>(ws + P.off_tab_q), ctrl, &t);
+  fill_table(P.ids_q, rope, reinterpret_cast<float2*>(ws + P.off_tab_q), reinterpret_cast<__half2*>(ws + P.off_tab16_q),
+             ctrl, &t);
   st_status st = cuda_check(launch_counted(ST_K_TABLE, stream, [&] { return launch_table(t, stream); }), "table kernel launch");
   if (st != ST_OK) return st;
   if (P.separate_k_table) {
-    fill_table(P.ids_k, rope, reinterpret_cast<float2*>(ws + P.off_tab_k), nullptr, &t);
+    fill_table(P.ids_k, rope, reinterpret_cast<float2*>(ws + P.off_tab_k),
+               reinterpret_cast<__half2*>(ws + P.off_tab16_k), nullptr, &t);
     if ((st = cuda_check(launch_counted(ST_K_TABLE, stream, [&] { return launch_table(t, stream); }), "table kernel launch")) != ST_OK) return st;
   }
   if (P.mask_kind == kMaskBool && P.nKt > 0 && P.nQt > 0) {

@@ -32,6 +32,7 @@ __global__ void table_kernel(const __grid_constant__ TableParams p) {
     float sn, cs;
     sincosf(static_cast<float>(red), &sn, &cs);
     p.out[e] = make_float2(cs, sn);
+    p.out16[e] = __floats2half2_rn(cs, sn);
   }
 }
 

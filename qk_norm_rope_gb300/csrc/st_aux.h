@@ -2,6 +2,7 @@
 #pragma once
 #include <algorithm>
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 #include "st_common.cuh"
 
 namespace st {
@@ -23,7 +24,8 @@ struct TableParams {
   int Bt, S;
   double omega[kPairs];      // frequency of each pair
   int axis_of[kPairs];       // axis that owns each pair
-  float2* out;               // [Bt, S, 64]
+  float2* out;               // [Bt, S, 64] (cos, sin) fp32
+  __half2* out16;            // [Bt, S, 64] (cos, sin) fp16, read by the operand prologues
   unsigned* ctrl;            // zeroed when non-null
 };
 

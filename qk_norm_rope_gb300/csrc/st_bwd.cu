@@ -35,7 +35,8 @@ constexpr uint32_t kOffDO = kOffQ + kQStages * kTileBytes;     // kQStages tiles
 constexpr uint32_t kOffDS = kOffDO + kQStages * kTileBytes;
 constexpr uint32_t kOffStat = kOffDS + kTileBytes;            // [stage][LSE*log2e | Delta][128] fp32
 constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * 128 * 4;
-constexpr uint32_t kBwdSmem = kOffBar + 256;                    // the base must be 1024-byte aligned
+constexpr uint32_t kOffW = kOffBar + 256;                       // q norm weights, fp32
+constexpr uint32_t kBwdSmem = kOffW + kD * 4;                   // the base must be 1024-byte aligned
 
 enum {
   kBarKRaw = 0,                       // raw k rows landed (TMA)
@@ -110,6 +111,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
+  float* sWq = reinterpret_cast<float*>(sm + kOffW);
+  if (tid < kD) sWq[tid] = __ldg(P.c.wq + tid);
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
     tma_prefetch_desc(&P.tmap_do);
@@ -156,20 +159,35 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const float* st_lse = stat + (n % kQStages) * 256;
       const float* st_dl = st_lse + 128;
       uint32_t pw[32];  // P^T of this warp's 64 query columns, bf16 pairs
+      // plain tiles: every query row valid, no mask values, no causal diagonal
+      const bool plain = (qt + 1) * kTile <= c.Sq && (c.mask_kind == kMaskNone || mask_bcast_q ||
+                                                      (c.mask_kind == kMaskBool && flag == kTileAllTrue)) &&
+                         (!c.causal || kt < qt);
+      const float sc = c.scale_log2;
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
         const int cbase = 64 * half + 16 * q4;  // first query column of this 16-column chunk
         uint32_t sv[16], dpv[16];
         tmem_ld16(tS + cbase, sv);
         tmem_ld16(tdP + cbase, dpv);
-        float dsv[16];
+        float lse2[16], dl[16];
 #pragma unroll
-        for (int t = 0; t < 16; ++t) {
-          const int iq = qt * kTile + cbase + t;
-          float s2 = fmaf(__uint_as_float(sv[t]), c.scale_log2, key_term);
-          const float lse2 = st_lse[cbase + t], dl = st_dl[cbase + t];
-          if (iq < c.Sq) {
-            if (!mask_bcast_q && c.mask_kind != kMaskNone && key_ok &&
+        for (int v4 = 0; v4 < 4; ++v4) {
+          const float4 a = *reinterpret_cast<const float4*>(st_lse + cbase + 4 * v4);
+          const float4 d = *reinterpret_cast<const float4*>(st_dl + cbase + 4 * v4);
+          lse2[4 * v4] = a.x; lse2[4 * v4 + 1] = a.y; lse2[4 * v4 + 2] = a.z; lse2[4 * v4 + 3] = a.w;
+          dl[4 * v4] = d.x; dl[4 * v4 + 1] = d.y; dl[4 * v4 + 2] = d.z; dl[4 * v4 + 3] = d.w;
+        }
+        float pv[16], dsv[16];
+        if (plain) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) pv[t] = ex2(fmaf(__uint_as_float(sv[t]), sc, key_term - lse2[t]));
+        } else {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            const int iq = qt * kTile + cbase + t;
+            float s2 = fmaf(__uint_as_float(sv[t]), sc, key_term);
+            if (iq < c.Sq && !mask_bcast_q && c.mask_kind != kMaskNone && key_ok &&
                 !(c.mask_kind == kMaskBool && flag == kTileAllTrue)) {
               const int64_t off = b * c.m_sb + h * c.m_sh + (int64_t)iq * c.m_sq + j;
               if (c.mask_kind == kMaskBool) {
@@ -180,13 +198,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
                 s2 = fmaf(__bfloat162float(static_cast<const __nv_bfloat16*>(c.mask)[off]), kLog2e, s2);
               }
             }
+            if (c.causal && j > iq) s2 = -INFINITY;
+            pv[t] = ex2(s2 - lse2[t]);  // lse2 = +inf for rows without keys or past S_q: P = 0
           }
-          if (c.causal && j > iq) s2 = -INFINITY;
-          const float pv = exp2f(s2 - lse2);
-          dsv[t] = pv * (__uint_as_float(dpv[t]) - dl);
-          if (t & 1) pw[8 * q4 + t / 2] = pack_bf16(__uint_as_float(sv[t - 1]), pv);
-          else sv[t] = __float_as_uint(pv);  // keep p of the even column for the pair
         }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) dsv[t] = pv[t] * (__uint_as_float(dpv[t]) - dl[t]);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) pw[8 * q4 + t] = pack_bf16(pv[2 * t], pv[2 * t + 1]);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {  // dS^T row r, query columns cbase + 8u .. +7
           const int chunk = (cbase >> 3) + u;  // 16-byte chunk 0..15 along the query dimension
@@ -323,7 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const float2* tab = c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs;
       if (P.qk_tma) {
         ok = wait_bar(&bars[kBarKRaw], 0, abort_flag, budget);
-        if (ok && j < c.Skv) rope_norm_inplace(sm + kOffK, p, c.wk, c.eps, tab);  // rows past S_kv stay zero
+        if (ok && j < c.Skv)  // rows past S_kv stay zero
+          rope_norm_inplace(sm + kOffK, p, c.wk, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs);
       } else if (j < c.Skv) {
         rope_norm_global(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps, tab,
                          sm + kOffK, p);
@@ -343,7 +363,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       const float2* tab = c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs;
       if (P.qk_tma) {
         if (!wait_bar(&bars[kBarQRaw + s], (n / kQStages) & 1, abort_flag, budget)) break;
-        if (i < c.Sq) rope_norm_inplace(tile, p, c.wq, c.eps, tab);
+        if (i < c.Sq) rope_norm_inplace(tile, p, sWq, c.eps, c.tab16_q + b * c.tab_q_sb + (int64_t)i * kPairs);
       } else {
         if (n >= kQStages && !wait_bar(&bars[kBarStageEmpty + s], ((n / kQStages) - 1) & 1, abort_flag, budget))
           break;

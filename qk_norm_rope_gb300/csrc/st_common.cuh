@@ -2,6 +2,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include "st_ptx.cuh"
 
 namespace st {
@@ -39,6 +40,8 @@ struct Common {
   const float2* tab_q;  // [Bt_q, Sq, 64] (cos, sin)
   const float2* tab_k;  // [Bt_k, Skv, 64]
   int64_t tab_q_sb, tab_k_sb;  // batch stride in float2 (0 when shared by the batch)
+  const __half2* tab16_q;      // the same tables in fp16 (same strides), for the prologues
+  const __half2* tab16_k;
   int mask_kind;
   const void* mask;            // element (b,h,i,j) at b*m_sb + h*m_sh + i*m_sq + j
   int64_t m_sb, m_sh, m_sq;    // 0 on broadcast dims

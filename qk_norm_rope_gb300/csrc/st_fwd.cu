@@ -40,7 +40,8 @@ constexpr uint32_t kOffQ = 0;                                  // 2 tiles
 constexpr uint32_t kOffK = 2 * kTileBytes;                     // kStages tiles
 constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;       // kStages tiles
 constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-constexpr uint32_t kFwdSmem = kOffBar + 256 + 1024;
+constexpr uint32_t kOffW = kOffBar + 256;                      // q and k norm weights, fp32
+constexpr uint32_t kFwdSmem = kOffW + 2 * kD * 4 + 1024;
 
 enum {
   kBarQRaw = 0,                       // raw q rows landed (TMA)
@@ -68,6 +69,9 @@ __device__ __forceinline__ uint8_t tile_flag(const Common& c, int b, int h, int 
   if (c.mask_kind == kMaskNone) return kTileAllTrue;
   return kTileMixed;  // additive masks are always applied
 }
+
+__device__ __forceinline__ float c_wq(const Common& c, int d) { return __ldg(c.wq + d); }
+__device__ __forceinline__ float c_wk(const Common& c, int d) { return __ldg(c.wk + d); }
 
 // Next key tile at or after kt that at least one of the two query tiles needs.
 __device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0, int kt, int kt_end) {
@@ -157,6 +161,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     *abort_flag = 0;
     fence_mbar_init();
   }
+  float* sW = reinterpret_cast<float*>(sm + kOffW);  // [wq | wk]
+  if (tid < 2 * kD) sW[tid] = tid < kD ? c_wq(P.c, tid) : c_wk(P.c, tid - kD);
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
     if (P.qk_tma) {
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         uint8_t* tile = sm + kOffQ + ti * kTileBytes;
         const float2* tab = c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs;
         if (P.qk_tma) {
-          if (i < c.Sq) rope_norm_inplace(tile, p, c.wq, c.eps, tab);  // rows past S_q stay TMA zeros
+          if (i < c.Sq) rope_norm_inplace(tile, p, sW, c.eps, c.tab16_q + b * c.tab_q_sb + (int64_t)i * kPairs);
         } else if (i < c.Sq) {
           rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps, tab, tile,
                            p);
@@ -335,7 +341,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const float2* tab = c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs;
       if (P.qk_tma) {
         if (!wait_bar(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
-        if (j < c.Skv) rope_norm_inplace(tile, p, c.wk, c.eps, tab);
+        if (j < c.Skv) rope_norm_inplace(tile, p, sW + kD, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs);
       } else {
         if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
         if (j < c.Skv)

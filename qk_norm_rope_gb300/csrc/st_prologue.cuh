@@ -86,9 +86,15 @@ struct RowPrologue {
 // bf16 rows (128B-swizzled, the operand layout): the thread reads its row,
 // normalises and rotates it, and writes the bf16 result back in place. The
 // swizzle makes eight consecutive rows hit eight different bank groups, so
-// the 16-byte accesses are conflict-free. tab: the row's 64 (cos, sin).
-__device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const float* __restrict__ w, float eps,
-                                                  const float2* __restrict__ tab) {
+// the 16-byte accesses are conflict-free. tab16: the row's 64 (cos, sin) in
+// fp16 (16 loads of 16 bytes, all issued before the arithmetic); w: the norm
+// weights in shared memory.
+__device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const float* w, float eps,
+                                                  const __half2* __restrict__ tab16) {
+  uint4 cs[kD / 8];  // (cos, sin) of pairs 4c .. 4c+3, fp16
+  const uint4* t16 = reinterpret_cast<const uint4*>(tab16);
+#pragma unroll
+  for (int c = 0; c < kD / 8; ++c) cs[c] = __ldg(t16 + c);
   float a0 = 0.f, a1 = 0.f;
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c) {
@@ -102,22 +108,21 @@ __device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const 
     }
   }
   const float r = rsqrtf((a0 + a1) * (1.0f / kD) + eps);
-  const float4* t4 = reinterpret_cast<const float4*>(tab);
   const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll 2
+#pragma unroll
   for (int c = 0; c < kD / 8; ++c) {
     uint4* p16 = reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7));
     const uint4 v = *p16;
     const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t t[4] = {cs[c].x, cs[c].y, cs[c].z, cs[c].w};
+    const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
+    const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
     uint32_t out[4];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float4 cs = __ldg(t4 + 2 * c + hh);  // (cos, sin) of two pairs
-      const float4 ww = __ldg(w4 + 2 * c + hh);
-      const float n0 = bf16_lo(u[2 * hh]) * ww.x * r, n1 = bf16_hi(u[2 * hh]) * ww.y * r;
-      const float n2 = bf16_lo(u[2 * hh + 1]) * ww.z * r, n3 = bf16_hi(u[2 * hh + 1]) * ww.w * r;
-      out[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
-      out[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+    for (int e = 0; e < 4; ++e) {  // pair 4c + e
+      const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
+      const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
+      out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
     }
     *p16 = make_uint4(out[0], out[1], out[2], out[3]);
   }
