@@ -286,6 +286,20 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// 2^x on the FMA and integer pipes, for finite x (clamped below at -126, where
+// the result is ~1e-38): x = n + f with n = round(x) taken from the low
+// mantissa bits of x + 1.5*2^23 (no conversion instruction), 2^f from a cubic
+// fitted on [-1/2, 1/2] (coefficients from csrc/derive_exp2_poly.py, maximum
+// relative error 7.6e-5), and n added to the exponent field. Used for a share
+// of the softmax exponentials so that the MUFU unit is not the bottleneck.
+__device__ __forceinline__ float ex2_fma(float x) {
+  x = fmaxf(x, -126.0f);
+  const float t = x + 12582912.0f;
+  const float f = x - (t - 12582912.0f);
+  const float p = fmaf(fmaf(fmaf(5.521666631e-02f, f, 2.426148951e-01f), f, 6.932526827e-01f), f, 9.999276400e-01f);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
+
 __device__ __forceinline__ void record_timeout(const Common& c) {
   atomicOr(c.status, kStatusTimeout);
   atomicAdd(c.counters + kCtrTimeouts, 1ull);

@@ -6,12 +6,14 @@
 //               32*(w%4).. (one thread per query row); two passes over the
 //               row's 128 scores in TMEM: the max of the raw scores, then
 //               P = exp2(s*scale*log2e - max) with the scale folded into one FMA
-//   warps 8-11  operand prologue, one thread per row: Q' for both query tiles,
-//               then K' for every key tile of a kStages-deep ring; bf16 rows
-//               arrive by TMA in the operand layout and are normalised and
-//               rotated in place (fp32 rows are read from global memory)
-//   warp 12     TMEM allocation + tcgen05.mma issue (one thread)
-//   warp 13     TMA: raw Q and K rows, V tiles
+//   warps 8-15  operand prologue, two lanes per row (one per 64-column half):
+//               Q' for both query tiles, then K' for every key tile of a
+//               kStages-deep ring; bf16 rows arrive by TMA in the operand
+//               layout and are normalised and rotated in place, their (cos,
+//               sin) rows being fetched while the TMA is in flight (fp32 rows
+//               are read from global memory, one thread per row)
+//   warp 16     TMEM allocation + tcgen05.mma issue (one thread)
+//   warp 17     TMA: raw Q and K rows, V tiles
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_i (bf16)
 // overwrites the first 64 columns of S_i and feeds PV from TMEM.
 // MMA issue order per key tile n: PV0(n-1), S0(n), PV1(n-1), S1(n), so that
@@ -27,9 +29,9 @@ namespace {
 
 constexpr int kStages = 2;
 constexpr int kSoftWarps = 8;
-constexpr int kWarpProl0 = 8, kProlWarps = 4;
-constexpr int kWarpMma = 12, kWarpTma = 13;
-constexpr int kFwdWarps = 14;
+constexpr int kWarpProl0 = 8, kProlWarps = 8;
+constexpr int kWarpMma = 16, kWarpTma = 17;
+constexpr int kFwdWarps = 18;
 constexpr int kFwdThreads = kFwdWarps * 32;
 // rescale O only when the running max grows by more than 8 (base 2); exact
 // either way since O and l always share the same reference max
@@ -247,9 +249,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tmem_ld32(tS + 32 * q4, raw);
         if (plain) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
+          for (int t = 0; t < 16; ++t) {  // one score in four takes the FMA-pipe exponential
             const float p0 = ex2(fmaf(__uint_as_float(raw[2 * t]), sc, -m_use));
-            const float p1 = ex2(fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use));
+            const float x1 = fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use);
+            const float p1 = (t & 1) ? ex2_fma(x1) : ex2(x1);
             ls0 += p0;
             ls1 += p1;
             pw[t] = pack_bf16(p0, p1);
@@ -311,22 +314,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
   } else if (warp < kWarpProl0 + kProlWarps) {
     // ------------------------------------------------------------ operand prologue
-    const int p = tid - kWarpProl0 * 32;  // row of the tile handled by this thread
+    const int p = tid - kWarpProl0 * 32;                      // 0..255
+    const int prow = (p >> 5) * 16 + (lane_id & 15), hh = lane_id >> 4;  // TMA path: half-row
     bool ok = true;
     if (P.qk_tma) ok = wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
     if (ok) {
 #pragma unroll 1
       for (int ti = 0; ti < 2; ++ti) {
-        const int i = (qt0 + ti) * kTile + p;
         uint8_t* tile = sm + kOffQ + ti * kTileBytes;
-        const float2* tab = c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs;
         if (P.qk_tma) {
-          if (i < c.Sq) rope_norm_inplace(tile, p, sW, c.eps, c.tab16_q + b * c.tab_q_sb + (int64_t)i * kPairs);
-        } else if (i < c.Sq) {
-          rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps, tab, tile,
-                           p);
-        } else {
-          zero_row(tile, p);
+          const int i = (qt0 + ti) * kTile + prow;  // rows past S_q stay TMA zeros
+          HalfRowPrologue hp;
+          if (i < c.Sq) {
+            const __half2* t16 = c.tab16_q + b * c.tab_q_sb + (int64_t)i * kPairs;
+            hp.prefetch(t16, hh);
+            hp.prefetch2(t16, hh);
+          }
+          hp.finish(tile, prow, hh, sW, c.eps, i < c.Sq);
+        } else if (p < kTile) {
+          const int i = (qt0 + ti) * kTile + p;
+          if (i < c.Sq)
+            rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
+                             c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, tile, p);
+          else
+            zero_row(tile, p);
         }
       }
       fence_proxy_async_smem();
@@ -337,18 +348,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
          kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
       const int slot = n % kStages;
       uint8_t* tile = sm + kOffK + slot * kTileBytes;
-      const int j = kt * kTile + p;
-      const float2* tab = c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs;
       if (P.qk_tma) {
+        const int j = kt * kTile + prow;
+        HalfRowPrologue hp;
+        if (j < c.Skv) {
+          const __half2* t16 = c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs;
+          hp.prefetch(t16, hh);
+          hp.prefetch2(t16, hh);
+        }
         if (!wait_bar(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
-        if (j < c.Skv) rope_norm_inplace(tile, p, sW + kD, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs);
+        hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
       } else {
         if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
-        if (j < c.Skv)
-          rope_norm_global(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps, tab, tile,
-                           p);
-        else
-          zero_row(tile, p);
+        if (p < kTile) {
+          const int j = kt * kTile + p;
+          if (j < c.Skv)
+            rope_norm_global(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps,
+                             c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs, tile, p);
+          else
+            zero_row(tile, p);
+        }
       }
       fence_proxy_async_smem();
       mbar_arrive(&bars[kBarKFull + slot]);

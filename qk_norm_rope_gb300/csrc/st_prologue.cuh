@@ -128,6 +128,64 @@ __device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const 
   }
 }
 
+// Half-row variant: two lanes of a warp (l and l ^ 16) share one row; lane
+// half `hh` owns head dims [64*hh, 64*hh + 64) = the 64-column half `hh` of the
+// swizzled tile. The (cos, sin) loads are issued by prefetch() before the raw
+// rows are known to have landed; finish() waits for nothing itself.
+struct HalfRowPrologue {
+  uint4 cs[4];  // (cos, sin) fp16 of this lane's 32 pairs
+  __device__ __forceinline__ void prefetch(const __half2* __restrict__ tab16_row, int hh) {
+    const uint4* t16 = reinterpret_cast<const uint4*>(tab16_row) + 8 * hh;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cs[c] = __ldg(t16 + c);
+  }
+  __device__ __forceinline__ void prefetch2(const __half2* __restrict__ tab16_row, int hh) {
+    const uint4* t16 = reinterpret_cast<const uint4*>(tab16_row) + 8 * hh + 4;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cs2[c] = __ldg(t16 + c);
+  }
+  uint4 cs2[4];
+  // valid: the row exists (both lanes of the row agree); w: the half's 64 weights
+  __device__ __forceinline__ void finish(uint8_t* tile, int row, int hh, const float* w, float eps, bool valid) const {
+    uint8_t* half = tile + hh * kHalfBytes;
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = *reinterpret_cast<const uint4*>(half + sw128_off(row, c));
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
+        a0 = fmaf(lo, lo, a0);
+        a1 = fmaf(hi, hi, a1);
+      }
+    }
+    float ss = a0 + a1;
+    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
+    if (!valid) return;
+    const float r = rsqrtf(ss * (1.0f / kD) + eps);
+    const float4* w4 = reinterpret_cast<const float4*>(w + 64 * hh);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      uint4* p16 = reinterpret_cast<uint4*>(half + sw128_off(row, c));
+      const uint4 v = *p16;
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      const uint4 tc = c < 4 ? cs[c] : cs2[c - 4];
+      const uint32_t t[4] = {tc.x, tc.y, tc.z, tc.w};
+      const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      uint32_t out[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
+        const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
+        out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
+      }
+      *p16 = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+  }
+};
+
 // Thread-per-row prologue reading the raw row (bf16 or fp32) from global
 // memory; used when q/k are fp32 (no in-place TMA staging) and for rows that
 // a TMA load does not cover. The raw row is read twice (sum of squares, then
