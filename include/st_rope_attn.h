@@ -218,6 +218,13 @@ ST_API void st_reset_stats(void);
 ST_API st_status st_timing_enable(int on);
 ST_API st_status st_timing_read(st_kernel_times* out);
 
+/* Self-test of the bounded-wait mechanism: enqueues one tiny kernel that waits
+ * on an mbarrier nothing arrives on and gives up after `budget_cycles`
+ * (clock64 cycles, 1..2^34), recording a timeout exactly as the attention
+ * kernels do. The next st_check_status() then returns ST_ERR_TIMEOUT and the
+ * CUDA context stays usable. */
+ST_API st_status st_selftest_wait_timeout(long long budget_cycles, void* stream);
+
 /* Synchronises `stream` and reports ST_ERR_TIMEOUT if any kernel recorded a
  * bounded-wait timeout since the previous check (the record is then cleared),
  * or ST_ERR_CUDA if the stream holds an error. For tests and debugging. */

@@ -89,6 +89,8 @@ def lib():
             L.st_check_status.restype = i
             L.st_rope_attn_fwd_noalloc.argtypes = [T, T, T, T, T, fl, R, T, i, fl, T, T, vp]
             L.st_rope_attn_fwd_noalloc.restype = i
+            L.st_selftest_wait_timeout.argtypes = [ctypes.c_longlong, vp]
+            L.st_selftest_wait_timeout.restype = i
             L.st_timing_enable.argtypes = [i]
             L.st_timing_enable.restype = i
             L.st_timing_read.argtypes = [ctypes.POINTER(st_kernel_times)]
@@ -237,6 +239,11 @@ def st_reset_stats() -> None:
 def st_check_status(stream=None) -> None:
     h = ctypes.c_void_p(stream.cuda_stream if stream is not None else torch.cuda.current_stream().cuda_stream)
     _check(lib().st_check_status(h))
+
+
+def st_selftest_wait_timeout(budget_cycles: int) -> None:
+    """Enqueues the bounded-wait self-test (see the C header)."""
+    _check(lib().st_selftest_wait_timeout(int(budget_cycles), _stream()))
 
 
 def st_timing_enable(on: bool) -> None:

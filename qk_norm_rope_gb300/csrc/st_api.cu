@@ -429,10 +429,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 4-D tiled map over a bf16 [B, S, H, D] tensor for 64-column x 128-row boxes
+// 4-D tiled map over a bf16 [B, S, H, D] tensor for 64-column x box_rows boxes
 // with 128-byte swizzle. The two middle dims are ordered by stride (s before h
 // when the sequence stride is the smaller one, as in a BHSD view).
-st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first) {
+st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, int box_rows = kTile) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int64_t B = t->shape[0], S = t->shape[1], H = t->shape[2];
@@ -449,9 +449,9 @@ st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first) {
   cuuint32_t box[4] = {64, 1, 1, 1}, es[4] = {1, 1, 1, 1};
   dims[0] = kD;
   if (*s_first) {
-    dims[1] = S; dims[2] = H; strides[0] = ss; strides[1] = sh; box[1] = kTile;
+    dims[1] = S; dims[2] = H; strides[0] = ss; strides[1] = sh; box[1] = box_rows;
   } else {
-    dims[1] = H; dims[2] = S; strides[0] = sh; strides[1] = ss; box[2] = kTile;
+    dims[1] = H; dims[2] = S; strides[0] = sh; strides[1] = ss; box[2] = box_rows;
   }
   dims[3] = B;
   strides[2] = sb;
@@ -754,6 +754,19 @@ st_status st_get_stats(st_stats* out) {
   out->timeouts = c[kCtrTimeouts];
   out->kernel_launches = h_launches.load();
   return ST_OK;
+}
+
+st_status st_selftest_wait_timeout(long long budget_cycles, void* stream_) {
+  if (budget_cycles < 1 || budget_cycles > (1ll << 34)) return fail(ST_ERR_INVALID_ARG, "budget out of range");
+  Dev dev;
+  st_status st = device_globals(&dev);
+  if (st != ST_OK) return st;
+  return cuda_check(launch_counted(ST_K_TABLE + 7, static_cast<cudaStream_t>(stream_),
+                                   [&] {
+                                     return launch_wait_probe(dev.status, dev.counters, budget_cycles,
+                                                              static_cast<cudaStream_t>(stream_));
+                                   }),
+                    "wait probe launch");
 }
 
 st_status st_timing_enable(int on) {

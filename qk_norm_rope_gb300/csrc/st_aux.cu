@@ -158,7 +158,27 @@ __global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ 
   }
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier that nothing
+// ever arrives on, gives up after `budget` clock64 cycles and records the
+// timeout exactly as the attention kernels do.
+__global__ void wait_probe_kernel(unsigned* status, unsigned long long* counters, long long budget) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    if (!mbar_wait(&bar, 0, budget)) {
+      atomicOr(status, kStatusTimeout);
+      atomicAdd(counters + kCtrTimeouts, 1ull);
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(unsigned* status, unsigned long long* counters, long long budget, cudaStream_t stream) {
+  wait_probe_kernel<<<1, 32, 0, stream>>>(status, counters, budget);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_table(const TableParams& p, cudaStream_t stream) {
   const int64_t n = (int64_t)p.Bt * p.S * kPairs;

@@ -78,5 +78,6 @@ cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream);
 cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream);
+cudaError_t launch_wait_probe(unsigned* status, unsigned long long* counters, long long budget, cudaStream_t stream);
 
 }  // namespace st

@@ -224,26 +224,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) bwd_kernel(const __grid_consta
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars[kBarPdSFull]);
-      // ---- dQ drain: lane = query row qt*128 + r, columns [64*half, +64)
+      // ---- dQ drain: lane = query row qt*128 + r, columns [64*half, +64). The
+      // slice is read into registers and the S columns are released before the
+      // reduction into the fp32 accumulator is issued, so the next S^T MMA does
+      // not wait for the atomic traffic.
       if (!(ok = wait_bar(&bars[kBarDQFull], n & 1, abort_flag, budget))) break;
       tc_fence_after();
-      const int iq = qt * kTile + r;
-#pragma unroll 1
-      for (int q2 = 0; q2 < 2; ++q2) {
-        const int d0 = 64 * half + 32 * q2;
-        uint32_t v[32];
-        tmem_ld32(tS + d0, v);
-        if (iq < c.Sq) {
-          float4* dst = reinterpret_cast<float4*>(P.dq_acc + (((int64_t)b * c.Sq + iq) * c.H + h) * kD + d0);
-#pragma unroll
-          for (int t = 0; t < 32; t += 4)
-            atomicAdd(dst + t / 4, make_float4(__uint_as_float(v[t]) * c.scale, __uint_as_float(v[t + 1]) * c.scale,
-                                               __uint_as_float(v[t + 2]) * c.scale,
-                                               __uint_as_float(v[t + 3]) * c.scale));
-        }
-      }
+      uint32_t dq0[32], dq1[32];
+      tmem_ld32(tS + 64 * half, dq0);
+      tmem_ld32(tS + 64 * half + 32, dq1);
       tc_fence_before();
       mbar_arrive(&bars[kBarSFree]);
+      const int iq = qt * kTile + r;
+      if (iq < c.Sq) {
+        float* dst = P.dq_acc + (((int64_t)b * c.Sq + iq) * c.H + h) * kD + 64 * half;
+        const float sc2 = c.scale;
+#pragma unroll
+        for (int t = 0; t < 32; t += 4)
+          red_add_v4(dst + t, __uint_as_float(dq0[t]) * sc2, __uint_as_float(dq0[t + 1]) * sc2,
+                     __uint_as_float(dq0[t + 2]) * sc2, __uint_as_float(dq0[t + 3]) * sc2);
+#pragma unroll
+        for (int t = 0; t < 32; t += 4)
+          red_add_v4(dst + 32 + t, __uint_as_float(dq1[t]) * sc2, __uint_as_float(dq1[t + 1]) * sc2,
+                     __uint_as_float(dq1[t + 2]) * sc2, __uint_as_float(dq1[t + 3]) * sc2);
+      }
     }
     processed = n;
     // ---- epilogue: warps 0-3 write dV, warps 4-7 dK (+ k-norm weight partials)

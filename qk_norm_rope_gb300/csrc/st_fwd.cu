@@ -65,10 +65,11 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return sdesc_sw128(base + kk * 2048, kHalfBytes, 1024);
 }
 
+template <int MK>
 __device__ __forceinline__ uint8_t tile_flag(const Common& c, int b, int h, int qt, int kt) {
   if (qt >= c.nQt) return kTileAllFalse;
-  if (c.mask_kind == kMaskBool) return c.flags[b * c.f_sb + h * c.f_sh + qt * c.f_sq + kt];
-  if (c.mask_kind == kMaskNone) return kTileAllTrue;
+  if constexpr (MK == kMaskBool) return c.flags[b * c.f_sb + h * c.f_sh + qt * c.f_sq + kt];
+  if constexpr (MK == kMaskNone) return kTileAllTrue;
   return kTileMixed;  // additive masks are always applied
 }
 
@@ -76,10 +77,11 @@ __device__ __forceinline__ float c_wq(const Common& c, int d) { return __ldg(c.w
 __device__ __forceinline__ float c_wk(const Common& c, int d) { return __ldg(c.wk + d); }
 
 // Next key tile at or after kt that at least one of the two query tiles needs.
+template <int MK>
 __device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0, int kt, int kt_end) {
-  if (c.mask_kind != kMaskBool) return kt;
+  if constexpr (MK != kMaskBool) return kt;
   for (; kt < kt_end; ++kt)
-    if (tile_flag(c, b, h, qt0, kt) != kTileAllFalse || tile_flag(c, b, h, qt0 + 1, kt) != kTileAllFalse) break;
+    if (tile_flag<MK>(c, b, h, qt0, kt) != kTileAllFalse || tile_flag<MK>(c, b, h, qt0 + 1, kt) != kTileAllFalse) break;
   return kt;
 }
 
@@ -87,6 +89,7 @@ __device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0,
 // TMEM values: s * scale * log2(e) (+ mask * log2(e)), -inf where a bool mask
 // is False, beyond the causal diagonal or at keys >= S_kv. Tiles that need no
 // masking take the caller's fast path instead.
+template <int MK, bool CAUSAL>
 __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t (&raw)[32], int b, int h, int i,
                                                 int j0, uint8_t flag, uint32_t mbits, float (&s)[32]) {
 #pragma unroll
@@ -96,20 +99,20 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
     for (int t = 0; t < 32; ++t) s[t] = -INFINITY;
     return;
   }
-  if (c.mask_kind == kMaskBool) {
+  if constexpr (MK == kMaskBool) {
     if (flag == kTileMixed) {
 #pragma unroll
       for (int t = 0; t < 32; ++t)
         if (!((mbits >> t) & 1u)) s[t] = -INFINITY;
     }
-  } else if (c.mask_kind == kMaskF32) {
+  } else if constexpr (MK == kMaskF32) {
     if (i < c.Sq) {
       const float* mrow = static_cast<const float*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
 #pragma unroll
       for (int t = 0; t < 32; ++t)
         if (j0 + t < c.Skv) s[t] = fmaf(__ldg(mrow + t), kLog2e, s[t]);
     }
-  } else if (c.mask_kind == kMaskBF16) {
+  } else if constexpr (MK == kMaskBF16) {
     if (i < c.Sq) {
       const __nv_bfloat16* mrow =
           static_cast<const __nv_bfloat16*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
@@ -118,7 +121,7 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
         if (j0 + t < c.Skv) s[t] = fmaf(__bfloat162float(mrow[t]), kLog2e, s[t]);
     }
   }
-  if (c.causal) {
+  if constexpr (CAUSAL) {
 #pragma unroll
     for (int t = 0; t < 32; ++t)
       if (j0 + t > i) s[t] = -INFINITY;
@@ -130,6 +133,7 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
   }
 }
 
+template <int MK, bool CAUSAL, bool QKT>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,7 +171,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   if (tid < 2 * kD) sW[tid] = tid < kD ? c_wq(P.c, tid) : c_wk(P.c, tid - kD);
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
-    if (P.qk_tma) {
+    if constexpr (QKT) {
       tma_prefetch_desc(&P.tmap_q);
       tma_prefetch_desc(&P.tmap_k);
     }
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const uint32_t tmem = *tslot;
 
   int kt_end = c.nKt;
-  if (c.causal) kt_end = min(c.nKt, (qt0 * kTile + 2 * kTile - 1) / kTile + 1);
+  if (CAUSAL) kt_end = min(c.nKt, (qt0 * kTile + 2 * kTile - 1) / kTile + 1);
   const long long budget = c.wait_budget;
 
   if (warp < kSoftWarps) {
@@ -192,15 +196,15 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0, useful = 0;
     bool ok = true;
-    for (int kt = next_tile(c, b, h, qt0, 0, kt_end); kt < kt_end; kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
-      const uint8_t flag = tile_flag(c, b, h, qt0 + ti, kt);
-      useful += (flag != kTileAllFalse && (!c.causal || kt <= qt0 + ti)) ? 1 : 0;
+    for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); kt < kt_end; kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
+      const uint8_t flag = tile_flag<MK>(c, b, h, qt0 + ti, kt);
+      useful += (flag != kTileAllFalse && (!CAUSAL || kt <= qt0 + ti)) ? 1 : 0;
       const int j0 = kt * kTile;
       // plain tiles: no mask values, no causal diagonal, no key bound inside
-      const bool plain = (flag == kTileAllTrue || (c.mask_kind == kMaskNone && flag != kTileAllFalse)) &&
-                         (!c.causal || j0 + kTile - 1 <= (qt0 + ti) * kTile) && j0 + kTile <= c.Skv;
+      const bool plain = (flag == kTileAllTrue || (MK == kMaskNone && flag != kTileAllFalse)) &&
+                         (!CAUSAL || j0 + kTile - 1 <= (qt0 + ti) * kTile) && j0 + kTile <= c.Skv;
       uint32_t mbits[4] = {~0u, ~0u, ~0u, ~0u};
-      if (c.mask_kind == kMaskBool && flag == kTileMixed && i < c.Sq) {
+      if (MK == kMaskBool && flag == kTileMixed && i < c.Sq) {
         const uint8_t* mrow = static_cast<const uint8_t*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
         const int nvalid = min(kTile, c.Skv - j0);
 #pragma unroll
@@ -230,7 +234,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           mt = fmaxf(mt, fmaxf(m0, m1) * sc);
         } else {
           float sv[32];
-          masked_scores32(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
+          masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
 #pragma unroll
           for (int t = 0; t < 32; ++t) mt = fmaxf(mt, sv[t]);
         }
@@ -249,17 +253,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tmem_ld32(tS + 32 * q4, raw);
         if (plain) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {  // one score in four takes the FMA-pipe exponential
+          for (int t = 0; t < 16; ++t) {
             const float p0 = ex2(fmaf(__uint_as_float(raw[2 * t]), sc, -m_use));
-            const float x1 = fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use);
-            const float p1 = (t & 1) ? ex2_fma(x1) : ex2(x1);
+            const float p1 = ex2(fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use));
             ls0 += p0;
             ls1 += p1;
             pw[t] = pack_bf16(p0, p1);
           }
         } else {
           float sv[32];
-          masked_scores32(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
+          masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const float p0 = ex2(sv[2 * t] - m_use), p1 = ex2(sv[2 * t + 1] - m_use);
@@ -317,12 +320,12 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int p = tid - kWarpProl0 * 32;                      // 0..255
     const int prow = (p >> 5) * 16 + (lane_id & 15), hh = lane_id >> 4;  // TMA path: half-row
     bool ok = true;
-    if (P.qk_tma) ok = wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+    if constexpr (QKT) ok = wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
     if (ok) {
 #pragma unroll 1
       for (int ti = 0; ti < 2; ++ti) {
         uint8_t* tile = sm + kOffQ + ti * kTileBytes;
-        if (P.qk_tma) {
+        if constexpr (QKT) {
           const int i = (qt0 + ti) * kTile + prow;  // rows past S_q stay TMA zeros
           HalfRowPrologue hp;
           if (i < c.Sq) {
@@ -344,11 +347,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars[kBarQFull]);
     }
     int n = 0;
-    for (int kt = next_tile(c, b, h, qt0, 0, kt_end); ok && kt < kt_end;
-         kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
+    for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); ok && kt < kt_end;
+         kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
       const int slot = n % kStages;
       uint8_t* tile = sm + kOffK + slot * kTileBytes;
-      if (P.qk_tma) {
+      if constexpr (QKT) {
         const int j = kt * kTile + prow;
         HalfRowPrologue hp;
         if (j < c.Skv) {
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: raw Q, raw K, V
     if (lane_id == 0) {
-      if (P.qk_tma) {
+      if constexpr (QKT) {
         mbar_arrive_expect_tx(&bars[kBarQRaw], 2 * kTileBytes);
 #pragma unroll 1
         for (int ti = 0; ti < 2; ++ti) {
@@ -387,11 +390,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         }
       }
       int n = 0;
-      for (int kt = next_tile(c, b, h, qt0, 0, kt_end); kt < kt_end;
-           kt = next_tile(c, b, h, qt0, kt + 1, kt_end), ++n) {
+      for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); kt < kt_end;
+           kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
         const int slot = n % kStages;
         if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
-        if (P.qk_tma) {
+        if constexpr (QKT) {
           uint8_t* ktile = sm + kOffK + slot * kTileBytes;
           const int y = P.k_s_first ? kt * kTile : h, z = P.k_s_first ? h : kt * kTile;
           mbar_arrive_expect_tx(&bars[kBarKRaw + slot], kTileBytes);
@@ -405,10 +408,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tma_load_4d(tile + kHalfBytes, &P.tmap_v, &bars[kBarVFull + slot], 64, y, z, b);
       }
       // every issued load lands before the CTA exits
-      if (P.qk_tma) wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+      if constexpr (QKT) wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
       for (int m = max(0, n - kStages); m < n; ++m) {
         wait_bar(&bars[kBarVFull + m % kStages], (m / kStages) & 1, abort_flag, budget);
-        if (P.qk_tma) wait_bar(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, abort_flag, budget);
+        if constexpr (QKT) wait_bar(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, abort_flag, budget);
       }
     }
   } else if (warp == kWarpMma) {
@@ -419,7 +422,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const uint32_t aQ0 = smem_u32(sm + kOffQ), aQ1 = aQ0 + kTileBytes;
       const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
       bool ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
-      int kt = next_tile(c, b, h, qt0, 0, kt_end);
+      int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end);
       int n = 0;
       bool issued = false;
       if (ok && kt < kt_end) {
@@ -438,7 +441,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       while (ok && kt < kt_end) {
         const int slot = n % kStages;
-        const int kt_next = next_tile(c, b, h, qt0, kt + 1, kt_end);
+        const int kt_next = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end);
         const bool has_next = kt_next < kt_end;
         const int nslot = (n + 1) % kStages;
         const uint32_t aV = smem_u32(sm + kOffV + slot * kTileBytes);
@@ -492,18 +495,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
+template <int MK, bool CAUSAL, bool QKT>
+cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
+  auto kern = fwd_kernel<MK, CAUSAL, QKT>;
   static unsigned configured = 0;
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured & (1u << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
     if (e != cudaSuccess) return e;
     configured |= 1u << (dev & 31);
   }
   dim3 grid((p.c.nQt + 1) / 2, p.c.H, p.c.B);
-  fwd_kernel<<<grid, kFwdThreads, kFwdSmem, stream>>>(p);
+  kern<<<grid, kFwdThreads, kFwdSmem, stream>>>(p);
   return cudaGetLastError();
+}
+
+template <bool QKT>
+cudaError_t launch_fwd_q(const FwdParams& p, cudaStream_t stream) {
+  if (p.c.causal) return launch_fwd_t<kMaskNone, true, QKT>(p, stream);  // masks and causal never combine
+  switch (p.c.mask_kind) {
+    case kMaskBool: return launch_fwd_t<kMaskBool, false, QKT>(p, stream);
+    case kMaskF32: return launch_fwd_t<kMaskF32, false, QKT>(p, stream);
+    case kMaskBF16: return launch_fwd_t<kMaskBF16, false, QKT>(p, stream);
+    default: return launch_fwd_t<kMaskNone, false, QKT>(p, stream);
+  }
+}
+
+// Kernels are specialised on the mask kind, causal masking and whether q/k
+// are staged by TMA, so that each carries only its own code.
+cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
+  return p.qk_tma ? launch_fwd_q<true>(p, stream) : launch_fwd_q<false>(p, stream);
 }
 
 }  // namespace st

@@ -149,7 +149,9 @@ def test_strided_views_bhsd_and_fused_qkv(cuda_lib):
     ref = gpu_fwd_bwd(cuda_lib, base, d=d)
     for k in ("o", "lse", "dk", "dv", "dwk"):
         assert torch.equal(got[k], ref[k]), k
-    compare("dq", got["dq"], ref["dq"].double().cpu().numpy(), atol=1e-3, rel_fro=1e-4)
+    # dq is bf16 and its fp32 accumulation order (atomic adds across key tiles)
+    # differs between runs, so single elements may differ by one bf16 ulp
+    compare("dq", got["dq"], ref["dq"].double().cpu().numpy(), atol=1e-2, rel_fro=1e-3)
 
 
 def test_all_true_mask_is_identical_to_no_mask(cuda_lib):
@@ -220,3 +222,14 @@ def test_autograd_function(cuda_lib):
     compare("o", o, ref["o"])
     for name, t in (("dq", q), ("dk", k), ("dv", v), ("dwq", wq), ("dwk", wk)):
         compare(name, t.grad, ref[name], check_max=name not in ("dwq", "dwk"))
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
+    before = cuda_lib.st_get_stats()["timeouts"]
+    cuda_lib.st_selftest_wait_timeout(2_000_000)  # ~1 ms of clock64 cycles
+    with pytest.raises(cuda_lib.StError) as ei:
+        cuda_lib.st_check_status()
+    assert ei.value.status == cuda_lib.ST_ERR_TIMEOUT
+    assert cuda_lib.st_get_stats()["timeouts"] == before + 1
+    cuda_lib.st_check_status()  # the record is cleared
+    run_case(cuda_lib, wl.make("tiny_flux"))  # and the context still computes correctly
