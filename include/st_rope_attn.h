@@ -124,10 +124,12 @@ enum {
   ST_K_CLASSIFY = 1,  /* bool mask tile classification */
   ST_K_FWD = 2,       /* forward attention */
   ST_K_BWD_PRE = 3,   /* Delta = rowsum(dO * O), zero the dQ accumulator */
-  ST_K_BWD = 4,       /* backward attention (dK, dV, dQ accumulation) */
+  ST_K_BWD = 4,       /* backward attention (dV, dK' and dQ' accumulation) */
   ST_K_DQ_POST = 5,   /* dQ: inverse rotation + RMSNorm backward */
   ST_K_DW = 6,        /* norm-weight gradient reduction */
-  ST_K_COUNT = 8
+  ST_K_DK_POST = 7,   /* dK: inverse rotation + RMSNorm backward */
+  ST_K_PROBE = 8,     /* bounded-wait self-test */
+  ST_K_COUNT = 9
 };
 
 /* Per-kernel device time between two st_timing_read calls. */

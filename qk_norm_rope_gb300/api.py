@@ -46,11 +46,11 @@ class st_stats(ctypes.Structure):
                                                 "kernel_launches")]
 
 
-KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce"]
+KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce", "dk_post", "probe"]
 
 
 class st_kernel_times(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_uint64 * 8), ("ms", ctypes.c_double * 8)]
+    _fields_ = [("launches", ctypes.c_uint64 * 9), ("ms", ctypes.c_double * 9)]
 
 
 class StError(RuntimeError):

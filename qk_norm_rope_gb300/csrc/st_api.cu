@@ -196,6 +196,7 @@ struct Plan {
   int nQt = 0, nKt = 0, nQtm = 1;
   // workspace offsets
   size_t off_tab16_q = 0, off_tab16_k = 0;
+  size_t off_dkacc = 0;
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
          off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
   int n_dwq = 0, n_dwk = 0;
@@ -290,7 +291,9 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     off = align_up(off + (size_t)s.B * s.H * s.Sq * sizeof(float), 256);
     P->off_dqacc = off;
     off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * sizeof(float), 256);
-    P->n_dwk = s.B * s.H * P->nKt;
+    P->off_dkacc = off;
+    off = align_up(off + (size_t)s.B * s.Skv * s.H * kD * sizeof(float), 256);
+    P->n_dwk = static_cast<int>(((int64_t)s.B * s.Skv * s.H + kTile - 1) / kTile);
     P->off_dwk = off;
     off = align_up(off + (size_t)P->n_dwk * kD * sizeof(float), 256);
     P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kTile - 1) / kTile);
@@ -462,6 +465,24 @@ st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, in
   return ST_OK;
 }
 
+// 4-D tiled map over the fp32 dQ accumulator [B, S_q, H, D] (contiguous) as
+// (d, h, s, b) for 32-column x 128-row boxes with 128-byte swizzle: the target
+// of the backward kernel's bulk reductions.
+st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t row = (cuuint64_t)kD * 4;
+  cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)Sq, (cuuint64_t)B};
+  cuuint64_t strides[3] = {row, row * H, row * H * Sq};
+  cuuint32_t box[4] = {32, 1, kTile, 1}, es[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ST_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the dq accumulator (error %d)", (int)r);
+  return ST_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -567,12 +588,12 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   memset(&bp, 0, sizeof(bp));
   if (P.nKt > 0) {
     if ((st = encode_rows_map(v, &bp.tmap_v, &bp.v_s_first)) != ST_OK) return st;
-    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first)) != ST_OK)
+    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first, kTile / 2)) != ST_OK)
       return st;
     bp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
     if (bp.qk_tma) {
       if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
-      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first)) != ST_OK)
+      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first, kTile / 2)) != ST_OK)
         return st;
     }
   }
@@ -600,10 +621,24 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     bp.lse = static_cast<const float*>(lse->data);
     bp.delta = delta;
     bp.dq_acc = dq_acc;
-    bp.dk = dk->data; bp.dk_sb = rdk.sb; bp.dk_ss = rdk.ss; bp.dk_sh = rdk.sh; bp.dk_f32 = rdk.is_f32;
+    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_dq_acc_map(dq_acc, s.B, s.Sq, s.H, &bp.tmap_dq)) != ST_OK)
+      return st;
     bp.dv = dv->data; bp.dv_sb = rdv.sb; bp.dv_ss = rdv.ss; bp.dv_sh = rdv.sh; bp.dv_f32 = rdv.is_f32;
-    bp.dwk_part = reinterpret_cast<float*>(ws + P.off_dwk);
+    bp.dk_acc = reinterpret_cast<float*>(ws + P.off_dkacc);
     if ((st = cuda_check(launch_counted(ST_K_BWD, stream, [&] { return launch_bwd(bp, stream); }), "backward kernel launch")) != ST_OK) return st;
+    // dK' -> dK: the same row transform as for dQ, on the key side
+    PostParams pk;
+    memset(&pk, 0, sizeof(pk));
+    pk.dq_acc = bp.dk_acc;
+    pk.q = P.k;
+    pk.tab_q = reinterpret_cast<const float2*>(ws + P.off_tab_k);
+    pk.tab_q_sb = P.ids_k.Bt > 1 ? (int64_t)s.Skv * kPairs : 0;
+    pk.wq = static_cast<const float*>(k_norm_w->data);
+    pk.eps = eps;
+    pk.dq = dk->data; pk.dq_sb = rdk.sb; pk.dq_ss = rdk.ss; pk.dq_sh = rdk.sh; pk.dq_f32 = rdk.is_f32;
+    pk.dwq_part = reinterpret_cast<float*>(ws + P.off_dwk);
+    pk.B = s.B; pk.H = s.H; pk.Sq = s.Skv;
+    if ((st = cuda_check(launch_counted(ST_K_DK_POST, stream, [&] { return launch_dq_post(pk, stream); }), "dk post launch")) != ST_OK) return st;
   }
   if ((int64_t)s.B * s.Sq * s.H > 0) {
     PostParams pq;
@@ -761,7 +796,7 @@ st_status st_selftest_wait_timeout(long long budget_cycles, void* stream_) {
   Dev dev;
   st_status st = device_globals(&dev);
   if (st != ST_OK) return st;
-  return cuda_check(launch_counted(ST_K_TABLE + 7, static_cast<cudaStream_t>(stream_),
+  return cuda_check(launch_counted(ST_K_PROBE, static_cast<cudaStream_t>(stream_),
                                    [&] {
                                      return launch_wait_probe(dev.status, dev.counters, budget_cycles,
                                                               static_cast<cudaStream_t>(stream_));

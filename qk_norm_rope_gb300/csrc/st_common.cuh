@@ -73,23 +73,21 @@ struct FwdParams {
 struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
-  CUtensorMap tmap_do;  // dO rows
+  CUtensorMap tmap_do;  // dO rows, 64-row boxes
   CUtensorMap tmap_q;   // raw q / k rows (bf16 only; see qk_tma)
   CUtensorMap tmap_k;
+  CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 128 rows (reduce target)
   int v_s_first, do_s_first, q_s_first, k_s_first;
   int qk_tma;
   const void* dout;
   int64_t do_sb, do_ss, do_sh;
   const float* lse;    // [B, H, Sq]
   const float* delta;  // [B, H, Sq]
-  float* dq_acc;       // [B, Sq, H, D] fp32, zeroed
-  void* dk;
-  int64_t dk_sb, dk_ss, dk_sh;
-  int dk_f32;
+  float* dq_acc;       // [B, Sq, H, D] fp32, zeroed: scale * dS K' (gradient of the rotated, normed q)
+  float* dk_acc;       // [B, Skv, H, D] fp32: scale * dS^T Q' (gradient of the rotated, normed k)
   void* dv;
   int64_t dv_sb, dv_ss, dv_sh;
   int dv_f32;
-  float* dwk_part;     // [B*H*nKt, D]
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -288,6 +286,18 @@ __device__ __forceinline__ bool wait_bar_cluster(uint64_t* bar, uint32_t parity,
     }
   }
   return true;
+}
+
+// Warp-uniform forms: every lane waits, and the warp proceeds only if all of
+// them succeeded, so that warp-collective instructions (tcgen05.ld/st,
+// shuffles) that follow are never reached by part of a warp.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                              long long budget) {
+  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, budget));
+}
+__device__ __forceinline__ bool wait_bar_cluster_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                                      long long budget) {
+  return __all_sync(0xffffffffu, wait_bar_cluster(bar, parity, abort_flag, budget));
 }
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {

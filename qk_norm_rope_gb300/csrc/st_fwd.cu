@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           mbits[q4] = bits;
         }
       }
-      if (!(ok = wait_bar(&bars[kBarSFull + ti], n & 1, abort_flag, budget))) break;
+      if (!(ok = wait_bar_warp(&bars[kBarSFull + ti], n & 1, abort_flag, budget))) break;
       tc_fence_after();
       // pass 1: row max (raw scores on plain tiles; the scale is positive)
       float mt = -INFINITY;
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars[kBarPFull + ti]);
     }
     // ---- epilogue: O / l, LSE
-    if (ok && n > 0) ok = wait_bar(&bars[kBarOFull], 0, abort_flag, budget);
+    if (ok && n > 0) ok = wait_bar_warp(&bars[kBarOFull], 0, abort_flag, budget);
     if (ok) {
       tc_fence_after();
       const float inv = (l_run > 0.f) ? 1.f / l_run : 0.f;
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const int p = tid - kWarpProl0 * 32;                      // 0..255
     const int prow = (p >> 5) * 16 + (lane_id & 15), hh = lane_id >> 4;  // TMA path: half-row
     bool ok = true;
-    if constexpr (QKT) ok = wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+    if constexpr (QKT) ok = wait_bar_warp(&bars[kBarQRaw], 0, abort_flag, budget);
     if (ok) {
 #pragma unroll 1
       for (int ti = 0; ti < 2; ++ti) {
@@ -359,7 +359,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           hp.prefetch(t16, hh);
           hp.prefetch2(t16, hh);
         }
-        if (!wait_bar(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
+        if (!wait_bar_warp(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
         hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
       } else {
         if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
@@ -408,10 +408,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         tma_load_4d(tile + kHalfBytes, &P.tmap_v, &bars[kBarVFull + slot], 64, y, z, b);
       }
       // every issued load lands before the CTA exits
-      if constexpr (QKT) wait_bar(&bars[kBarQRaw], 0, abort_flag, budget);
+      // (these waits do not give up on abort; each is bounded)
+      if constexpr (QKT) mbar_wait(&bars[kBarQRaw], 0, budget);
       for (int m = max(0, n - kStages); m < n; ++m) {
-        wait_bar(&bars[kBarVFull + m % kStages], (m / kStages) & 1, abort_flag, budget);
-        if constexpr (QKT) wait_bar(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, abort_flag, budget);
+        mbar_wait(&bars[kBarVFull + m % kStages], (m / kStages) & 1, budget);
+        if constexpr (QKT) mbar_wait(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, budget);
       }
     }
   } else if (warp == kWarpMma) {

@@ -122,6 +122,15 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t remote_dst, const voi
       "r"(smem_u32(src)), "r"(bytes), "r"(remote_bar)
       : "memory");
 }
+// Asynchronous 16-byte store into another CTA's shared memory (cluster
+// address from mapa), completing as 16 transaction bytes on that CTA's
+// mbarrier `remote_bar`; the sender does not wait for it.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t remote_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
@@ -148,6 +157,24 @@ __device__ __forceinline__ void tma_load_4d_mc(void* dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w), "h"(mask)
       : "memory");
 }
+
+// Element-wise add of a shared-memory box into a global tensor through a
+// tiled tensor map (fp32 add performed by the TMA unit), tracked by the
+// issuing thread's bulk async-group.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int x, int y, int z,
+                                                  int w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading
+// its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // ------------------------------------------------------------ TMEM alloc
 // Executed by one full warp. The allocated TMEM address is written to *dst.
@@ -208,6 +235,11 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
   return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) | (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
          (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
+
+// Descriptor of the operand `bytes` further into shared memory. The start
+// address field holds addr >> 4 in 14 bits; shared-memory addresses stay
+// below 256 KB, so the add never carries out of the field.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
 
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` inside a
 // 128B-swizzled block whose rows are 128 bytes long. The block must start on
@@ -289,6 +321,22 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void red_add_v4(float* dst, float a, float b, float c, float d) {
   asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(a), "f"(b), "f"(c), "f"(d)
                : "memory");
+}
+
+// Read-only 16-byte global load issued where it stands: volatile asm keeps it
+// in program order with the other volatile asm (barrier waits), so a prefetch
+// is not sunk down to its first use.
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ldg_nc_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 // Pack two floats into a bf16x2 word (round to nearest even); `lo` lands in
