@@ -6,20 +6,17 @@
 //   P^T = exp2(S^T scale log2e - LSE log2e)            (compute warps)
 //   dS^T = P^T (dP^T - Delta)
 //   dV += P^T dO, dK += dS^T Q', dQ_part = dS K'       (tensor core, TMEM)
-// dQ_part (this CTA's 128 keys) is pre-reduced with the peer CTA's: each CTA
-// owns 64 of the 128 head dims, receives the peer's partial sums for them in
-// shared memory (DSMEM stores), adds its own and issues one TMA bulk reduce
-// (fp32 add) into the global accumulator, which halves the reduction traffic.
+// dQ_part (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
+// bulk reduces. The two CTAs of a cluster share the Q' operand prologue.
 //
 // Warp roles (576 threads; 96 registers per thread):
 //   warps 0-7    compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and
 //                query columns [64*(w/4), +64) of each tile; P^T goes to TMEM
 //                (bf16, in the warp's own S^T columns: 0-31 for the first query
 //                half, 96-127 for the second), dS^T to shared memory
-//   warps 8-11   dQ drain: TMEM lanes = query rows; the peer's 64 columns are
-//                stored into the peer's staging buffer (asynchronous DSMEM stores
-//                counted as transaction bytes on its barrier), the own 64 are added to
-//                what the peer stored here and reduced to global memory by TMA
+//   warps 8-11   dQ drain: TMEM lanes = query rows; B is read out at once
+//                (half staged in shared memory, half held in registers) and
+//                released, then reduced to global memory by TMA in two rounds
 //   warps 12-15  Q' prologue: each CTA of the cluster normalises and rotates
 //                64 of the tile's 128 rows (eight lanes per row) and copies them
 //                into the peer's stage as well (DSMEM bulk copy); the tile's
@@ -61,7 +58,7 @@ constexpr uint32_t kOffV = kTileBytes;
 constexpr uint32_t kOffQ = 2 * kTileBytes;                  // kQStages tiles
 constexpr uint32_t kOffDO = kOffQ + kQStages * kTileBytes;  // rows 0-63 / 64-127 refilled separately
 constexpr uint32_t kOffDS = kOffDO + kTileBytes;
-constexpr uint32_t kOffR = kOffDS + kTileBytes;             // dQ staging: 2 boxes (this CTA's 64 head dims)
+constexpr uint32_t kOffR = kOffDS + kTileBytes;             // dQ staging: 2 boxes of 32 head dims
 constexpr uint32_t kOffStat = kOffR + 2 * kRBoxBytes;       // [stage][LSE*log2e | Delta][128] fp32
 constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kTile * 4;
 constexpr uint32_t kOffW = kOffBar + 256;                   // q norm weights, fp32
@@ -85,8 +82,6 @@ enum {
   kBarHalf1,
   kBarDQFull,                            // dQ partial in B (and every earlier MMA done)
   kBarBFree,                             // B drained (128 arrivals)
-  kBarRFull,                             // the peer's partial sums stored here (local arm + 32 KB of tx)
-  kBarTxOk,                              // the peer's staging is free again (1 remote arrival)
   kBarFinal,                             // abort path: all issued MMAs done
   kNumBars
 };
@@ -197,8 +192,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     mbar_init(&bars[kBarHalf1], 128);
     mbar_init(&bars[kBarDQFull], 1);
     mbar_init(&bars[kBarBFree], kDrainWarps * 32);
-    mbar_init(&bars[kBarRFull], 1);
-    mbar_init(&bars[kBarTxOk], 1);
     mbar_init(&bars[kBarFinal], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -367,77 +360,68 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       }
     }
   } else if (warp < kWarpDrain0 + kDrainWarps) {
-    // ------------------------------------------------------------ dQ drain + pair reduction
+    // ------------------------------------------------------------ dQ drain
+    // The tile's partial dQ (128 query rows x 128 head dims, fp32) leaves B
+    // at once: columns 0-63 are staged in shared memory, 64-127 held in
+    // registers, then B is released; each half goes out as two TMA bulk
+    // reduces (fp32 add into the global accumulator).
     const int qd = warp & 3;
     const int qrow = qd * 32 + lane_id;  // query row in the tile = TMEM lane
     const uint32_t tB = tmem + 128 + (static_cast<uint32_t>(qd * 32) << 16);
-    const uint32_t own_c0 = 64 * crank, peer_c0 = 64 * peer;
     uint8_t* R = sm + kOffR;
-    const uint32_t rR = mapa_shared(smem_u32(R), peer);
-    const uint32_t r_rfull = mapa_shared(smem_u32(&bars[kBarRFull]), peer);
-    const uint32_t r_txok = mapa_shared(smem_u32(&bars[kBarTxOk]), peer);
     const float scale = c.scale;
     const bool issuer = warp == kWarpDrain0 && lane_id == 0;
+    auto stage32 = [&](int box, const uint32_t (&v)[32]) {  // 32 columns of this row into staging box `box`
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(R + box * kRBoxBytes + sw128_off(qrow, k)) =
+            make_uint4(__float_as_uint(__uint_as_float(v[4 * k]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * scale),
+                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * scale));
+    };
     int n = 0;
     for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0), ++n) {
       const int qt = W.qt(m);
-      // A failed wait skips the work but not the named barrier below; every
+      // A failed wait skips the work but not the named barriers below; every
       // thread then leaves together on the abort flag.
-      // the peer's stores for this tile complete as transaction bytes on RFull
-      if (issuer) mbar_arrive_expect_tx(&bars[kBarRFull], 2 * kRBoxBytes);
-      bool ok = wait_bar_warp(&bars[kBarDQFull], n & 1, abort_flag, budget);
-      if (ok) tc_fence_after();
-      // the peer's 64 head dims of this partial -> the peer's staging (free once
-      // the peer's previous reduce has read it)
-      ok = ok && (n == 0 || wait_bar_cluster_warp(&bars[kBarTxOk], (n - 1) & 1, abort_flag, budget));
-      uint32_t own0[32], own1[32];
+      const bool ok = wait_bar_warp(&bars[kBarDQFull], n & 1, abort_flag, budget);
+      uint32_t hold0[32], hold1[32];
       if (ok) {
+        tc_fence_after();
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           uint32_t v[32];
-          tmem_ld32(tB + peer_c0 + 32 * cc, v);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            st_async_v4(rR + cc * kRBoxBytes + sw128_off(qrow, k),
-                        make_uint4(__float_as_uint(__uint_as_float(v[4 * k]) * scale),
-                                   __float_as_uint(__uint_as_float(v[4 * k + 1]) * scale),
-                                   __float_as_uint(__uint_as_float(v[4 * k + 2]) * scale),
-                                   __float_as_uint(__uint_as_float(v[4 * k + 3]) * scale)),
-                        r_rfull);
+          tmem_ld32(tB + 32 * cc, v);
+          stage32(cc, v);
         }
-        tmem_ld32(tB + own_c0, own0);
-        tmem_ld32(tB + own_c0 + 32, own1);
+        tmem_ld32(tB + 64, hold0);
+        tmem_ld32(tB + 96, hold1);
         tc_fence_before();
         mbar_arrive(&bars[kBarBFree]);
-      }
-      ok = ok && wait_bar_cluster_warp(&bars[kBarRFull], n & 1, abort_flag, budget);
-      if (ok) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4* p = reinterpret_cast<uint4*>(R + cc * kRBoxBytes + sw128_off(qrow, k));
-            const uint32_t* o = cc ? &own1[4 * k] : &own0[4 * k];
-            uint4 a = *p;
-            a.x = __float_as_uint(fmaf(__uint_as_float(o[0]), scale, __uint_as_float(a.x)));
-            a.y = __float_as_uint(fmaf(__uint_as_float(o[1]), scale, __uint_as_float(a.y)));
-            a.z = __float_as_uint(fmaf(__uint_as_float(o[2]), scale, __uint_as_float(a.z)));
-            a.w = __float_as_uint(fmaf(__uint_as_float(o[3]), scale, __uint_as_float(a.w)));
-            *p = a;
-          }
-        }
       }
       fence_proxy_async_smem();
       named_bar(2, kDrainWarps * 32);
       if (*abort_flag) break;
+      const int row = qt * kTile;
       if (issuer) {
-        const int row = qt * kTile;
-        tma_reduce_add_4d(&P.tmap_dq, R, own_c0, h, row, b);
-        tma_reduce_add_4d(&P.tmap_dq, R + kRBoxBytes, own_c0 + 32, h, row, b);
+        tma_reduce_add_4d(&P.tmap_dq, R, 0, h, row, b);
+        tma_reduce_add_4d(&P.tmap_dq, R + kRBoxBytes, 32, h, row, b);
         bulk_commit_group();
         bulk_wait_read_all();
-        mbar_arrive_cluster(r_txok);
       }
+      named_bar(2, kDrainWarps * 32);  // staging read: columns 64-127 next
+      stage32(0, hold0);
+      stage32(1, hold1);
+      fence_proxy_async_smem();
+      named_bar(2, kDrainWarps * 32);
+      if (issuer) {
+        tma_reduce_add_4d(&P.tmap_dq, R, 64, h, row, b);
+        tma_reduce_add_4d(&P.tmap_dq, R + kRBoxBytes, 96, h, row, b);
+        bulk_commit_group();
+        bulk_wait_read_all();
+      }
+      named_bar(2, kDrainWarps * 32);  // staging free for the next tile
     }
     if (issuer) bulk_wait_all();
   } else if (warp < kWarpProl0 + kProlWarps) {
