@@ -29,8 +29,8 @@
 // MMA order per query tile n:
 //   [half 0 done] dV, dK over queries 0-63 | [half 1 done] dV, dK over
 //   queries 64-127, dQ (into B) | S^T(n+1) (into A) | [B drained] dP^T(n+1)
-// so the tensor core computes the next tile's scores while the compute warps
-// finish the current one and the drain warps empty B.
+// so the tensor core computes the next tile's scores while the drain warps
+// empty B.
 #include "st_common.cuh"
 #include "st_kernels.h"
 #include "st_prologue.cuh"
@@ -149,7 +149,22 @@ __device__ __forceinline__ float score2(const Common& c, float s, float key_term
   return s2;
 }
 
-template <int MK, bool CAUSAL, bool QKT>
+// As score2, with the element's mask term already loaded (mterm: mask*log2e,
+// -inf for a False bool element, 0 where no mask applies).
+template <bool CAUSAL>
+__device__ __forceinline__ float score2_term(const Common& c, float s, float key_term, float mterm, int iq, int j,
+                                             uint8_t flag) {
+  if (flag == kTileAllFalse) return -INFINITY;
+  float s2 = fmaf(s, c.scale_log2, key_term) + mterm;
+  if constexpr (CAUSAL) {
+    if (j > iq) s2 = -INFINITY;
+  }
+  return s2;
+}
+
+// ELEM: the mask varies along the queries (per-element terms); a mask that is
+// broadcast over the queries reduces to one term per key.
+template <int MK, bool CAUSAL, bool QKT, bool ELEM>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -280,7 +295,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
             pw[16 * cc + 2 * v4 + 1] = pack_bf16(ex2(x23.x), ex2(x23.y));
           }
         }
-      } else {
+      } else if constexpr (!ELEM) {
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int q0 = 64 * hq + 32 * cc;
@@ -298,6 +313,60 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
             }
             pw[16 * cc + t2] = pack_bf16(p2[0], p2[1]);
           }
+        }
+      } else {
+        // 16 queries at a time; the next chunk's mask terms are loaded while
+        // this one is computed (pinned at the end of the chunk)
+        const bool elem_mask = ELEM && key_ok && flag != kTileAllFalse && !(MK == kMaskBool && flag == kTileAllTrue);
+        float mv[2][16];
+        uint32_t mraw[2][16];
+        auto issue = [&](int c4, uint32_t (&raw)[16]) {
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            raw[t] = 0u;
+            if constexpr (ELEM) {
+              const int iq = qt * kTile + 64 * hq + 16 * c4 + t;
+              if (elem_mask && iq < c.Sq) {
+                const int64_t off = b * c.m_sb + h * c.m_sh + (int64_t)iq * c.m_sq + j;
+                if constexpr (MK == kMaskBool) raw[t] = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0u : 1u;
+                else if constexpr (MK == kMaskF32)
+                  raw[t] = __float_as_uint(ldg_nc_f32(static_cast<const float*>(c.mask) + off));
+                else raw[t] = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(c.mask) + off)) << 16;
+              }
+            }
+          }
+        };
+        auto settle = [&](const uint32_t (&raw)[16], float (&m)[16]) {  // pin, then convert
+          uint32_t folded = 0;
+#pragma unroll
+          for (int t = 0; t < 16; ++t) folded ^= raw[t];
+          pin_loads(folded, scratch);
+#pragma unroll
+          for (int t = 0; t < 16; ++t) {
+            if constexpr (MK == kMaskBool) m[t] = raw[t] ? -INFINITY : 0.f;
+            else m[t] = __uint_as_float(raw[t]) * kLog2e;
+          }
+        };
+        issue(0, mraw[0]);
+        settle(mraw[0], mv[0]);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          if (c4 < 3) issue(c4 + 1, mraw[(c4 + 1) & 1]);
+          const int q0 = 64 * hq + 16 * c4;  // first query column (in the tile) of this chunk
+          uint32_t sv[16];
+          tmem_ld16(tA + q0, sv);
+#pragma unroll
+          for (int t2 = 0; t2 < 8; ++t2) {
+            float p2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int t = 2 * t2 + e;
+              const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mv[c4 & 1][t], qt * kTile + q0 + t, j, flag);
+              p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
+            }
+            pw[8 * c4 + t2] = pack_bf16(p2[0], p2[1]);
+          }
+          if (c4 < 3) settle(mraw[(c4 + 1) & 1], mv[(c4 + 1) & 1]);
         }
       }
       tmem_st32(tP, pw);
@@ -726,9 +795,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 
 }  // namespace
 
-template <int MK, bool CAUSAL, bool QKT>
+template <int MK, bool CAUSAL, bool QKT, bool ELEM>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_kernel<MK, CAUSAL, QKT>;
+  auto kern = bwd_kernel<MK, CAUSAL, QKT, ELEM>;
   static unsigned configured = 0;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -744,12 +813,16 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
 
 template <bool QKT>
 cudaError_t launch_bwd_q(const BwdParams& p, cudaStream_t stream) {
-  if (p.c.causal) return launch_bwd_t<kMaskNone, true, QKT>(p, stream);  // masks and causal never combine
+  if (p.c.causal) return launch_bwd_t<kMaskNone, true, QKT, false>(p, stream);  // masks and causal never combine
+  const bool elem = p.c.m_sq != 0;  // the mask varies along the queries
   switch (p.c.mask_kind) {
-    case kMaskBool: return launch_bwd_t<kMaskBool, false, QKT>(p, stream);
-    case kMaskF32: return launch_bwd_t<kMaskF32, false, QKT>(p, stream);
-    case kMaskBF16: return launch_bwd_t<kMaskBF16, false, QKT>(p, stream);
-    default: return launch_bwd_t<kMaskNone, false, QKT>(p, stream);
+    case kMaskBool:
+      return elem ? launch_bwd_t<kMaskBool, false, QKT, true>(p, stream) : launch_bwd_t<kMaskBool, false, QKT, false>(p, stream);
+    case kMaskF32:
+      return elem ? launch_bwd_t<kMaskF32, false, QKT, true>(p, stream) : launch_bwd_t<kMaskF32, false, QKT, false>(p, stream);
+    case kMaskBF16:
+      return elem ? launch_bwd_t<kMaskBF16, false, QKT, true>(p, stream) : launch_bwd_t<kMaskBF16, false, QKT, false>(p, stream);
+    default: return launch_bwd_t<kMaskNone, false, QKT, false>(p, stream);
   }
 }
 

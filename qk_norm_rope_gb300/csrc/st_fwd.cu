@@ -89,9 +89,13 @@ __device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0,
 // TMEM values: s * scale * log2(e) (+ mask * log2(e)), -inf where a bool mask
 // is False, beyond the causal diagonal or at keys >= S_kv. Tiles that need no
 // masking take the caller's fast path instead.
+// Additive-mask rows are read as 16-byte vectors when the mask's base and
+// strides allow it (and the chunk lies inside the row), all issued before the
+// first use and pinned so that they complete together.
 template <int MK, bool CAUSAL>
 __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t (&raw)[32], int b, int h, int i,
-                                                int j0, uint8_t flag, uint32_t mbits, float (&s)[32]) {
+                                                int j0, uint8_t flag, uint32_t mbits, float (&s)[32],
+                                                bool mask_vec, uint32_t* scratch) {
 #pragma unroll
   for (int t = 0; t < 32; ++t) s[t] = __uint_as_float(raw[t]) * c.scale_log2;
   if (flag == kTileAllFalse) {
@@ -108,17 +112,53 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
   } else if constexpr (MK == kMaskF32) {
     if (i < c.Sq) {
       const float* mrow = static_cast<const float*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+      if (mask_vec && j0 + 32 <= c.Skv) {
+        uint4 u[8];
 #pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (j0 + t < c.Skv) s[t] = fmaf(__ldg(mrow + t), kLog2e, s[t]);
+        for (int k = 0; k < 8; ++k) u[k] = ldg_nc_v4(mrow + 4 * k);
+        uint32_t folded = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) folded ^= u[k].x ^ u[k].y ^ u[k].z ^ u[k].w;
+        pin_loads(folded, scratch);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          s[4 * k] = fmaf(__uint_as_float(u[k].x), kLog2e, s[4 * k]);
+          s[4 * k + 1] = fmaf(__uint_as_float(u[k].y), kLog2e, s[4 * k + 1]);
+          s[4 * k + 2] = fmaf(__uint_as_float(u[k].z), kLog2e, s[4 * k + 2]);
+          s[4 * k + 3] = fmaf(__uint_as_float(u[k].w), kLog2e, s[4 * k + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (j0 + t < c.Skv) s[t] = fmaf(__ldg(mrow + t), kLog2e, s[t]);
+      }
     }
   } else if constexpr (MK == kMaskBF16) {
     if (i < c.Sq) {
       const __nv_bfloat16* mrow =
           static_cast<const __nv_bfloat16*>(c.mask) + b * c.m_sb + h * c.m_sh + (int64_t)i * c.m_sq + j0;
+      if (mask_vec && j0 + 32 <= c.Skv) {
+        uint4 u[4];
 #pragma unroll
-      for (int t = 0; t < 32; ++t)
-        if (j0 + t < c.Skv) s[t] = fmaf(__bfloat162float(mrow[t]), kLog2e, s[t]);
+        for (int k = 0; k < 4; ++k) u[k] = ldg_nc_v4(mrow + 8 * k);
+        uint32_t folded = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) folded ^= u[k].x ^ u[k].y ^ u[k].z ^ u[k].w;
+        pin_loads(folded, scratch);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            s[8 * k + 2 * e] = fmaf(bf16_lo(w[e]), kLog2e, s[8 * k + 2 * e]);
+            s[8 * k + 2 * e + 1] = fmaf(bf16_hi(w[e]), kLog2e, s[8 * k + 2 * e + 1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t)
+          if (j0 + t < c.Skv) s[t] = fmaf(__bfloat162float(mrow[t]), kLog2e, s[t]);
+      }
     }
   }
   if constexpr (CAUSAL) {
@@ -193,6 +233,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     const uint32_t lane = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + ti * 128 + lane, tO = tmem + 256 + ti * 128 + lane;
     const float sc = c.scale_log2;
+    uint32_t* scratch = tslot + 2;  // sink for pin_loads
+    constexpr int kVecElems = MK == kMaskBF16 ? 8 : 4;  // elements per 16 bytes
+    const bool mask_vec = (reinterpret_cast<uintptr_t>(c.mask) & 15u) == 0 && c.m_sb % kVecElems == 0 &&
+                          c.m_sh % kVecElems == 0 && c.m_sq % kVecElems == 0;
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0, useful = 0;
     bool ok = true;
@@ -233,12 +277,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           mt = fmaxf(mt, fmaxf(m0, m1) * sc);
         } else {
+          // scaled and masked once; pass 2 reads them back instead of the mask
           float sv[32];
-          masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
+          masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv, mask_vec, scratch);
+          uint32_t w32[32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) mt = fmaxf(mt, sv[t]);
+          for (int t = 0; t < 32; ++t) {
+            mt = fmaxf(mt, sv[t]);
+            w32[t] = __float_as_uint(sv[t]);
+          }
+          tmem_st32(tS + 32 * q4, w32);
         }
       }
+      if (!plain) tmem_st_wait();
       float corr = 1.f;
       if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
         corr = ex2(m_run - mt);  // 0 when m_run is -inf
@@ -261,11 +312,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             pw[t] = pack_bf16(p0, p1);
           }
         } else {
-          float sv[32];
-          masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv);
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
-            const float p0 = ex2(sv[2 * t] - m_use), p1 = ex2(sv[2 * t + 1] - m_use);
+            const float p0 = ex2(__uint_as_float(raw[2 * t]) - m_use), p1 = ex2(__uint_as_float(raw[2 * t + 1]) - m_use);
             ls0 += p0;
             ls1 += p1;
             pw[t] = pack_bf16(p0, p1);
