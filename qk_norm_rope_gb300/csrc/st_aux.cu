@@ -3,8 +3,9 @@
 //  - mask classify:  bool mask tiles -> {all True, all False, mixed}, plus the
 //                    "whole mask is all True" counter;
 //  - backward pre:   Delta_i = sum_d dO_id O_id, zero the fp32 dQ accumulator;
-//  - dq post:        dQ accumulator -> inverse rotation -> RMSNorm backward -> dq,
-//                    per-block partial sums of the q-norm weight gradient;
+//  - dq post:        fp32 gradient rows of the rotated, normed q (or k) ->
+//                    inverse rotation -> RMSNorm backward -> dq (or dk), with
+//                    per-block partial sums of the norm-weight gradient;
 //  - dw reduce:      fixed-order sums of the weight-gradient partials.
 #include "st_aux.h"
 
@@ -101,36 +102,75 @@ __global__ void bwd_pre_kernel(const __grid_constant__ PreParams p) {
   reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// One thread per (b, i, h) row, 128 rows per block.
-constexpr uint32_t kPostSmem = kTile * (kD + 1) * sizeof(float);
+// One warp per (b, i, h) row, 128 rows per block (8 warps x 16 rows). Lane l
+// owns head dims 4l..4l+3 (rotation pairs 2l, 2l+1), so every row load and
+// store is one coalesced access per warp; the row's sums (x.x, x.g) are warp
+// shuffles. With dy = R^T g (sin negated) and g' = w dy:
+//   dx = r g' - (r^3 / D) x (x . g'); the weight gradient gathers dy x r.
+constexpr int kPostWarps = 8;
+constexpr int kPostThreads = kPostWarps * 32;
 
-__global__ void __launch_bounds__(128) dq_post_kernel(const __grid_constant__ PostParams p) {
-  extern __shared__ float red[];  // [128][129]
-  const int tid = threadIdx.x;
-  const int64_t row = (int64_t)blockIdx.x * kTile + tid;
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_constant__ PostParams p) {
+  __shared__ float4 part[kPostWarps][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
-  float* my = red + tid * (kD + 1);
-  if (row < nrows) {
+  const int64_t row0 = (int64_t)blockIdx.x * kTile;
+  const float4 w = __ldg(reinterpret_cast<const float4*>(p.wq) + lane);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int k = warp; k < kTile; k += kPostWarps) {
+    const int64_t row = row0 + k;
+    if (row >= nrows) break;
     const int h = static_cast<int>(row % p.H);
     const int i = static_cast<int>((row / p.H) % p.Sq);
     const int b = static_cast<int>(row / ((int64_t)p.H * p.Sq));
-    float g[kD];
-    const float4* src = reinterpret_cast<const float4*>(p.dq_acc + row * kD);
-#pragma unroll
-    for (int c = 0; c < kD / 4; ++c) {
-      const float4 v = src[c];
-      g[4 * c] = v.x; g[4 * c + 1] = v.y; g[4 * c + 2] = v.z; g[4 * c + 3] = v.w;
+    const float4 g = __ldg(reinterpret_cast<const float4*>(p.dq_acc + row * kD) + lane);
+    const int64_t xoff = b * p.q.sb + (int64_t)i * p.q.ss + h * p.q.sh + 4 * lane;
+    float4 x;
+    if (p.q.is_f32) {
+      x = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.q.p) + xoff));
+    } else {
+      const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q.p) + xoff));
+      x = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
     }
-    rope_norm_bwd_row(g, p.q.p, b * p.q.sb + (int64_t)i * p.q.ss + h * p.q.sh, p.q.is_f32,
-                      p.tab_q + b * p.tab_q_sb + (int64_t)i * kPairs, p.wq, p.eps, my);
-    store_row(p.dq, b * p.dq_sb + (int64_t)i * p.dq_ss + h * p.dq_sh, p.dq_f32, g);
-  } else {
-    for (int d = 0; d < kD; ++d) my[d] = 0.f;
+    const float4 cs = __ldg(reinterpret_cast<const float4*>(p.tab_q + b * p.tab_q_sb + (int64_t)i * kPairs) + lane);
+    const float r = rsqrtf(warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) * (1.0f / kD) + p.eps);
+    // inverse rotation of the two pairs: (cos, sin) = (cs.x, cs.y), (cs.z, cs.w)
+    const float d0 = g.x * cs.x + g.y * cs.y, d1 = -g.x * cs.y + g.y * cs.x;
+    const float d2 = g.z * cs.z + g.w * cs.w, d3 = -g.z * cs.w + g.w * cs.z;
+    acc.x = fmaf(d0, x.x * r, acc.x);
+    acc.y = fmaf(d1, x.y * r, acc.y);
+    acc.z = fmaf(d2, x.z * r, acc.z);
+    acc.w = fmaf(d3, x.w * r, acc.w);
+    const float g0 = w.x * d0, g1 = w.y * d1, g2 = w.z * d2, g3 = w.w * d3;
+    const float xg = warp_sum(x.x * g0 + x.y * g1 + x.z * g2 + x.w * g3);
+    const float c3 = r * r * r * xg * (1.0f / kD);
+    const float y0 = r * g0 - c3 * x.x, y1 = r * g1 - c3 * x.y, y2 = r * g2 - c3 * x.z, y3 = r * g3 - c3 * x.w;
+    const int64_t yoff = b * p.dq_sb + (int64_t)i * p.dq_ss + h * p.dq_sh + 4 * lane;
+    if (p.dq_f32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(p.dq) + yoff) = make_float4(y0, y1, y2, y3);
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dq) + yoff) = make_uint2(pack_bf16(y0, y1), pack_bf16(y2, y3));
+    }
   }
+  part[warp][lane] = acc;
   __syncthreads();
-  float acc = 0.f;
-  for (int r = 0; r < kTile; ++r) acc += red[r * (kD + 1) + tid];
-  p.dwq_part[(int64_t)blockIdx.x * kD + tid] = acc;
+  if (threadIdx.x < kD) {  // column d = 4 * lane + component, summed over the warps in order
+    const int l = threadIdx.x >> 2, comp = threadIdx.x & 3;
+    float sum = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < kPostWarps; ++w8) {
+      const float4 v = part[w8][l];
+      sum += comp == 0 ? v.x : comp == 1 ? v.y : comp == 2 ? v.z : v.w;
+    }
+    p.dwq_part[(int64_t)blockIdx.x * kD + threadIdx.x] = sum;
+  }
 }
 
 // Grid (nblocks, 2): y = 0 reduces the q-weight partials, y = 1 the k-weight
@@ -205,15 +245,7 @@ cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream) {
 cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const int64_t blocks = (nrows + kTile - 1) / kTile;
-  static unsigned configured = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured & (1u << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(dq_post_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPostSmem);
-    if (e != cudaSuccess) return e;
-    configured |= 1u << (dev & 31);
-  }
-  dq_post_kernel<<<static_cast<unsigned>(blocks), kTile, kPostSmem, stream>>>(p);
+  dq_post_kernel<<<static_cast<unsigned>(blocks), kPostThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

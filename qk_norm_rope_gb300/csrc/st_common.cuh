@@ -209,54 +209,6 @@ __device__ __forceinline__ void load_chunk8(const void* base, int64_t off, int i
   }
 }
 
-// Backward of the rotation and the RMSNorm for one row.
-//   g: gradient w.r.t. the rotated, normalised row (fp32, overwritten with dx);
-//   the raw input row x is re-read from (xbase, xoff) chunk by chunk;
-//   tab: the row's (cos, sin); w: norm weight.
-// With dy = R^T g (inverse rotation, sin negated), g' = w * dy:
-//   dx = r g' - (r^3 / D) x (x . g'); the weight-gradient term dy * x * r of
-// the row goes to contrib[0..127] (shared memory; the caller sums over rows).
-__device__ __forceinline__ void rope_norm_bwd_row(float (&g)[kD], const void* xbase, int64_t xoff, int x_f32,
-                                                  const float2* __restrict__ tab, const float* __restrict__ w,
-                                                  float eps, float* contrib) {
-  float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {
-    float x[8];
-    load_chunk8(xbase, xoff, x_f32, c, x);
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) { ss0 = fmaf(x[e], x[e], ss0); ss1 = fmaf(x[e + 1], x[e + 1], ss1); }
-  }
-  const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + eps);
-  float xg = 0.f;
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {
-    float x[8];
-    load_chunk8(xbase, xoff, x_f32, c, x);
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const int d = 8 * c + e;
-      const float2 cs = __ldg(tab + d / 2);
-      const float d0 = g[d] * cs.x + g[d + 1] * cs.y;
-      const float d1 = -g[d] * cs.y + g[d + 1] * cs.x;
-      contrib[d] = d0 * (x[e] * r);
-      contrib[d + 1] = d1 * (x[e + 1] * r);
-      const float g0 = d0 * __ldg(w + d), g1 = d1 * __ldg(w + d + 1);
-      g[d] = g0;
-      g[d + 1] = g1;
-      xg = fmaf(x[e], g0, fmaf(x[e + 1], g1, xg));
-    }
-  }
-  const float c3 = r * r * r * xg * (1.0f / kD);
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {
-    float x[8];
-    load_chunk8(xbase, xoff, x_f32, c, x);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) g[8 * c + e] = r * g[8 * c + e] - c3 * x[e];
-  }
-}
-
 // Bounded wait on an mbarrier phase that also gives up when another role of
 // the CTA has aborted; a wait that runs out of budget raises the CTA's abort
 // flag.

@@ -243,14 +243,6 @@ struct OctRow {
   }
 };
 
-// The compiler may sink prefetched global loads down to their first use,
-// which turns a batch of independent loads into a chain of round trips. A
-// store of a value that depends on every loaded word (to a scratch shared
-// word) makes all of them complete at this point instead, together.
-__device__ __forceinline__ void pin_loads(uint32_t folded, uint32_t* scratch) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(scratch)), "r"(folded) : "memory");
-}
-
 // Half-row variant: two lanes of a warp (l and l ^ 16) share one row; lane
 // half `hh` owns head dims [64*hh, 64*hh + 64) = the 64-column half `hh` of the
 // swizzled tile. The (cos, sin) loads are issued by prefetch() before the raw

@@ -350,6 +350,14 @@ __device__ __forceinline__ float ldg_nc_f32(const float* p) {
   return v;
 }
 
+// The compiler may sink prefetched global loads down to their first use,
+// which turns a batch of independent loads into a chain of round trips. A
+// store of a value that depends on every loaded word (to a scratch shared
+// word) makes all of them complete at this point instead, together.
+__device__ __forceinline__ void pin_loads(uint32_t folded, uint32_t* scratch) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(smem_u32(scratch)), "r"(folded) : "memory");
+}
+
 // Pack two floats into a bf16x2 word (round to nearest even); `lo` lands in
 // the low half, i.e. the lower K index.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
