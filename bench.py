@@ -127,6 +127,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def reduce_max(value: float, world: int, device) -> float:
+    """The maximum of `value` over all ranks (the slowest rank's time)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world: int, flops_per_step: float, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`
+    (weak scaling), and the job took `ms` (the maximum over ranks)."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def load_traffic(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it
     was captured from the current kernel source (matching hash)."""
@@ -206,12 +221,9 @@ def run_ours(args, rank, world, dev):
     barrier()
     clk = clocks.stop()
     api.st_check_status()
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_max = float(t.item())
+    ms_max = reduce_max(ms, world, dev)
     ms_per_step = ms_max / args.steps
-    value = world * step_flops * args.steps / (ms_max * 1e-3) / 1e12
+    value = job_tflops(world, step_flops, args.steps, ms_max)
 
     # ---- per-kernel device time (events on the launching stream, inside the library)
     api.st_timing_enable(True)
@@ -267,12 +279,10 @@ def run_ours(args, rank, world, dev):
         barrier()
         n_e2e = max(3, min(args.steps, 20))
         ms_e = timed(n_e2e, e2e_step)
-        te = torch.tensor([ms_e], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-        e2e = {"value": round(world * step_flops * n_e2e / (float(te.item()) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        me = reduce_max(ms_e, world, dev)
+        e2e = {"value": round(job_tflops(world, step_flops, n_e2e, me), 2), "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
-               "ms_per_step": round(float(te.item()) / n_e2e, 4)}
+               "ms_per_step": round(me / n_e2e, 4)}
         if hmask is None and mask is not None:
             e2e["note"] = "mask stays resident on the device (over 1 GB)"
 
