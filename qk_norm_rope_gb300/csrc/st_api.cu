@@ -466,15 +466,16 @@ st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, in
 }
 
 // 4-D tiled map over the fp32 dQ accumulator [B, S_q, H, D] (contiguous) as
-// (d, h, s, b) for 32-column x 128-row boxes with 128-byte swizzle: the target
-// of the backward kernel's bulk reductions.
+// (d, h, s, b) for 32-column x 64-row boxes with 128-byte swizzle: the target
+// of the backward kernel's bulk reductions (one box per 32 head dims of a
+// 64-query sub-tile).
 st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t row = (cuuint64_t)kD * 4;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)Sq, (cuuint64_t)B};
   cuuint64_t strides[3] = {row, row * H, row * H * Sq};
-  cuuint32_t box[4] = {32, 1, kTile, 1}, es[4] = {1, 1, 1, 1};
+  cuuint32_t box[4] = {32, 1, kTile / 2, 1}, es[4] = {1, 1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dq_acc, dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -593,7 +594,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     bp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
     if (bp.qk_tma) {
       if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
-      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first, kTile / 2)) != ST_OK)
+      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first, kTile / 4)) != ST_OK)
         return st;
     }
   }

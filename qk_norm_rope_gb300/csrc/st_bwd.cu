@@ -1,36 +1,39 @@
 // Backward main kernel: one CTA per (key tile of 128 rows, head, batch), in
 // clusters of two CTAs over adjacent key tiles (kt0 = 2p, kt0 + 1) that walk
-// the same query tiles in lockstep. Per query tile, with Q' = RoPE(RMSNorm(q))
-// and K' the same for k (bf16, 128B-swizzled operand tiles):
+// the same query tiles in lockstep. Query tiles are processed as two 64-query
+// sub-tiles; per sub-tile, with Q' = RoPE(RMSNorm(q)) and K' the same for k
+// (bf16, 128B-swizzled operand tiles):
 //   S^T = K' Q'^T, dP^T = V dO^T                      (tensor core, TMEM)
 //   P^T = exp2(S^T scale log2e - LSE log2e)            (compute warps)
 //   dS^T = P^T (dP^T - Delta)
-//   dV += P^T dO, dK += dS^T Q', dQ_part = dS K'       (tensor core, TMEM)
-// dQ_part (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
+//   dV += P^T dO, dK' += dS^T Q', dQ'^T = K'^T dS^T    (tensor core, TMEM)
+// dQ'^T (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
 // bulk reduces. The two CTAs of a cluster share the Q' operand prologue.
 //
 // Warp roles (576 threads; 96 registers per thread):
 //   warps 0-7    compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and
-//                query columns [64*(w/4), +64) of each tile; P^T goes to TMEM
-//                (bf16, in the warp's own S^T columns: 0-31 for the first query
-//                half, 96-127 for the second), dS^T to shared memory
-//   warps 8-11   dQ drain: TMEM lanes = query rows; B is read out at once
-//                (half staged in shared memory, half held in registers) and
-//                released, then reduced to global memory by TMA in two rounds
+//                queries [32*(w/4), +32) of each sub-tile; P^T goes to TMEM
+//                (bf16, inside the warp's own S^T columns), dS^T to shared
+//                memory
+//   warps 8-11   dQ drain: TMEM lanes = head dims; a sub-tile's dQ'^T is read
+//                out at once and its columns released; each warp then stages
+//                its 32 head dims in its own shared-memory box and adds the box
+//                into global memory with a TMA bulk reduce of its own
 //   warps 12-15  Q' prologue: each CTA of the cluster normalises and rotates
-//                64 of the tile's 128 rows (eight lanes per row) and copies them
-//                into the peer's stage as well (DSMEM bulk copy); the tile's
-//                LSE and Delta; K' once
+//                32 of a sub-tile's 64 rows (eight lanes per row) and copies
+//                them into the peer's stage as well (DSMEM bulk copy); the
+//                sub-tile's LSE and Delta; K' once
 //   warp 16      TMEM allocation + tcgen05.mma issue (one thread)
-//   warp 17      TMA: raw K, V once; this CTA's 64 raw Q rows per tile (2-stage
-//                ring, a stage reused once both CTAs' MMAs released it); dO in
-//                two 64-row halves, each refilled as soon as its dV MMAs ran
-// TMEM (512 columns): A = S^T / P^T | B = dP^T / dQ | dV | dK.
-// MMA order per query tile n:
-//   [half 0 done] dV, dK over queries 0-63 | [half 1 done] dV, dK over
-//   queries 64-127, dQ (into B) | S^T(n+1) (into A) | [B drained] dP^T(n+1)
-// so the tensor core computes the next tile's scores while the drain warps
-// empty B.
+//   warp 17      TMA: raw K, V once; this CTA's 32 raw Q rows per sub-tile
+//                (4-stage ring, a stage reused once both CTAs' MMAs released
+//                it); dO sub-tiles (2-stage ring)
+// TMEM (512 columns): two sub-tile buffers of 128 columns, dV, dK'. A buffer
+// holds S^T (later P^T, later dQ'^T) in one 64-column half and dP^T in the
+// other; the halves swap roles on each use of the buffer.
+// MMA order for sub-tile n (buffer n % 2): [compute done] dV, dK', dQ'^T (over
+// P^T) | S^T(n+2) (over dP^T(n)) | [dQ'^T drained] dP^T(n+2), so the compute
+// warps work on one buffer while the tensor core finishes the other, and the
+// drain overlaps the next scores.
 #include "st_common.cuh"
 #include "st_kernels.h"
 #include "st_prologue.cuh"
@@ -45,25 +48,31 @@ constexpr int kWarpDrain0 = 8, kDrainWarps = 4;
 constexpr int kWarpProl0 = 12, kProlWarps = 4;
 constexpr int kWarpMma = 16, kWarpTma = 17;
 constexpr int kBwdWarps = 18;
-constexpr int kProlThreads = kProlWarps * 32;
 constexpr int kBwdThreads = kBwdWarps * 32;
-constexpr int kQStages = 2;
-constexpr uint32_t kRBoxBytes = kTile * 32 * 4;  // one [128 query rows][32 head dims] fp32 box, 128B-swizzled
-constexpr int kHalfRows = kTile / kCluster;                      // Q' rows produced per CTA
-constexpr uint32_t kHalfRowsBytes = kHalfRows * 128;             // those rows in one 64-column half
+constexpr int kProlThreads = kProlWarps * 32;
+constexpr int kSub = 64;                                   // queries per sub-tile
+constexpr int kQStages = 4;                                // Q' ring, in sub-tiles
+constexpr int kDOStages = 2;                               // dO ring, in sub-tiles
+constexpr uint32_t kSubBytes = kSub * kD * 2;              // 16 KB bf16 sub-tile (two 8 KB column halves)
+constexpr uint32_t kSubHalf = kSubBytes / 2;
+constexpr int kPeerRows = kSub / kCluster;                 // Q' rows produced per CTA per sub-tile
+constexpr uint32_t kPeerRowsBytes = kPeerRows * 128;       // those rows in one column half
+constexpr uint32_t kRBoxBytes = kSub * 32 * 4;             // one [64 queries][32 head dims] fp32 box
 
 // shared memory layout (offsets from the 1024-byte aligned dynamic base)
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kTileBytes;
-constexpr uint32_t kOffQ = 2 * kTileBytes;                  // kQStages tiles
-constexpr uint32_t kOffDO = kOffQ + kQStages * kTileBytes;  // rows 0-63 / 64-127 refilled separately
-constexpr uint32_t kOffDS = kOffDO + kTileBytes;
-constexpr uint32_t kOffR = kOffDS + kTileBytes;             // dQ staging: 2 boxes of 32 head dims
-constexpr uint32_t kOffStat = kOffR + 2 * kRBoxBytes;       // [stage][LSE*log2e | Delta][128] fp32
-constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kTile * 4;
-constexpr uint32_t kOffW = kOffBar + 256;                   // q norm weights, fp32
-constexpr uint32_t kBwdSmem = kOffW + kD * 4;               // the base must be 1024-byte aligned
+constexpr uint32_t kOffQ = 2 * kTileBytes;                      // kQStages sub-tiles
+constexpr uint32_t kOffDO = kOffQ + kQStages * kSubBytes;       // kDOStages sub-tiles
+constexpr uint32_t kOffDS = kOffDO + kDOStages * kSubBytes;     // 2 buffers of [128 keys][64 queries] bf16
+constexpr uint32_t kOffR = kOffDS + 2 * kSubBytes;              // dQ'^T staging: a box per drain warp
+constexpr uint32_t kOffStat = kOffR + kDrainWarps * kRBoxBytes; // [stage][LSE*log2e | Delta][64] fp32
+constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kSub * 4;
+constexpr uint32_t kBarBytes = 512;
+constexpr uint32_t kOffW = kOffBar + kBarBytes;                 // q norm weights, fp32
+constexpr uint32_t kBwdSmem = kOffW + kD * 4;                   // the base must be 1024-byte aligned
 static_assert(kBwdSmem <= 232448, "backward shared memory exceeds the per-block limit");
+static_assert(kProlThreads >= kSub, "one prologue thread per stat row");
 
 enum {
   kBarKRaw = 0,                          // raw k rows landed (TMA)
@@ -72,24 +81,25 @@ enum {
   kBarQRaw,                              // + stage: raw q rows landed (TMA)
   kBarQFull = kBarQRaw + kQStages,       // + stage: Q' + stats ready (prologue threads + the peer's rows)
   kBarQFree = kBarQFull + kQStages,      // + stage: both CTAs' MMAs done with the stage
-  kBarDOLoFull = kBarQFree + kQStages,   // dO rows 0-63 landed
-  kBarDOHiFull,                          // dO rows 64-127 landed
-  kBarDOLoFree,                          // MMAs done with dO rows 0-63
-  kBarDOHiFree,
-  kBarSFull,                             // S^T in A
-  kBarDPFull,                            // dP^T in B
-  kBarHalf0,                             // compute warps of query half 0 done (128 arrivals)
-  kBarHalf1,
-  kBarDQFull,                            // dQ partial in B (and every earlier MMA done)
-  kBarBFree,                             // B drained (128 arrivals)
-  kBarFinal,                             // abort path: all issued MMAs done
+  kBarDOFull = kBarQFree + kQStages,     // + stage: dO rows landed
+  kBarDOFree = kBarDOFull + kDOStages,   // + stage: MMAs done with the dO rows
+  kBarSFull = kBarDOFree + kDOStages,    // + buffer: S^T in TMEM
+  kBarDPFull = kBarSFull + 2,            // + buffer: dP^T in TMEM
+  kBarCDone = kBarDPFull + 2,            // + buffer: P^T in TMEM, dS^T in shared memory (256 arrivals)
+  kBarDQ = kBarCDone + 2,                // + buffer: dQ'^T in TMEM (and every earlier MMA done)
+  kBarBFree = kBarDQ + 2,                // + buffer: dQ'^T read out (128 arrivals)
+  kBarFinal = kBarBFree + 2,             // abort path: all issued MMAs done
   kNumBars
 };
-static_assert(kNumBars * 8 + 12 <= 256, "barrier area");
-static_assert(kTile % kProlThreads == 0 && kProlThreads <= kTile, "prologue threads cover the stat rows evenly");
+static_assert(kNumBars * 8 + 12 <= kBarBytes, "barrier area");
 
-__device__ __forceinline__ uint32_t kofs(int kk) { return (kk >> 2) * kHalfBytes + (kk & 3) * 32; }  // K-major step
-__device__ __forceinline__ uint32_t mofs(int kk) { return kk * 2048; }                               // MN-major step
+__device__ __forceinline__ uint32_t kofs128(int kk) { return (kk >> 2) * kHalfBytes + (kk & 3) * 32; }  // K-major, 128 rows
+__device__ __forceinline__ uint32_t kofs64(int kk) { return (kk >> 2) * kSubHalf + (kk & 3) * 32; }     // K-major, 64 rows
+__device__ __forceinline__ uint32_t mofs(int kk) { return kk * 2048; }                                   // MN-major, 16 rows
+// TMEM column of sub-tile n's S^T half and of its dP^T half (the halves of
+// buffer n % 2 swap roles on every use of the buffer)
+__device__ __forceinline__ uint32_t s_col(int n) { return 128 * (n & 1) + 64 * ((n >> 1) & 1); }
+__device__ __forceinline__ uint32_t dp_col(int n) { return s_col(n) ^ 64u; }
 
 // Tile class of (query tile qt, key tile kt) for this CTA's own key tile; a
 // CTA past the last key tile sees nothing.
@@ -197,16 +207,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       mbar_init(&bars[kBarQFull + s], kProlThreads);
       mbar_init(&bars[kBarQFree + s], kCluster);
     }
-    mbar_init(&bars[kBarDOLoFull], 1);
-    mbar_init(&bars[kBarDOHiFull], 1);
-    mbar_init(&bars[kBarDOLoFree], 1);
-    mbar_init(&bars[kBarDOHiFree], 1);
-    mbar_init(&bars[kBarSFull], 1);
-    mbar_init(&bars[kBarDPFull], 1);
-    mbar_init(&bars[kBarHalf0], 128);
-    mbar_init(&bars[kBarHalf1], 128);
-    mbar_init(&bars[kBarDQFull], 1);
-    mbar_init(&bars[kBarBFree], kDrainWarps * 32);
+    for (int s = 0; s < kDOStages; ++s) {
+      mbar_init(&bars[kBarDOFull + s], 1);
+      mbar_init(&bars[kBarDOFree + s], 1);
+    }
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&bars[kBarSFull + u], 1);
+      mbar_init(&bars[kBarDPFull + u], 1);
+      mbar_init(&bars[kBarCDone + u], kComputeWarps * 32);
+      mbar_init(&bars[kBarDQ + u], 1);
+      mbar_init(&bars[kBarBFree + u], kDrainWarps * 32);
+    }
     mbar_init(&bars[kBarFinal], 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -224,7 +235,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers exist before any remote store or arrival
+  cluster_sync();  // the peer's barriers exist before any remote copy or arrival
   tc_fence_after();
   const uint32_t tmem = *tslot;
   const uint32_t crank = cluster_rank(), peer = crank ^ 1u;
@@ -238,13 +249,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 
   if (warp < kComputeWarps) {
     // ------------------------------------------------------------ compute
-    const int qd = warp & 3, hq = warp >> 2;  // TMEM lane quarter, query half
+    const int qd = warp & 3, hq = warp >> 2;  // TMEM lane quarter, query half of a sub-tile
     const int r = qd * 32 + lane_id;          // key row in the tile / TMEM lane
     const int j = kt * kTile + r;
     const bool key_ok = j < c.Skv;
     const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tA = tmem + lanebits, tB = tmem + 128 + lanebits;
-    const uint32_t tP = tA + (hq ? 96 : 0);  // P^T of the warp's 64 queries, inside its own S^T columns
     // masks that do not depend on the query row: one term per key for the CTA
     float key_term = 0.f;
     const bool mask_bcast_q = MK != kMaskNone && c.m_sq == 0;
@@ -256,154 +265,128 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     }
     if (!key_ok) key_term = -INFINITY;
     const float sc = c.scale_log2;
+    const int q0 = 32 * hq;  // this warp's first query of a sub-tile
     bool ok = true;
     int n = 0;
-    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0), ++n) {
+    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); ok && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
       const int qt = W.qt(m);
       const uint8_t flag = own_flag<MK>(c, b, h, qt, kt);
       useful += (flag != kTileAllFalse && (!CAUSAL || qt >= kt)) ? 1 : 0;
-      const int s = n % kQStages;
-      if (!(ok = wait_bar_warp(&bars[kBarSFull], n & 1, abort_flag, budget))) break;
-      // the prologue's LSE/Delta for this stage become visible through this wait
-      if (!(ok = wait_bar_warp(&bars[kBarQFull + s], (n / kQStages) & 1, abort_flag, budget))) break;
-      tc_fence_after();
-      const float* st_lse = stat + s * 256;
-      const float* st_dl = st_lse + 128;
-      // plain tiles: every query row valid, no mask values, no causal diagonal
-      const bool plain = flag != kTileAllFalse && (qt + 1) * kTile <= c.Sq &&
-                         (MK == kMaskNone || mask_bcast_q || (MK == kMaskBool && flag == kTileAllTrue)) &&
-                         (!CAUSAL || kt < qt);
-      // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), bf16 into TMEM. The
-      // general path (masks, causal diagonal, ragged tiles) is kept apart so
-      // that the plain loop stays short and contiguous in the instruction cache.
-      uint32_t pw[32];
-      if (plain) {
-        const float2 sc2 = make_float2(sc, sc), kt2 = make_float2(key_term, key_term);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int q0 = 64 * hq + 32 * cc;  // first query column (in the tile) of this chunk
+      for (int s = 0; s < 2; ++s, ++n) {
+        const int bf = n & 1, sq = n % kQStages;
+        const int iq0 = qt * kTile + kSub * s;  // first query of the sub-tile
+        if (!(ok = wait_bar_warp(&bars[kBarSFull + bf], (n >> 1) & 1, abort_flag, budget))) break;
+        // the prologue's LSE/Delta for this stage become visible through this wait
+        if (!(ok = wait_bar_warp(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget))) break;
+        tc_fence_after();
+        const float* st_lse = stat + sq * 2 * kSub;
+        const float* st_dl = st_lse + kSub;
+        const uint32_t tS = tmem + lanebits + s_col(n), tdP = tmem + lanebits + dp_col(n);
+        // plain sub-tiles: every query row valid, no mask values, no causal diagonal
+        const bool plain = flag != kTileAllFalse && iq0 + kSub <= c.Sq &&
+                           (MK == kMaskNone || mask_bcast_q || (MK == kMaskBool && flag == kTileAllTrue)) &&
+                           (!CAUSAL || iq0 >= kt * kTile + kTile - 1);
+        // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), bf16 into TMEM
+        uint32_t pw[16];
+        {
           uint32_t sv[32];
-          tmem_ld32(tA + q0, sv);
+          tmem_ld32(tS + q0, sv);
+          if (plain) {
+            const float2 sc2 = make_float2(sc, sc), kt2 = make_float2(key_term, key_term);
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4) {
-            const float4 l = *reinterpret_cast<const float4*>(st_lse + q0 + 4 * v4);
-            const float2 c01 = __fadd2_rn(kt2, make_float2(-l.x, -l.y)), c23 = __fadd2_rn(kt2, make_float2(-l.z, -l.w));
-            const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4]), __uint_as_float(sv[4 * v4 + 1])), sc2, c01);
-            const float2 x23 =
-                __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4 + 2]), __uint_as_float(sv[4 * v4 + 3])), sc2, c23);
-            pw[16 * cc + 2 * v4] = pack_bf16(ex2(x01.x), ex2(x01.y));
-            pw[16 * cc + 2 * v4 + 1] = pack_bf16(ex2(x23.x), ex2(x23.y));
-          }
-        }
-      } else if constexpr (!ELEM) {
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int q0 = 64 * hq + 32 * cc;
-          uint32_t sv[32];
-          tmem_ld32(tA + q0, sv);
-#pragma unroll
-          for (int t2 = 0; t2 < 16; ++t2) {
-            float p2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int t = 2 * t2 + e;
-              const float s2 = score2<MK, CAUSAL>(c, __uint_as_float(sv[t]), key_term, b, h, qt * kTile + q0 + t, j,
-                                                  key_ok, flag, mask_bcast_q);
-              p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
+            for (int v4 = 0; v4 < 8; ++v4) {
+              const float4 l = *reinterpret_cast<const float4*>(st_lse + q0 + 4 * v4);
+              const float2 c01 = __fadd2_rn(kt2, make_float2(-l.x, -l.y)), c23 = __fadd2_rn(kt2, make_float2(-l.z, -l.w));
+              const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4]), __uint_as_float(sv[4 * v4 + 1])), sc2, c01);
+              const float2 x23 =
+                  __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4 + 2]), __uint_as_float(sv[4 * v4 + 3])), sc2, c23);
+              pw[2 * v4] = pack_bf16(ex2(x01.x), ex2(x01.y));
+              pw[2 * v4 + 1] = pack_bf16(ex2(x23.x), ex2(x23.y));
             }
-            pw[16 * cc + t2] = pack_bf16(p2[0], p2[1]);
-          }
-        }
-      } else {
-        // 16 queries at a time; the next chunk's mask terms are loaded while
-        // this one is computed (pinned at the end of the chunk)
-        const bool elem_mask = ELEM && key_ok && flag != kTileAllFalse && !(MK == kMaskBool && flag == kTileAllTrue);
-        float mv[2][16];
-        uint32_t mraw[2][16];
-        auto issue = [&](int c4, uint32_t (&raw)[16]) {
+          } else if constexpr (!ELEM) {
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            raw[t] = 0u;
-            if constexpr (ELEM) {
-              const int iq = qt * kTile + 64 * hq + 16 * c4 + t;
-              if (elem_mask && iq < c.Sq) {
-                const int64_t off = b * c.m_sb + h * c.m_sh + (int64_t)iq * c.m_sq + j;
-                if constexpr (MK == kMaskBool) raw[t] = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0u : 1u;
-                else if constexpr (MK == kMaskF32)
-                  raw[t] = __float_as_uint(ldg_nc_f32(static_cast<const float*>(c.mask) + off));
-                else raw[t] = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(c.mask) + off)) << 16;
+            for (int t2 = 0; t2 < 16; ++t2) {
+              float p2[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int t = 2 * t2 + e;
+                const float s2 = score2<MK, CAUSAL>(c, __uint_as_float(sv[t]), key_term, b, h, iq0 + q0 + t, j, key_ok,
+                                                    flag, mask_bcast_q);
+                p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
+              }
+              pw[t2] = pack_bf16(p2[0], p2[1]);
+            }
+          } else {
+            // per-element mask terms of the 32 queries, 16 at a time (loads pinned)
+            const bool elem_mask = key_ok && flag != kTileAllFalse && !(MK == kMaskBool && flag == kTileAllTrue);
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              uint32_t raw[16];
+#pragma unroll
+              for (int t = 0; t < 16; ++t) {
+                raw[t] = 0u;
+                const int iq = iq0 + q0 + 16 * hh + t;
+                if (elem_mask && iq < c.Sq) {
+                  const int64_t off = b * c.m_sb + h * c.m_sh + (int64_t)iq * c.m_sq + j;
+                  if constexpr (MK == kMaskBool) raw[t] = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0u : 1u;
+                  else if constexpr (MK == kMaskF32)
+                    raw[t] = __float_as_uint(ldg_nc_f32(static_cast<const float*>(c.mask) + off));
+                  else raw[t] = static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(c.mask) + off)) << 16;
+                }
+              }
+              uint32_t folded = 0;
+#pragma unroll
+              for (int t = 0; t < 16; ++t) folded ^= raw[t];
+              pin_loads(folded, scratch);
+#pragma unroll
+              for (int t2 = 0; t2 < 8; ++t2) {
+                float p2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int tl = 2 * t2 + e, t = 16 * hh + tl;
+                  const float mterm = (MK == kMaskBool) ? (raw[tl] ? -INFINITY : 0.f) : __uint_as_float(raw[tl]) * kLog2e;
+                  const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mterm, iq0 + q0 + t, j, flag);
+                  p2[e] = ex2(s2 - st_lse[q0 + t]);
+                }
+                pw[8 * hh + t2] = pack_bf16(p2[0], p2[1]);
               }
             }
           }
-        };
-        auto settle = [&](const uint32_t (&raw)[16], float (&m)[16]) {  // pin, then convert
-          uint32_t folded = 0;
+        }
+        tmem_st16(tS + q0, pw);  // the first 16 of the warp's own 32 S^T columns
+        // ---- dS^T = P^T (dP^T - Delta), bf16 into shared memory (row r, K-major)
+        if (!(ok = wait_bar_warp(&bars[kBarDPFull + bf], (n >> 1) & 1, abort_flag, budget))) break;
+        tc_fence_after();
+        {
+          uint32_t dpv[32];
+          tmem_ld32(tdP + q0, dpv);
+          uint8_t* dsb = sm + kOffDS + bf * kSubBytes;
 #pragma unroll
-          for (int t = 0; t < 16; ++t) folded ^= raw[t];
-          pin_loads(folded, scratch);
+          for (int u = 0; u < 4; ++u) {  // 8 queries = one 16-byte chunk of the dS^T row
+            const float4 d0 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u);
+            const float4 d1 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u + 4);
+            const float2 ndl[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
+                                   make_float2(-d1.z, -d1.w)};
+            uint32_t out[4];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            if constexpr (MK == kMaskBool) m[t] = raw[t] ? -INFINITY : 0.f;
-            else m[t] = __uint_as_float(raw[t]) * kLog2e;
-          }
-        };
-        issue(0, mraw[0]);
-        settle(mraw[0], mv[0]);
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          if (c4 < 3) issue(c4 + 1, mraw[(c4 + 1) & 1]);
-          const int q0 = 64 * hq + 16 * c4;  // first query column (in the tile) of this chunk
-          uint32_t sv[16];
-          tmem_ld16(tA + q0, sv);
-#pragma unroll
-          for (int t2 = 0; t2 < 8; ++t2) {
-            float p2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int t = 2 * t2 + e;
-              const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mv[c4 & 1][t], qt * kTile + q0 + t, j, flag);
-              p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
+            for (int e = 0; e < 4; ++e) {
+              const uint32_t pp = pw[4 * u + e];
+              const float2 dp = make_float2(__uint_as_float(dpv[8 * u + 2 * e]), __uint_as_float(dpv[8 * u + 2 * e + 1]));
+              const float2 ds = __fmul2_rn(make_float2(bf16_lo(pp), bf16_hi(pp)), __fadd2_rn(dp, ndl[e]));
+              out[e] = pack_bf16(ds.x, ds.y);
             }
-            pw[8 * c4 + t2] = pack_bf16(p2[0], p2[1]);
+            *reinterpret_cast<uint4*>(dsb + sw128_off(r, 4 * hq + u)) = make_uint4(out[0], out[1], out[2], out[3]);
           }
-          if (c4 < 3) settle(mraw[(c4 + 1) & 1], mv[(c4 + 1) & 1]);
         }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kBarCDone + bf]);
       }
-      tmem_st32(tP, pw);
-      // ---- dS^T = P^T (dP^T - Delta), bf16 into shared memory (row r, K-major)
-      if (!(ok = wait_bar_warp(&bars[kBarDPFull], n & 1, abort_flag, budget))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int q0 = 64 * hq + 32 * cc;
-        uint32_t dpv[32];
-        tmem_ld32(tB + q0, dpv);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {  // 8 queries = one 16-byte chunk of the dS^T row
-          const float4 d0 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u);
-          const float4 d1 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u + 4);
-          const float2 ndl[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
-                                 make_float2(-d1.z, -d1.w)};
-          uint32_t out[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t pp = pw[16 * cc + 4 * u + e];
-            const float2 dp = make_float2(__uint_as_float(dpv[8 * u + 2 * e]), __uint_as_float(dpv[8 * u + 2 * e + 1]));
-            const float2 ds = __fmul2_rn(make_float2(bf16_lo(pp), bf16_hi(pp)), __fadd2_rn(dp, ndl[e]));
-            out[e] = pack_bf16(ds.x, ds.y);
-          }
-          *reinterpret_cast<uint4*>(sm + kOffDS + hq * kHalfBytes + sw128_off(r, 4 * cc + u)) =
-              make_uint4(out[0], out[1], out[2], out[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(&bars[kBarHalf0 + hq]);
     }
     // ---- epilogue: warps of query half 0 write dV, half 1 scale * dK' (fp32;
     // the inverse rotation and the RMSNorm backward run in a row kernel after)
-    if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQFull], (n - 1) & 1, abort_flag, budget);
+    if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
     if (ok) {
       tc_fence_after();
       const uint32_t tacc = tmem + (hq == 0 ? 256 : 384) + lanebits;
@@ -430,69 +413,48 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     }
   } else if (warp < kWarpDrain0 + kDrainWarps) {
     // ------------------------------------------------------------ dQ drain
-    // The tile's partial dQ (128 query rows x 128 head dims, fp32) leaves B
-    // at once: columns 0-63 are staged in shared memory, 64-127 held in
-    // registers, then B is released; each half goes out as two TMA bulk
-    // reduces (fp32 add into the global accumulator).
+    // A sub-tile's dQ'^T (128 head dims x 64 queries, fp32) leaves TMEM at once
+    // (64 registers per thread) and its columns are released. Warp qd stages
+    // head dims [32 qd, +32) as a [64 query][32] box and lane 0 adds it into
+    // the global accumulator (TMA bulk reduce); the box is rewritten one
+    // sub-tile later, once that reduce has read it. The warps never wait for
+    // one another.
     const int qd = warp & 3;
-    const int qrow = qd * 32 + lane_id;  // query row in the tile = TMEM lane
-    const uint32_t tB = tmem + 128 + (static_cast<uint32_t>(qd * 32) << 16);
-    uint8_t* R = sm + kOffR;
+    const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
+    uint8_t* box = sm + kOffR + qd * kRBoxBytes;
     const float scale = c.scale;
-    const bool issuer = warp == kWarpDrain0 && lane_id == 0;
-    auto stage32 = [&](int box, const uint32_t (&v)[32]) {  // 32 columns of this row into staging box `box`
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(R + box * kRBoxBytes + sw128_off(qrow, k)) =
-            make_uint4(__float_as_uint(__uint_as_float(v[4 * k]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 1]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 2]) * scale),
-                       __float_as_uint(__uint_as_float(v[4 * k + 3]) * scale));
-    };
+    const bool leader = lane_id == 0;
+    const uint32_t chunk = static_cast<uint32_t>(lane_id) >> 2, word = (lane_id & 3) * 4;
     int n = 0;
-    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0), ++n) {
+    bool ok = true;
+    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); ok && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
       const int qt = W.qt(m);
-      // A failed wait skips the work but not the named barriers below; every
-      // thread then leaves together on the abort flag.
-      const bool ok = wait_bar_warp(&bars[kBarDQFull], n & 1, abort_flag, budget);
-      uint32_t hold0[32], hold1[32];
-      if (ok) {
+      for (int s = 0; s < 2; ++s, ++n) {
+        const int bf = n & 1;
+        if (!(ok = wait_bar_warp(&bars[kBarDQ + bf], (n >> 1) & 1, abort_flag, budget))) break;
         tc_fence_after();
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          uint32_t v[32];
-          tmem_ld32(tB + 32 * cc, v);
-          stage32(cc, v);
-        }
-        tmem_ld32(tB + 64, hold0);
-        tmem_ld32(tB + 96, hold1);
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lanebits + s_col(n), v0);
+        tmem_ld32(tmem + lanebits + s_col(n) + 32, v1);
         tc_fence_before();
-        mbar_arrive(&bars[kBarBFree]);
+        mbar_arrive(&bars[kBarBFree + bf]);
+        if (leader) bulk_wait_read_all();  // the previous reduce has read the box
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < kSub; ++q) {  // row q of the box: 32 consecutive head dims, 128B-swizzled
+          const uint32_t v = q < 32 ? v0[q] : v1[q - 32];
+          *reinterpret_cast<float*>(box + q * 128 + ((chunk ^ (q & 7)) << 4) + word) = __uint_as_float(v) * scale;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int row = qt * kTile + kSub * s;
+        if (leader && row < c.Sq) {  // a sub-tile wholly past S_q adds nothing
+          tma_reduce_add_4d(&P.tmap_dq, box, 32 * qd, h, row, b);
+          bulk_commit_group();
+        }
       }
-      fence_proxy_async_smem();
-      named_bar(2, kDrainWarps * 32);
-      if (*abort_flag) break;
-      const int row = qt * kTile;
-      if (issuer) {
-        tma_reduce_add_4d(&P.tmap_dq, R, 0, h, row, b);
-        tma_reduce_add_4d(&P.tmap_dq, R + kRBoxBytes, 32, h, row, b);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
-      named_bar(2, kDrainWarps * 32);  // staging read: columns 64-127 next
-      stage32(0, hold0);
-      stage32(1, hold1);
-      fence_proxy_async_smem();
-      named_bar(2, kDrainWarps * 32);
-      if (issuer) {
-        tma_reduce_add_4d(&P.tmap_dq, R, 64, h, row, b);
-        tma_reduce_add_4d(&P.tmap_dq, R + kRBoxBytes, 96, h, row, b);
-        bulk_commit_group();
-        bulk_wait_read_all();
-      }
-      named_bar(2, kDrainWarps * 32);  // staging free for the next tile
     }
-    if (issuer) bulk_wait_all();
+    if (leader) bulk_wait_all();
   } else if (warp < kWarpProl0 + kProlWarps) {
     // ------------------------------------------------------------ Q' / K' prologue
     const int p = tid - kWarpProl0 * 32;  // 0 .. kProlThreads - 1
@@ -526,99 +488,89 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     const uint32_t peer_q = mapa_shared(smem_u32(sm + kOffQ), peer);
     const uint32_t peer_qfull = mapa_shared(smem_u32(&bars[kBarQFull]), peer);
     // Q' rows: eight lanes per row (see OctRow), four rows per warp and pass;
-    // pass k of warp pw handles row 16k + 4pw + (lane & 3) of this CTA's 64.
-    // The (cos, sin) rows of the next tile are loaded while this one is
-    // finished, pass by pass, and pinned before the next tile starts.
+    // pass k (0, 1) of warp pw handles row 16k + 4pw + (lane & 3) of this
+    // CTA's 32 rows of a sub-tile. The (cos, sin) rows of the next sub-tile
+    // are loaded while this one is finished and pinned before it starts.
     const int part = lane_id >> 2, pw = warp - kWarpProl0;
-    constexpr int kPasses = kHalfRows / (kProlWarps * 4);
-    auto pass_row = [&](int k) { return kHalfRows * crank + 4 * kProlWarps * k + 4 * pw + (lane_id & 3); };
+    const int ra = kPeerRows * static_cast<int>(crank) + 4 * pw + (lane_id & 3), rb = ra + 16;
     const __half2* tab16 = c.tab16_q + b * c.tab_q_sb;
-    OctRow rp[kPasses];
-    int m = next_pos<MK>(c, b, h, W, 0, kt0);
+    OctRow rp[2];
+    // LSE and Delta of row p of the current sub-tile, loaded one sub-tile ahead
+    float lse_c = -INFINITY, dl_c = 0.f;
+    auto load_stats = [&](int iq0) {
+      lse_c = -INFINITY;
+      dl_c = 0.f;
+      if (p < kSub && iq0 + p < c.Sq) {
+        const int64_t ri = ((int64_t)b * c.H + h) * c.Sq + iq0 + p;
+        lse_c = ldg_nc_f32(P.lse + ri);
+        dl_c = ldg_nc_f32(P.delta + ri);
+      }
+    };
+    int m = next_pos<MK>(c, b, h, W, 0, kt0), s = 0;
+    if (m < W.len) load_stats(W.qt(m) * kTile);
     if constexpr (QKT) {
       if (m < W.len) {
-#pragma unroll
-        for (int k = 0; k < kPasses; ++k) {
-          const int i = W.qt(m) * kTile + pass_row(k);
-          if (i < c.Sq) rp[k].prefetch(tab16 + (int64_t)i * kPairs, part);
-        }
+        const int i0 = W.qt(m) * kTile;
+        if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
+        if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
       }
     }
-    int n = 0;
-    for (; ok && m < W.len; ++n) {
+    for (int n = 0; ok && m < W.len; ++n) {
       const int qt = W.qt(m);
-      const int m_next = next_pos<MK>(c, b, h, W, m + 1, kt0);
-      const int s = n % kQStages;
-      uint8_t* tile = sm + kOffQ + s * kTileBytes;
-      // LSE (base 2; +inf for rows without keys, so P = 0) and Delta of rows
-      // p, p + kProlThreads, ...: every CTA keeps all 128 of the tile
-      constexpr int kStatRows = kTile / kProlThreads;
-      float l2[kStatRows], dl[kStatRows];
-#pragma unroll
-      for (int u = 0; u < kStatRows; ++u) {
-        const int ii = qt * kTile + p + kProlThreads * u;
-        l2[u] = INFINITY;
-        dl[u] = 0.f;
-        if (ii < c.Sq) {
-          const int64_t ri = ((int64_t)b * c.H + h) * c.Sq + ii;
-          const float l = ldg_nc_f32(P.lse + ri);
-          l2[u] = (l == -INFINITY) ? INFINITY : l * kLog2e;
-          dl[u] = ldg_nc_f32(P.delta + ri);
-        }
-      }
+      // the next sub-tile of the walk
+      const int m_next = s == 0 ? m : next_pos<MK>(c, b, h, W, m + 1, kt0), s_next = s ^ 1;
+      const int sq = n % kQStages;
+      uint8_t* stage = sm + kOffQ + sq * kSubBytes;
+      const int iq0 = qt * kTile + kSub * s;
+      if constexpr (QKT) pin_loads(rp[1].fold(rp[0].fold(__float_as_uint(lse_c) ^ __float_as_uint(dl_c))), scratch);
+      // LSE (base 2; +inf for rows without keys or past S_q, so P = 0) and
+      // Delta of the sub-tile's 64 rows (every CTA keeps all of them)
+      const float l2 = (lse_c == -INFINITY) ? INFINITY : lse_c * kLog2e, dl = dl_c;
       // a failed wait skips the work but not the named barrier below
       if constexpr (QKT) {
-        uint32_t folded = 0;
-#pragma unroll
-        for (int k = 0; k < kPasses; ++k) folded = rp[k].fold(folded);
-        pin_loads(folded, scratch);
-        if (wait_bar_warp(&bars[kBarQRaw + s], (n / kQStages) & 1, abort_flag, budget)) {
-#pragma unroll
-          for (int k = 0; k < kPasses; k += 2) {  // rows past S_q stay TMA zeros
-            const int ra = pass_row(k), rb = pass_row(k + 1);
-            OctRow::finish2(rp[k], rp[k + 1], tile, ra, rb, part, sWq, c.eps, qt * kTile + ra < c.Sq,
-                            qt * kTile + rb < c.Sq);
-            if (m_next < W.len) {
-              const int ia = W.qt(m_next) * kTile + ra, ib = W.qt(m_next) * kTile + rb;
-              if (ia < c.Sq) rp[k].prefetch(tab16 + (int64_t)ia * kPairs, part);
-              if (ib < c.Sq) rp[k + 1].prefetch(tab16 + (int64_t)ib * kPairs, part);
-            }
+        if (wait_bar_warp(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) {
+          // rows past S_q stay TMA zeros
+          OctRow::finish2(rp[0], rp[1], stage, ra, rb, part, sWq, c.eps, iq0 + ra < c.Sq, iq0 + rb < c.Sq, kSubHalf);
+          if (m_next < W.len) {
+            const int i0 = W.qt(m_next) * kTile + kSub * s_next;
+            if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
+            if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
           }
         }
       } else {
-        if (n < kQStages || wait_bar_cluster(&bars[kBarQFree + s], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
-          for (int rr = p; rr < kHalfRows; rr += kProlThreads) {  // this CTA's 64 rows
-            const int row = kHalfRows * crank + rr;
-            const int i = qt * kTile + row;
+        if (n < kQStages || wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
+          for (int rr = p; rr < kPeerRows; rr += kProlThreads) {  // this CTA's 32 rows
+            const int row = kPeerRows * static_cast<int>(crank) + rr;
+            const int i = iq0 + row;
             if (i < c.Sq)
               rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
-                               c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, tile, row);
+                               c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, stage, row, kSubHalf);
             else
-              zero_row(tile, row);
+              zero_row(stage, row, kSubHalf);
           }
         }
       }
-#pragma unroll
-      for (int u = 0; u < kStatRows; ++u) {
-        stat[s * 256 + p + kProlThreads * u] = l2[u];
-        stat[s * 256 + 128 + p + kProlThreads * u] = dl[u];
+      if (p < kSub) {
+        stat[sq * 2 * kSub + p] = l2;
+        stat[sq * 2 * kSub + kSub + p] = dl;
       }
-      // this CTA's 64 rows are final: one bulk copy per 64-column half to the
+      if (m_next < W.len) load_stats(W.qt(m_next) * kTile + kSub * s_next);
+      // this CTA's 32 rows are final: one bulk copy per column half to the
       // same offsets of the peer's stage, completing on its Q' barrier
       fence_proxy_async_smem();
-      named_bar(3, kProlThreads);
-      if (*abort_flag) break;  // uniform: set before any failed thread reached the barrier
+      if (named_bar_any(3, kProlThreads, *abort_flag != 0)) break;
       if (p == 0) {
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t off = s * kTileBytes + hh * kHalfBytes + kHalfRowsBytes * crank;
-          bulk_copy_to_peer(peer_q + off, sm + kOffQ + off, kHalfRowsBytes, peer_qfull + 8u * s);
+          const uint32_t off = sq * kSubBytes + hh * kSubHalf + kPeerRowsBytes * crank;
+          bulk_copy_to_peer(peer_q + off, sm + kOffQ + off, kPeerRowsBytes, peer_qfull + 8u * sq);
         }
-        mbar_arrive_expect_tx(&bars[kBarQFull + s], 2 * kHalfRowsBytes);  // the peer's rows
+        mbar_arrive_expect_tx(&bars[kBarQFull + sq], 2 * kPeerRowsBytes);  // the peer's rows
       } else {
-        mbar_arrive(&bars[kBarQFull + s]);
+        mbar_arrive(&bars[kBarQFull + sq]);
       }
       m = m_next;
+      s = s_next;
     }
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: raw K, V, raw Q, dO
@@ -637,40 +589,39 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       } else {
         mbar_arrive(&bars[kBarVFull]);  // V is zeroed by the prologue, before K' is declared ready
       }
-      int n = 0, q_issued = 0, lo_issued = 0, hi_issued = 0;
-      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0), ++n) {
+      int n = 0, q_issued = 0, do_issued = 0;
+      bool stop = false;
+      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
         const int qt = W.qt(m);
-        const int s = n % kQStages;
-        if constexpr (QKT) {  // this CTA's 64 raw rows of the tile
-          if (n >= kQStages &&
-              !wait_bar_cluster(&bars[kBarQFree + s], ((n / kQStages) - 1) & 1, abort_flag, budget))
+        for (int s = 0; s < 2; ++s, ++n) {
+          const int sq = n % kQStages, sd = n % kDOStages;
+          if constexpr (QKT) {  // this CTA's 32 raw rows of the sub-tile
+            if (n >= kQStages &&
+                !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
+              stop = true;
+              break;
+            }
+            uint8_t* qrows = sm + kOffQ + sq * kSubBytes + kPeerRowsBytes * crank;
+            const int row = qt * kTile + kSub * s + kPeerRows * static_cast<int>(crank);
+            const int y = P.q_s_first ? row : h, z = P.q_s_first ? h : row;
+            mbar_arrive_expect_tx(&bars[kBarQRaw + sq], 2 * kPeerRowsBytes);
+            tma_load_4d(qrows, &P.tmap_q, &bars[kBarQRaw + sq], 0, y, z, b);
+            tma_load_4d(qrows + kSubHalf, &P.tmap_q, &bars[kBarQRaw + sq], 64, y, z, b);
+            ++q_issued;
+          }
+          if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) {
+            stop = true;
             break;
-          uint8_t* qrows = sm + kOffQ + s * kTileBytes + kHalfRowsBytes * crank;
-          const int row = qt * kTile + kHalfRows * crank;
-          const int y = P.q_s_first ? row : h, z = P.q_s_first ? h : row;
-          mbar_arrive_expect_tx(&bars[kBarQRaw + s], 2 * kHalfRowsBytes);
-          tma_load_4d(qrows, &P.tmap_q, &bars[kBarQRaw + s], 0, y, z, b);
-          tma_load_4d(qrows + kHalfBytes, &P.tmap_q, &bars[kBarQRaw + s], 64, y, z, b);
-          ++q_issued;
-        }
-        // dO rows [0, 64) and [64, 128) of the tile, 64-row boxes into each column half
-        if (n > 0 && !wait_bar(&bars[kBarDOLoFree], (n - 1) & 1, abort_flag, budget)) break;
-        {
-          const int row = qt * kTile;
-          const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
-          mbar_arrive_expect_tx(&bars[kBarDOLoFull], kTileBytes / 2);
-          tma_load_4d(sm + kOffDO, &P.tmap_do, &bars[kBarDOLoFull], 0, y, z, b);
-          tma_load_4d(sm + kOffDO + kHalfBytes, &P.tmap_do, &bars[kBarDOLoFull], 64, y, z, b);
-          ++lo_issued;
-        }
-        if (n > 0 && !wait_bar(&bars[kBarDOHiFree], (n - 1) & 1, abort_flag, budget)) break;
-        {
-          const int row = qt * kTile + 64;
-          const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
-          mbar_arrive_expect_tx(&bars[kBarDOHiFull], kTileBytes / 2);
-          tma_load_4d(sm + kOffDO + kHalfBytes / 2, &P.tmap_do, &bars[kBarDOHiFull], 0, y, z, b);
-          tma_load_4d(sm + kOffDO + kHalfBytes + kHalfBytes / 2, &P.tmap_do, &bars[kBarDOHiFull], 64, y, z, b);
-          ++hi_issued;
+          }
+          {
+            const int row = qt * kTile + kSub * s;
+            const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
+            uint8_t* dst = sm + kOffDO + sd * kSubBytes;
+            mbar_arrive_expect_tx(&bars[kBarDOFull + sd], kSubBytes);
+            tma_load_4d(dst, &P.tmap_do, &bars[kBarDOFull + sd], 0, y, z, b);
+            tma_load_4d(dst + kSubHalf, &P.tmap_do, &bars[kBarDOFull + sd], 64, y, z, b);
+            ++do_issued;
+          }
         }
       }
       // drain: every issued load lands before the CTA exits (these waits do not
@@ -679,92 +630,90 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         mbar_wait(&bars[kBarVFull], 0, budget);
         if constexpr (QKT) mbar_wait(&bars[kBarKRaw], 0, budget);
       }
-      if (lo_issued > 0) mbar_wait(&bars[kBarDOLoFull], (lo_issued - 1) & 1, budget);
-      if (hi_issued > 0) mbar_wait(&bars[kBarDOHiFull], (hi_issued - 1) & 1, budget);
+      for (int x = max(0, do_issued - kDOStages); x < do_issued; ++x)
+        mbar_wait(&bars[kBarDOFull + x % kDOStages], (x / kDOStages) & 1, budget);
       if constexpr (QKT) {
-        for (int m = max(0, q_issued - kQStages); m < q_issued; ++m)
-          mbar_wait(&bars[kBarQRaw + m % kQStages], (m / kQStages) & 1, budget);
+        for (int x = max(0, q_issued - kQStages); x < q_issued; ++x)
+          mbar_wait(&bars[kBarQRaw + x % kQStages], (x / kQStages) & 1, budget);
       }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     if (lane_id == 0) {
-      constexpr uint32_t idesc_kk = idesc_bf16(128, 128, 0, 0);
-      constexpr uint32_t idesc_kmn = idesc_bf16(128, 128, 0, 1);
-      constexpr uint32_t idesc_mnmn = idesc_bf16(128, 128, 1, 1);
+      constexpr uint32_t idesc_sdp = idesc_bf16(128, kSub, 0, 0);  // S^T, dP^T: N = 64 queries
+      constexpr uint32_t idesc_kv = idesc_bf16(128, 128, 0, 1);    // dV, dK': N = 128 head dims
+      constexpr uint32_t idesc_q = idesc_bf16(128, kSub, 1, 1);    // dQ'^T = K'^T dS^T
       const uint64_t dKk = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
       const uint64_t dKm = sdesc_sw128(smem_u32(sm + kOffK), kHalfBytes, 1024);
       const uint64_t dVk = sdesc_sw128(smem_u32(sm + kOffV), 16, 1024);
-      const uint64_t dOk = sdesc_sw128(smem_u32(sm + kOffDO), 16, 1024);
-      const uint64_t dOm = sdesc_sw128(smem_u32(sm + kOffDO), kHalfBytes, 1024);
-      const uint64_t dSk = sdesc_sw128(smem_u32(sm + kOffDS), 16, 1024);
-      const uint64_t dSm = sdesc_sw128(smem_u32(sm + kOffDS), kHalfBytes, 1024);
       const uint64_t dQk0 = sdesc_sw128(smem_u32(sm + kOffQ), 16, 1024);
-      const uint64_t dQm0 = sdesc_sw128(smem_u32(sm + kOffQ), kHalfBytes, 1024);
-      const uint32_t tA = tmem, tB = tmem + 128, tdV = tmem + 256, tdK = tmem + 384;
-      bool ok = wait_bar(&bars[kBarKFull], 0, abort_flag, budget) && wait_bar(&bars[kBarVFull], 0, abort_flag, budget);
-      int m = next_pos<MK>(c, b, h, W, 0, kt0);
-      int n = 0;
-      bool issued = false;
-      if (ok && m < W.len) {
-        ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
-        if (ok) {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tA, sdesc_add(dKk, kofs(kk)), sdesc_add(dQk0, kofs(kk)), idesc_kk, kk > 0);
-          mma_commit(&bars[kBarSFull]);
-          issued = true;
-          ok = wait_bar(&bars[kBarDOLoFull], 0, abort_flag, budget) &&
-               wait_bar(&bars[kBarDOHiFull], 0, abort_flag, budget);
-        }
-        if (ok) {
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tB, sdesc_add(dVk, kofs(kk)), sdesc_add(dOk, kofs(kk)), idesc_kk, kk > 0);
-          mma_commit(&bars[kBarDPFull]);
-        }
-      }
-      while (ok && m < W.len) {
-        const int s = n % kQStages;
-        const uint64_t dQm = sdesc_add(dQm0, s * kTileBytes);
-        if (!(ok = wait_bar(&bars[kBarHalf0], n & 1, abort_flag, budget))) break;
+      const uint64_t dQm0 = sdesc_sw128(smem_u32(sm + kOffQ), kSubHalf, 1024);
+      const uint64_t dOk0 = sdesc_sw128(smem_u32(sm + kOffDO), 16, 1024);
+      const uint64_t dOm0 = sdesc_sw128(smem_u32(sm + kOffDO), kSubHalf, 1024);
+      const uint64_t dSk0 = sdesc_sw128(smem_u32(sm + kOffDS), 16, 1024);
+      const uint64_t dSm0 = sdesc_sw128(smem_u32(sm + kOffDS), kSubHalf, 1024);
+      const uint32_t tdV = tmem + 256, tdK = tmem + 384;
+      int nsub = 0;  // sub-tiles in the walk
+      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) nsub += 2;
+      auto issue_s = [&](int n) -> bool {  // S^T(n) into its half of buffer n % 2
+        const int sq = n % kQStages;
+        if (!wait_bar(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
         tc_fence_after();
+        const uint64_t dQk = sdesc_add(dQk0, sq * kSubBytes);
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ts(tdV, tA + 8 * kk, sdesc_add(dOm, mofs(kk)), idesc_kmn, (n > 0 || kk > 0));
-        mma_commit(&bars[kBarDOLoFree]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + s_col(n), sdesc_add(dKk, kofs128(kk)), sdesc_add(dQk, kofs64(kk)), idesc_sdp, kk > 0);
+        mma_commit(&bars[kBarSFull + (n & 1)]);
+        return true;
+      };
+      auto issue_dp = [&](int n) -> bool {  // dP^T(n) into the other half
+        const int sd = n % kDOStages;
+        if (!wait_bar(&bars[kBarDOFull + sd], (n / kDOStages) & 1, abort_flag, budget)) return false;
+        tc_fence_after();
+        const uint64_t dOk = sdesc_add(dOk0, sd * kSubBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tmem + dp_col(n), sdesc_add(dVk, kofs128(kk)), sdesc_add(dOk, kofs64(kk)), idesc_sdp, kk > 0);
+        mma_commit(&bars[kBarDPFull + (n & 1)]);
+        return true;
+      };
+      bool ok = wait_bar(&bars[kBarKFull], 0, abort_flag, budget) && wait_bar(&bars[kBarVFull], 0, abort_flag, budget);
+      bool issued = false;
+      for (int n = 0; ok && n < nsub && n < 2; ++n) {
+        issued = true;
+        ok = issue_s(n) && issue_dp(n);
+      }
+      for (int n = 0; ok && n < nsub; ++n) {
+        const int bf = n & 1, sq = n % kQStages, sd = n % kDOStages;
+        if (!(ok = wait_bar(&bars[kBarCDone + bf], (n >> 1) & 1, abort_flag, budget))) break;
+        tc_fence_after();
+        // dV += P^T dO: P^T (bf16) in TMEM, queries 0-31 packed in columns 0-15 of
+        // the S^T half, queries 32-63 in columns 32-47
+        const uint32_t tP = tmem + s_col(n);
+        const uint64_t dOm = sdesc_add(dOm0, sd * kSubBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tdK, sdesc_add(dSk, kofs(kk)), sdesc_add(dQm, mofs(kk)), idesc_kmn, (n > 0 || kk > 0));
-        if (!(ok = wait_bar(&bars[kBarHalf1], n & 1, abort_flag, budget))) break;
-        tc_fence_after();
+          mma_ts(tdV, tP + 8 * kk + (kk >= 2 ? 16 : 0), sdesc_add(dOm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
+        mma_commit(&bars[kBarDOFree + sd]);
+        // dK' += dS^T Q'
+        const uint64_t dQm = sdesc_add(dQm0, sq * kSubBytes), dSk = sdesc_add(dSk0, bf * kSubBytes);
 #pragma unroll
-        for (int kk = 4; kk < 8; ++kk) mma_ts(tdV, tA + 64 + 8 * kk, sdesc_add(dOm, mofs(kk)), idesc_kmn, 1u);
-        mma_commit(&bars[kBarDOHiFree]);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tdK, sdesc_add(dSk, kk * 32), sdesc_add(dQm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
+        // dQ'^T = K'^T dS^T over P^T (the MMAs above read it first: same issuing thread, in order)
+        const uint64_t dSm = sdesc_add(dSm0, bf * kSubBytes);
 #pragma unroll
-        for (int kk = 4; kk < 8; ++kk) mma_ss(tdK, sdesc_add(dSk, kofs(kk)), sdesc_add(dQm, mofs(kk)), idesc_kmn, 1u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ss(tB, sdesc_add(dSm, mofs(kk)), sdesc_add(dKm, mofs(kk)), idesc_mnmn, kk > 0);
-        mma_commit(&bars[kBarDQFull]);
-        mma_commit_mc(&bars[kBarQFree + s], 0x3);  // released in both CTAs' view
-        const int m_next = next_pos<MK>(c, b, h, W, m + 1, kt0);
-        if (m_next < W.len) {
-          const int ns = (n + 1) % kQStages;
-          if (!(ok = wait_bar(&bars[kBarQFull + ns], ((n + 1) / kQStages) & 1, abort_flag, budget))) break;
-          tc_fence_after();
-          const uint64_t dQk = sdesc_add(dQk0, ns * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tA, sdesc_add(dKk, kofs(kk)), sdesc_add(dQk, kofs(kk)), idesc_kk, kk > 0);
-          mma_commit(&bars[kBarSFull]);
-          if (!(ok = wait_bar(&bars[kBarBFree], n & 1, abort_flag, budget))) break;
-          if (!(ok = wait_bar(&bars[kBarDOLoFull], (n + 1) & 1, abort_flag, budget))) break;
-          if (!(ok = wait_bar(&bars[kBarDOHiFull], (n + 1) & 1, abort_flag, budget))) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tB, sdesc_add(dVk, kofs(kk)), sdesc_add(dOk, kofs(kk)), idesc_kk, kk > 0);
-          mma_commit(&bars[kBarDPFull]);
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tP, sdesc_add(dKm, mofs(kk)), sdesc_add(dSm, mofs(kk)), idesc_q, kk > 0);
+        mma_commit(&bars[kBarDQ + bf]);
+        mma_commit_mc(&bars[kBarQFree + sq], 0x3);  // released in both CTAs' view
+        if (n + 2 < nsub) {
+          // S^T(n+2) over dP^T(n) (read by the compute warps before they signalled),
+          // dP^T(n+2) over dQ'^T(n) once the drain has read it
+          if (!(ok = issue_s(n + 2))) break;
+          if (!(ok = wait_bar(&bars[kBarBFree + bf], (n >> 1) & 1, abort_flag, budget))) break;
+          ok = issue_dp(n + 2);
         }
-        m = m_next;
-        ++n;
       }
       if (issued && !ok) {
         // abort: let every issued MMA finish before TMEM is released
@@ -786,7 +735,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     record_timeout(c);
   }
   tc_fence_before();
-  cluster_sync();  // no DSMEM store or remote arrival may target a CTA that has exited
+  cluster_sync();  // no DSMEM copy or remote arrival may target a CTA that has exited
   if (warp == kWarpMma) {
     __syncwarp();
     tmem_dealloc(tmem, 512);
@@ -826,8 +775,9 @@ cudaError_t launch_bwd_q(const BwdParams& p, cudaStream_t stream) {
   }
 }
 
-// Kernels are specialised on the mask kind, causal masking and whether q/k
-// are staged by TMA, so that each carries only its own code.
+// Kernels are specialised on the mask kind, causal masking, whether q/k are
+// staged by TMA and whether the mask varies along the queries, so that each
+// carries only its own code.
 cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream) {
   return p.qk_tma ? launch_bwd_q<true>(p, stream) : launch_bwd_q<false>(p, stream);
 }

@@ -74,9 +74,9 @@ struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
   CUtensorMap tmap_do;  // dO rows, 64-row boxes
-  CUtensorMap tmap_q;   // raw q / k rows (bf16 only; see qk_tma)
+  CUtensorMap tmap_q;   // raw q rows, 32-row boxes / raw k rows, 128-row boxes (bf16 only; see qk_tma)
   CUtensorMap tmap_k;
-  CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 128 rows (reduce target)
+  CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 64 rows (reduce target)
   int v_s_first, do_s_first, q_s_first, k_s_first;
   int qk_tma;
   const void* dout;
@@ -160,10 +160,10 @@ __device__ __forceinline__ void copy_row_bf16(const void* base, int64_t off, uin
     *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) = __ldg(p + c);
 }
 
-__device__ __forceinline__ void zero_row(uint8_t* tile, int row) {
+__device__ __forceinline__ void zero_row(uint8_t* tile, int row, uint32_t half = kHalfBytes) {
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c)
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) = make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) = make_uint4(0, 0, 0, 0);
 }
 
 // Stores a 128-element fp32 row to a bf16 or fp32 destination.
@@ -254,6 +254,18 @@ __device__ __forceinline__ bool wait_bar_cluster_warp(uint64_t* bar, uint32_t pa
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier that also ORs a predicate over the participating threads: the
+// result is the same in every thread (a uniform exit decision).
+__device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
 }
 
 // 2^x on the MUFU unit (flushes denormal results to zero).

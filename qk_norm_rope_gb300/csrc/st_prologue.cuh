@@ -174,13 +174,15 @@ struct OctRow {
   }
   // Two rows at once (independent chains interleaved for instruction-level
   // parallelism); same contract as finish().
+  // half: byte distance of the two 64-column halves (kHalfBytes for a
+  // 128-row tile, half that for a 64-row one)
   __device__ __forceinline__ static void finish2(const OctRow& ra, const OctRow& rb, uint8_t* tile, int row_a,
                                                  int row_b, int part, const float* w, float eps, bool valid_a,
-                                                 bool valid_b) {
+                                                 bool valid_b, uint32_t half = kHalfBytes) {
     uint4* pa0 = reinterpret_cast<uint4*>(tile + sw128_off(row_a, part));
-    uint4* pa1 = reinterpret_cast<uint4*>(tile + kHalfBytes + sw128_off(row_a, part));
+    uint4* pa1 = reinterpret_cast<uint4*>(tile + half + sw128_off(row_a, part));
     uint4* pb0 = reinterpret_cast<uint4*>(tile + sw128_off(row_b, part));
-    uint4* pb1 = reinterpret_cast<uint4*>(tile + kHalfBytes + sw128_off(row_b, part));
+    uint4* pb1 = reinterpret_cast<uint4*>(tile + half + sw128_off(row_b, part));
     uint4 va0 = *pa0, va1 = *pa1, vb0 = *pb0, vb1 = *pb1;
     const uint32_t ua[8] = {va0.x, va0.y, va0.z, va0.w, va1.x, va1.y, va1.z, va1.w};
     const uint32_t ub[8] = {vb0.x, vb0.y, vb0.z, vb0.w, vb1.x, vb1.y, vb1.z, vb1.w};
@@ -366,7 +368,8 @@ struct QuarterRowPrologue {
 // transform), the second time from L1.
 __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, int is_f32,
                                                  const float* __restrict__ w, float eps,
-                                                 const float2* __restrict__ tab, uint8_t* tile, int row) {
+                                                 const float2* __restrict__ tab, uint8_t* tile, int row,
+                                                 uint32_t half = kHalfBytes) {
   float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c) {
@@ -395,7 +398,7 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
       packed[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
       packed[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
     }
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) =
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) =
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
   }
 }
