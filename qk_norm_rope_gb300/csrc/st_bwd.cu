@@ -10,7 +10,7 @@
 // dQ'^T (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
 // bulk reduces. The two CTAs of a cluster share the Q' operand prologue.
 //
-// Warp roles (576 threads; 96 registers per thread):
+// Warp roles (608 threads; 96 registers per thread):
 //   warps 0-7    compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and
 //                queries [32*(w/4), +32) of each sub-tile; P^T goes to TMEM
 //                (bf16, inside the warp's own S^T columns), dS^T to shared
@@ -26,7 +26,9 @@
 //   warp 16      TMEM allocation + tcgen05.mma issue (one thread)
 //   warp 17      TMA: raw K, V once; this CTA's 32 raw Q rows per sub-tile
 //                (4-stage ring, a stage reused once both CTAs' MMAs released
-//                it); dO sub-tiles (2-stage ring)
+//                it)
+//   warp 18      TMA: dO sub-tiles (2-stage ring), so that the Q' ring never
+//                waits behind a dO stage
 // TMEM (512 columns): two sub-tile buffers of 128 columns, dV, dK'. A buffer
 // holds S^T (later P^T, later dQ'^T) in one 64-column half and dP^T in the
 // other; the halves swap roles on each use of the buffer.
@@ -46,8 +48,8 @@ constexpr int kCluster = 2;
 constexpr int kComputeWarps = 8;
 constexpr int kWarpDrain0 = 8, kDrainWarps = 4;
 constexpr int kWarpProl0 = 12, kProlWarps = 4;
-constexpr int kWarpMma = 16, kWarpTma = 17;
-constexpr int kBwdWarps = 18;
+constexpr int kWarpMma = 16, kWarpTma = 17, kWarpTmaDO = 18;
+constexpr int kBwdWarps = 19;
 constexpr int kBwdThreads = kBwdWarps * 32;
 constexpr int kProlThreads = kProlWarps * 32;
 constexpr int kSub = 64;                                   // queries per sub-tile
@@ -573,7 +575,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       s = s_next;
     }
   } else if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA: raw K, V, raw Q, dO
+    // ------------------------------------------------------------ TMA: raw K, V, raw Q
     if (lane_id == 0) {
       if (!phantom) {
         if constexpr (QKT) {
@@ -589,13 +591,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       } else {
         mbar_arrive(&bars[kBarVFull]);  // V is zeroed by the prologue, before K' is declared ready
       }
-      int n = 0, q_issued = 0, do_issued = 0;
+      int n = 0, q_issued = 0;
       bool stop = false;
-      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
-        const int qt = W.qt(m);
-        for (int s = 0; s < 2; ++s, ++n) {
-          const int sq = n % kQStages, sd = n % kDOStages;
-          if constexpr (QKT) {  // this CTA's 32 raw rows of the sub-tile
+      if constexpr (QKT) {
+        for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
+          const int qt = W.qt(m);
+          for (int s = 0; s < 2; ++s, ++n) {  // this CTA's 32 raw rows of the sub-tile
+            const int sq = n % kQStages;
             if (n >= kQStages &&
                 !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
               stop = true;
@@ -609,19 +611,6 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
             tma_load_4d(qrows + kSubHalf, &P.tmap_q, &bars[kBarQRaw + sq], 64, y, z, b);
             ++q_issued;
           }
-          if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) {
-            stop = true;
-            break;
-          }
-          {
-            const int row = qt * kTile + kSub * s;
-            const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
-            uint8_t* dst = sm + kOffDO + sd * kSubBytes;
-            mbar_arrive_expect_tx(&bars[kBarDOFull + sd], kSubBytes);
-            tma_load_4d(dst, &P.tmap_do, &bars[kBarDOFull + sd], 0, y, z, b);
-            tma_load_4d(dst + kSubHalf, &P.tmap_do, &bars[kBarDOFull + sd], 64, y, z, b);
-            ++do_issued;
-          }
         }
       }
       // drain: every issued load lands before the CTA exits (these waits do not
@@ -630,12 +619,33 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         mbar_wait(&bars[kBarVFull], 0, budget);
         if constexpr (QKT) mbar_wait(&bars[kBarKRaw], 0, budget);
       }
+      for (int x = max(0, q_issued - kQStages); x < q_issued; ++x)
+        mbar_wait(&bars[kBarQRaw + x % kQStages], (x / kQStages) & 1, budget);
+    }
+  } else if (warp == kWarpTmaDO) {
+    // ------------------------------------------------------------ TMA: dO
+    if (lane_id == 0) {
+      int n = 0, do_issued = 0;
+      bool stop = false;
+      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
+        const int qt = W.qt(m);
+        for (int s = 0; s < 2; ++s, ++n) {
+          const int sd = n % kDOStages;
+          if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) {
+            stop = true;
+            break;
+          }
+          const int row = qt * kTile + kSub * s;
+          const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
+          uint8_t* dst = sm + kOffDO + sd * kSubBytes;
+          mbar_arrive_expect_tx(&bars[kBarDOFull + sd], kSubBytes);
+          tma_load_4d(dst, &P.tmap_do, &bars[kBarDOFull + sd], 0, y, z, b);
+          tma_load_4d(dst + kSubHalf, &P.tmap_do, &bars[kBarDOFull + sd], 64, y, z, b);
+          ++do_issued;
+        }
+      }
       for (int x = max(0, do_issued - kDOStages); x < do_issued; ++x)
         mbar_wait(&bars[kBarDOFull + x % kDOStages], (x / kDOStages) & 1, budget);
-      if constexpr (QKT) {
-        for (int x = max(0, q_issued - kQStages); x < q_issued; ++x)
-          mbar_wait(&bars[kBarQRaw + x % kQStages], (x / kQStages) & 1, budget);
-      }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
@@ -700,13 +710,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           mma_ss(tdK, sdesc_add(dSk, kk * 32), sdesc_add(dQm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
+        mma_commit_mc(&bars[kBarQFree + sq], 0x3);  // the Q' stage is released in both CTAs' view
         // dQ'^T = K'^T dS^T over P^T (the MMAs above read it first: same issuing thread, in order)
         const uint64_t dSm = sdesc_add(dSm0, bf * kSubBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tP, sdesc_add(dKm, mofs(kk)), sdesc_add(dSm, mofs(kk)), idesc_q, kk > 0);
         mma_commit(&bars[kBarDQ + bf]);
-        mma_commit_mc(&bars[kBarQFree + sq], 0x3);  // released in both CTAs' view
         if (n + 2 < nsub) {
           // S^T(n+2) over dP^T(n) (read by the compute warps before they signalled),
           // dP^T(n+2) over dQ'^T(n) once the drain has read it
