@@ -493,7 +493,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     // pass k (0, 1) of warp pw handles row 16k + 4pw + (lane & 3) of this
     // CTA's 32 rows of a sub-tile. The (cos, sin) rows of the next sub-tile
     // are loaded while this one is finished and pinned before it starts.
-    const int part = lane_id >> 2, pw = warp - kWarpProl0;
+    // Chunk (part) order over the lanes: the eight lanes of a quarter warp
+    // hold chunks c and c + 4 of four consecutive rows, eight distinct 16-byte
+    // slots of the swizzled rows, so their shared-memory accesses do not
+    // conflict.
+    const int part = (((lane_id >> 2) & 1) << 2) | (lane_id >> 3), pw = warp - kWarpProl0;
     const int ra = kPeerRows * static_cast<int>(crank) + 4 * pw + (lane_id & 3), rb = ra + 16;
     const __half2* tab16 = c.tab16_q + b * c.tab_q_sb;
     OctRow rp[2];
