@@ -544,16 +544,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
           }
         }
       } else {
-        if (n < kQStages || wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
-          for (int rr = p; rr < kPeerRows; rr += kProlThreads) {  // this CTA's 32 rows
-            const int row = kPeerRows * static_cast<int>(crank) + rr;
-            const int i = iq0 + row;
-            if (i < c.Sq)
-              rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
-                               c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, stage, row, kSubHalf);
-            else
-              zero_row(stage, row, kSubHalf);
-          }
+        static_assert(kProlThreads == 4 * kPeerRows, "four lanes per Q' row");
+        if (n < kQStages ||
+            wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
+          // this CTA's 32 rows, four lanes per row (rows past S_q become zeros)
+          const int row = kPeerRows * static_cast<int>(crank) + (p >> 2);
+          const bool valid = iq0 + row < c.Sq;
+          const int i = valid ? iq0 + row : 0;
+          rope_norm_global_quad(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
+                                c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, stage, row, p & 3, valid, kSubHalf);
         }
       }
       if (p < kSub) {

@@ -403,4 +403,49 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
   }
 }
 
+// Four-lanes-per-row form of rope_norm_global: lane `quarter` (0..3) of the
+// four lanes that share a row handles head dims [32 quarter, +32) (chunks
+// 4 quarter .. 4 quarter + 3); the row's sum of squares is reduced over the four
+// lanes with shuffles, so every lane of the warp calls it (valid: the row
+// exists; the four lanes of a row agree; an invalid row is written as zeros).
+__device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t off, int is_f32,
+                                                      const float* __restrict__ w, float eps,
+                                                      const float2* __restrict__ tab, uint8_t* tile, int row,
+                                                      int quarter, bool valid, uint32_t half) {
+  float x[4][8];
+  float ss = 0.f;
+  if (valid) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) load_chunk8(base, off, is_f32, 4 * quarter + i, x[i]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(x[i][e], x[i][e], ss);
+    }
+  }
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+  const float r = rsqrtf(ss * (1.0f / kD) + eps);
+  const float4* t4 = reinterpret_cast<const float4*>(tab);
+  const float4* w4 = reinterpret_cast<const float4*>(w);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = 4 * quarter + i;
+    uint32_t packed[4] = {0u, 0u, 0u, 0u};
+    if (valid) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float4 cs = __ldg(t4 + 2 * c + hh);
+        const float4 ww = __ldg(w4 + 2 * c + hh);
+        const float n0 = x[i][4 * hh] * ww.x * r, n1 = x[i][4 * hh + 1] * ww.y * r;
+        const float n2 = x[i][4 * hh + 2] * ww.z * r, n3 = x[i][4 * hh + 3] * ww.w * r;
+        packed[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+        packed[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+      }
+    }
+    *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) =
+        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+  }
+}
+
 }  // namespace st
