@@ -64,6 +64,14 @@ def _load():
             lib.oracle_fwd.restype = c_int
             lib.oracle_bwd.argtypes = common + [dp, ip, c_int, dp, dp, dp, dp, dp]
             lib.oracle_bwd.restype = c_int
+            lib.oracle_qk_transform_tab.argtypes = [dp, c_i64, c_int, dp, c_dbl, dp, dp, dp]
+            lib.oracle_qk_transform_tab.restype = None
+            common_tab = [c_int, c_int, c_int, c_int, c_int, dp, dp, dp, dp, dp, c_dbl, dp, dp, c_int, dp, dp,
+                          c_int, c_int, vp, i64p, c_int, c_dbl]
+            lib.oracle_fwd_tab.argtypes = common_tab + [ip, c_int, dp, dp]
+            lib.oracle_fwd_tab.restype = c_int
+            lib.oracle_bwd_tab.argtypes = common_tab + [dp, ip, c_int, dp, dp, dp, dp, dp]
+            lib.oracle_bwd_tab.restype = c_int
             _lib = lib
     return _lib
 
@@ -191,4 +199,90 @@ def bwd(q, k, v, wq, wk, eps, ids_q, axes_dim, theta, dout, mask=None, causal=Fa
                             _dp(dout), hp, nh, _dp(dq), _dp(dk), _dp(dv), _dp(dwq), _dp(dwk))
     if rc != 0:
         raise MemoryError("oracle_bwd could not allocate its work buffers")
+    return dq, dk, dv, dwq, dwk
+
+
+# ---------------------------------------------------------------- table form
+# The pages' entry point takes the rotation as cos/sin tables ("Metal Flash
+# Attention", section "Fused RoPE + SDPA": pair-duplicated, shape [S, D],
+# [1, S, D] or per-sample [B, S, D]). The oracle applies them elementwise,
+# y = x * cos + rot(x) * sin with rot(x) = (-x1, x0) per interleaved pair.
+
+
+def _tables(cos_t, sin_t, S, D):
+    """[Bp, S, D] fp64 copies of a table pair of shape [S, D] or [Bp, S, D]."""
+    c, s = _f64(cos_t), _f64(sin_t)
+    assert c.shape == s.shape and c.shape[-2:] == (S, D), (c.shape, s.shape, S, D)
+    if c.ndim == 2:
+        c, s = c[None], s[None]
+    assert c.ndim == 3
+    return np.ascontiguousarray(c), np.ascontiguousarray(s)
+
+
+def qk_transform_tab(x, w, eps: float, cos_t, sin_t) -> np.ndarray:
+    """RoPE(RMSNorm(x)) row by row with table rows: x, cos_t, sin_t [..., D]."""
+    x = _f64(x)
+    c = _f64(np.broadcast_to(cos_t, x.shape))
+    s = _f64(np.broadcast_to(sin_t, x.shape))
+    w = _f64(w)
+    out = np.zeros_like(x)
+    n = int(np.prod(x.shape[:-1]))
+    _load().oracle_qk_transform_tab(_dp(x), n, x.shape[-1], _dp(w), float(eps), _dp(c), _dp(s), _dp(out))
+    return out
+
+
+def _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k):
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    assert k.shape == (B, Skv, H, D) and v.shape == (B, Skv, H, D)
+    if cos_k is None:
+        assert Sq == Skv, "cos_k/sin_k are required when S_q != S_kv"
+        cos_k, sin_k = cos_q, sin_q
+    cq, sq = _tables(cos_q, sin_q, Sq, D)
+    ck, sk = _tables(cos_k, sin_k, Skv, D)
+    assert cq.shape[0] in (1, B) and ck.shape[0] in (1, B)
+    return q, k, v, _f64(wq), _f64(wk), cq, sq, ck, sk, B, Sq, Skv, H, D
+
+
+def fwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, mask=None, causal=False, scale=None, cos_k=None, sin_k=None,
+            heads=None):
+    """As fwd, with the rotation given by cos/sin tables instead of ids."""
+    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    kind, marr, mst = _mask_args(mask, B, H, Sq, Skv)
+    o = np.full((B, Sq, H, D), np.nan)
+    lse = np.full((B, H, Sq), np.nan)
+    hp, nh = _heads_arg(heads, B, H)
+    rc = _load().oracle_fwd_tab(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
+                                _dp(sq), cq.shape[0], _dp(ck), _dp(sk), ck.shape[0], kind,
+                                None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale), hp,
+                                nh, _dp(o), _dp(lse))
+    if rc != 0:
+        raise MemoryError("oracle_fwd_tab could not allocate its work buffers")
+    return o, lse
+
+
+def bwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, dout, mask=None, causal=False, scale=None, cos_k=None, sin_k=None,
+            heads=None):
+    """As bwd, with the rotation given by cos/sin tables instead of ids."""
+    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dout = _f64(dout)
+    assert dout.shape == q.shape
+    kind, marr, mst = _mask_args(mask, B, H, Sq, Skv)
+    dq = np.full(q.shape, np.nan)
+    dk = np.full(k.shape, np.nan)
+    dv = np.full(v.shape, np.nan)
+    dwq = np.zeros(D)
+    dwk = np.zeros(D)
+    hp, nh = _heads_arg(heads, B, H)
+    rc = _load().oracle_bwd_tab(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
+                                _dp(sq), cq.shape[0], _dp(ck), _dp(sk), ck.shape[0], kind,
+                                None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale),
+                                _dp(dout), hp, nh, _dp(dq), _dp(dk), _dp(dv), _dp(dwq), _dp(dwk))
+    if rc != 0:
+        raise MemoryError("oracle_bwd_tab could not allocate its work buffers")
     return dq, dk, dv, dwq, dwk

@@ -25,7 +25,10 @@
  * fully-masked rows, causal alignment) are stated beside the code below.
  *
  * Layouts: q, dq, o, do are [B, S_q, H, D]; k, v, dk, dv are [B, S_kv, H, D];
- * all contiguous fp64. Angles phi are [Bp, S, D/2] with Bp in {1, B}.
+ * all contiguous fp64. The rotation comes either from angles phi [Bp, S, D/2]
+ * or from the pages' cos/sin tables [Bp, S, D] (same page, section "Fused
+ * RoPE + SDPA": pair-duplicated tables of shape [S, D], [1, S, D] or
+ * [B, S, D]), with Bp in {1, B}.
  */
 #include <math.h>
 #include <stdint.h>
@@ -76,35 +79,73 @@ static double rmsnorm_row(const double* x, const double* w, int D, double eps, d
   return r;
 }
 
-/* Interleaved-pair rotation (counter-clockwise):
- *   y0 = x0 cos(phi) - x1 sin(phi),  y1 = x0 sin(phi) + x1 cos(phi). */
-static void rope_row(const double* x, const double* phi, int D, double* y) {
+/* Rotation source of one head: angles (phi: [S][D/2]) or the pages' tables
+ * (cos, sin: [S][D]); exactly one of phi and cos is set. */
+typedef struct {
+  const double* phi;
+  const double* cos;
+  const double* sin;
+} rot_src;
+
+/* The rows of batch element b (per-sample sources have Bp = B). */
+static rot_src rot_at(const rot_src* r, int bp, int b, int S, int D) {
+  const int64_t bi = bp > 1 ? b : 0;
+  rot_src o = {NULL, NULL, NULL};
+  if (r->phi) o.phi = r->phi + bi * S * (D / 2);
+  else {
+    o.cos = r->cos + bi * S * D;
+    o.sin = r->sin + bi * S * D;
+  }
+  return o;
+}
+
+/* Interleaved-pair rotation (counter-clockwise) of row s:
+ *   angles: y0 = x0 cos(phi) - x1 sin(phi),  y1 = x0 sin(phi) + x1 cos(phi);
+ *   tables: y = x * cos + rot(x) * sin elementwise, rot(x) = (-x1, x0) per
+ *   pair, which is the same rotation when the tables are pair-duplicated. */
+static void rope_row(const double* x, const rot_src* r, int64_t s, int D, double* y) {
   for (int p = 0; p < D / 2; ++p) {
-    const double c = cos(phi[p]), s = sin(phi[p]);
-    y[2 * p] = x[2 * p] * c - x[2 * p + 1] * s;
-    y[2 * p + 1] = x[2 * p] * s + x[2 * p + 1] * c;
+    if (r->phi) {
+      const double c = cos(r->phi[s * (D / 2) + p]), sn = sin(r->phi[s * (D / 2) + p]);
+      y[2 * p] = x[2 * p] * c - x[2 * p + 1] * sn;
+      y[2 * p + 1] = x[2 * p] * sn + x[2 * p + 1] * c;
+    } else {
+      const double* c = r->cos + s * D + 2 * p;
+      const double* sn = r->sin + s * D + 2 * p;
+      y[2 * p] = x[2 * p] * c[0] - x[2 * p + 1] * sn[0];
+      y[2 * p + 1] = x[2 * p + 1] * c[1] + x[2 * p] * sn[1];
+    }
   }
 }
 
-/* Inverse rotation: the same pairwise rotation with sin negated. */
-static void rope_row_inverse(const double* g, const double* phi, int D, double* y) {
+/* Transpose of that rotation (the backward): for angles, the same pairwise
+ * rotation with sin negated; for tables, the transpose of the elementwise form
+ * (equal to it when the tables are pair-duplicated). */
+static void rope_row_inverse(const double* g, const rot_src* r, int64_t s, int D, double* y) {
   for (int p = 0; p < D / 2; ++p) {
-    const double c = cos(phi[p]), s = -sin(phi[p]);
-    y[2 * p] = g[2 * p] * c - g[2 * p + 1] * s;
-    y[2 * p + 1] = g[2 * p] * s + g[2 * p + 1] * c;
+    if (r->phi) {
+      const double c = cos(r->phi[s * (D / 2) + p]), sn = -sin(r->phi[s * (D / 2) + p]);
+      y[2 * p] = g[2 * p] * c - g[2 * p + 1] * sn;
+      y[2 * p + 1] = g[2 * p] * sn + g[2 * p + 1] * c;
+    } else {
+      const double* c = r->cos + s * D + 2 * p;
+      const double* sn = r->sin + s * D + 2 * p;
+      y[2 * p] = g[2 * p] * c[0] + g[2 * p + 1] * sn[1];
+      y[2 * p + 1] = g[2 * p + 1] * c[1] - g[2 * p] * sn[0];
+    }
   }
 }
 
 /* Pre-attention transform of one head: out[s][:] = RoPE(RMSNorm(x[b,s,h,:])).
  * r_out[s] receives the RMSNorm reciprocal root of each row. */
 static void transform_head(const double* x, int S, int H, int D, int b, int h, const double* w, double eps,
-                           const double* phi, double* out, double* r_out) {
+                           const rot_src* rot, double* out, double* r_out) {
 #pragma omp parallel for schedule(static)
   for (int s = 0; s < S; ++s) {
     double tmp[1024];
     const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
     r_out[s] = rmsnorm_row(xr, w, D, eps, tmp);
-    rope_row(tmp, phi + (int64_t)s * (D / 2), D, out + (int64_t)s * D);
+    rope_row(tmp, rot, s, D, out + (int64_t)s * D);
   }
 }
 
@@ -112,10 +153,22 @@ static void transform_head(const double* x, int S, int H, int D, int b, int h, c
  * angle row phi [n_rows][D/2] per input row. */
 void oracle_qk_transform(const double* x, int64_t n_rows, int D, const double* w, double eps, const double* phi,
                          double* out) {
+  const rot_src rot = {phi, NULL, NULL};
   for (int64_t s = 0; s < n_rows; ++s) {
     double tmp[1024];
     rmsnorm_row(x + s * D, w, D, eps, tmp);
-    rope_row(tmp, phi + s * (D / 2), D, out + s * D);
+    rope_row(tmp, &rot, s, D, out + s * D);
+  }
+}
+
+/* As oracle_qk_transform with the pages' tables: cos, sin [n_rows][D]. */
+void oracle_qk_transform_tab(const double* x, int64_t n_rows, int D, const double* w, double eps,
+                             const double* cos_t, const double* sin_t, double* out) {
+  const rot_src rot = {NULL, cos_t, sin_t};
+  for (int64_t s = 0; s < n_rows; ++s) {
+    double tmp[1024];
+    rmsnorm_row(x + s * D, w, D, eps, tmp);
+    rope_row(tmp, &rot, s, D, out + s * D);
   }
 }
 
@@ -203,13 +256,13 @@ static void scatter_head(const double* m, int S, int H, int D, int b, int h, dou
 }
 
 /* Forward for the heads listed in `bh` (flattened b*H + h; NULL = all).
- * phi_q: [Bpq, Sq, D/2], phi_k: [Bpk, Skv, D/2] (Bp* in {1, B}).
+ * rot_q: Bpq x Sq rows, rot_k: Bpk x Skv rows (Bp* in {1, B}).
  * Writes o [B,Sq,H,D] and lse [B,H,Sq] at the listed heads only.
  * Returns 0, or -1 when a work buffer cannot be allocated. */
-int oracle_fwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
-               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
-               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
-               const int* bh, int n_bh, double* o, double* lse) {
+static int fwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+                    const double* wq, const double* wk, double eps, rot_src rot_q, int bpq, rot_src rot_k, int bpk,
+                    int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+                    const int* bh, int n_bh, double* o, double* lse) {
   double* qp = malloc(sizeof(double) * (size_t)Sq * D);
   double* kp = malloc(sizeof(double) * (size_t)Skv * D);
   double* vh = malloc(sizeof(double) * (size_t)Skv * D);
@@ -223,8 +276,9 @@ int oracle_fwd(int B, int Sq, int Skv, int H, int D, const double* q, const doub
   for (int t = 0; t < n; ++t) {
     const int idx = bh ? bh[t] : t;
     const int b = idx / H, h = idx % H;
-    transform_head(q, Sq, H, D, b, h, wq, eps, phi_q + (int64_t)(bpq > 1 ? b : 0) * Sq * (D / 2), qp, rq);
-    transform_head(k, Skv, H, D, b, h, wk, eps, phi_k + (int64_t)(bpk > 1 ? b : 0) * Skv * (D / 2), kp, rk);
+    const rot_src rq_b = rot_at(&rot_q, bpq, b, Sq, D), rk_b = rot_at(&rot_k, bpk, b, Skv, D);
+    transform_head(q, Sq, H, D, b, h, wq, eps, &rq_b, qp, rq);
+    transform_head(k, Skv, H, D, b, h, wk, eps, &rk_b, kp, rk);
     gather_head(v, Skv, H, D, b, h, vh);
     head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P,
                lse + ((int64_t)b * H + h) * Sq);
@@ -236,13 +290,34 @@ done:
   return rc;
 }
 
+/* Forward with angles: phi_q [Bpq, Sq, D/2], phi_k [Bpk, Skv, D/2]. */
+int oracle_fwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
+               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+               const int* bh, int n_bh, double* o, double* lse) {
+  const rot_src rq = {phi_q, NULL, NULL}, rk = {phi_k, NULL, NULL};
+  return fwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+                  scale, bh, n_bh, o, lse);
+}
+
+/* Forward with the pages' tables: cos_q, sin_q [Bpq, Sq, D]; cos_k, sin_k [Bpk, Skv, D]. */
+int oracle_fwd_tab(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+                   const double* wq, const double* wk, double eps, const double* cos_q, const double* sin_q, int bpq,
+                   const double* cos_k, const double* sin_k, int bpk, int mask_kind, const void* mask,
+                   const int64_t* mask_strides, int causal, double scale, const int* bh, int n_bh, double* o,
+                   double* lse) {
+  const rot_src rq = {NULL, cos_q, sin_q}, rk = {NULL, cos_k, sin_k};
+  return fwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+                  scale, bh, n_bh, o, lse);
+}
+
 /* RMSNorm + RoPE backward of one head. gp: gradient w.r.t. the rotated,
  * normalised rows [S][D]; x: raw input [B,S,H,D]. Writes dx into [B,S,H,D]
  * and adds sum_s (R^T gp) * x * r into dw.
  *   dy = R^T gp (inverse rotation), g = w * dy,
  *   dx = r g - (r^3 / D) x (x . g),   dw += dy * x * r. */
 static void transform_head_bwd(const double* gp, const double* x, int S, int H, int D, int b, int h,
-                               const double* w, const double* phi, const double* r, double* dx, double* dw) {
+                               const double* w, const rot_src* rot, const double* r, double* dx, double* dw) {
   double* dy_all = malloc(sizeof(double) * (size_t)S * D);
 #pragma omp parallel for schedule(static)
   for (int s = 0; s < S; ++s) {
@@ -250,7 +325,7 @@ static void transform_head_bwd(const double* gp, const double* x, int S, int H, 
     double* dy = dy_all + (int64_t)s * D;
     const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
     double* dxr = dx + (((int64_t)b * S + s) * H + h) * D;
-    rope_row_inverse(gp + (int64_t)s * D, phi + (int64_t)s * (D / 2), D, dy);
+    rope_row_inverse(gp + (int64_t)s * D, rot, s, D, dy);
     double xg = 0.0;
     for (int d = 0; d < D; ++d) {
       g[d] = w[d] * dy[d];
@@ -271,11 +346,11 @@ static void transform_head_bwd(const double* gp, const double* x, int S, int H, 
  *   dQ' = scale dS K', dK' = scale dS^T Q', then the RoPE/RMSNorm backward.
  * dwq/dwk [D] receive the sums over the listed heads only.
  * Returns 0, or -1 when a work buffer cannot be allocated. */
-int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
-               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
-               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
-               const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
-               double* dwk) {
+static int bwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+                    const double* wq, const double* wk, double eps, rot_src rot_q, int bpq, rot_src rot_k, int bpk,
+                    int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+                    const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
+                    double* dwk) {
   double* qp = malloc(sizeof(double) * (size_t)Sq * D);
   double* kp = malloc(sizeof(double) * (size_t)Skv * D);
   double* vh = malloc(sizeof(double) * (size_t)Skv * D);
@@ -295,10 +370,9 @@ int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const doub
   for (int t = 0; t < n; ++t) {
     const int idx = bh ? bh[t] : t;
     const int b = idx / H, h = idx % H;
-    const double* pq = phi_q + (int64_t)(bpq > 1 ? b : 0) * Sq * (D / 2);
-    const double* pk = phi_k + (int64_t)(bpk > 1 ? b : 0) * Skv * (D / 2);
-    transform_head(q, Sq, H, D, b, h, wq, eps, pq, qp, rq);
-    transform_head(k, Skv, H, D, b, h, wk, eps, pk, kp, rk);
+    const rot_src pq = rot_at(&rot_q, bpq, b, Sq, D), pk = rot_at(&rot_k, bpk, b, Skv, D);
+    transform_head(q, Sq, H, D, b, h, wq, eps, &pq, qp, rq);
+    transform_head(k, Skv, H, D, b, h, wk, eps, &pk, kp, rk);
     gather_head(v, Skv, H, D, b, h, vh);
     gather_head(dout, Sq, H, D, b, h, doh);
     head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P, lse);
@@ -325,11 +399,33 @@ int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const doub
     mat_atb(dS, Sq, Skv, qp, D, gk);
     for (int64_t e = 0; e < (int64_t)Sq * D; ++e) gq[e] *= scale;
     for (int64_t e = 0; e < (int64_t)Skv * D; ++e) gk[e] *= scale;
-    transform_head_bwd(gq, q, Sq, H, D, b, h, wq, pq, rq, dq, dwq);
-    transform_head_bwd(gk, k, Skv, H, D, b, h, wk, pk, rk, dk, dwk);
+    transform_head_bwd(gq, q, Sq, H, D, b, h, wq, &pq, rq, dq, dwq);
+    transform_head_bwd(gk, k, Skv, H, D, b, h, wk, &pk, rk, dk, dwk);
   }
 done:
   free(qp); free(kp); free(vh); free(doh); free(rq); free(rk); free(lse);
   free(P); free(dS); free(dvh); free(gq); free(gk);
   return rc;
+}
+
+/* Backward with angles: phi_q [Bpq, Sq, D/2], phi_k [Bpk, Skv, D/2]. */
+int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+               const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
+               int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
+               const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
+               double* dwk) {
+  const rot_src rq = {phi_q, NULL, NULL}, rk = {phi_k, NULL, NULL};
+  return bwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+                  scale, dout, bh, n_bh, dq, dk, dv, dwq, dwk);
+}
+
+/* Backward with the pages' tables: cos_q, sin_q [Bpq, Sq, D]; cos_k, sin_k [Bpk, Skv, D]. */
+int oracle_bwd_tab(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+                   const double* wq, const double* wk, double eps, const double* cos_q, const double* sin_q, int bpq,
+                   const double* cos_k, const double* sin_k, int bpk, int mask_kind, const void* mask,
+                   const int64_t* mask_strides, int causal, double scale, const double* dout, const int* bh, int n_bh,
+                   double* dq, double* dk, double* dv, double* dwq, double* dwk) {
+  const rot_src rq = {NULL, cos_q, sin_q}, rk = {NULL, cos_k, sin_k};
+  return bwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+                  scale, dout, bh, n_bh, dq, dk, dv, dwq, dwk);
 }

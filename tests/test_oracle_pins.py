@@ -355,3 +355,121 @@ def test_heads_subset_matches_full():
         np.testing.assert_array_equal(os_[b, :, h], o[b, :, h])
         np.testing.assert_array_equal(ls[b, h], lse[b, h])
     assert np.all(np.isnan(os_[0, :, 0]))
+
+
+# ------------------------------------------------- table form of the rotation
+# "Metal Flash Attention", section "Fused RoPE + SDPA": the entry point takes
+# pair-duplicated cos/sin tables of shape [S, D], [1, S, D] or [B, S, D].
+def _dup_tables(phi):
+    """Pair-duplicated (cos, sin) [..., S, D] of angles [..., S, D/2]."""
+    return np.repeat(np.cos(phi), 2, axis=-1), np.repeat(np.sin(phi), 2, axis=-1)
+
+
+@pytest.mark.parametrize("per_sample", [False, True])
+def test_table_form_equals_angle_form(per_sample):
+    """Tables holding cos/sin of the ids' angles give the ids' results."""
+    B, H, Sq, Skv = 2, 2, 7, 5
+    g = torch.Generator().manual_seed(21)
+    Bi = B if per_sample else 1
+    ids = torch.randint(0, 9, (Bi, Sq, 3), generator=g, dtype=torch.int32)
+    ids_k = torch.randint(0, 9, (Bi, Skv, 3), generator=g, dtype=torch.int32)
+    inp = wl.make_custom(B, H, 8, Sq, Skv, axes=(2, 2, 4), qk_dtype="fp32", v_dtype="fp32", seed=22, ids=ids,
+                         ids_k=ids_k)
+    cq, sq = _dup_tables(oracle.rope_angles(ids.numpy(), inp.axes, inp.theta))
+    ck, sk = _dup_tables(oracle.rope_angles(ids_k.numpy(), inp.axes, inp.theta))
+    if not per_sample:
+        cq, sq, ck, sk = cq[0], sq[0], ck[0], sk[0]  # the [S, D] form
+    args = (_np(inp.q), _np(inp.k), _np(inp.v), _np(inp.wq), _np(inp.wk), inp.eps)
+    o, lse = oracle.fwd(*args, ids.numpy(), inp.axes, inp.theta, ids_k=ids_k.numpy())
+    ot, lset = oracle.fwd_tab(*args, cq, sq, cos_k=ck, sin_k=sk)
+    np.testing.assert_allclose(ot, o, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lset, lse, rtol=1e-13, atol=1e-14)
+    ga = oracle.bwd(*args, ids.numpy(), inp.axes, inp.theta, _np(inp.do), ids_k=ids_k.numpy())
+    gt = oracle.bwd_tab(*args, cq, sq, _np(inp.do), cos_k=ck, sin_k=sk)
+    for a, t in zip(ga, gt):
+        np.testing.assert_allclose(t, a, rtol=1e-12, atol=1e-13)
+
+
+def _rand_tables(rng, shape):
+    """Tables that are neither pair-duplicated nor unit rotations, so that every
+    index of the elementwise form and of its transpose is exercised."""
+    return rng.uniform(-1.2, 1.2, shape), rng.uniform(-1.2, 1.2, shape)
+
+
+def test_table_form_matches_torch_elementwise_composition():
+    """Library special case: torch fp64 rms_norm, x * cos + rot(x) * sin with
+    rot(x) = (-x1, x0) per pair, SDPA and autograd."""
+    B, H, Sq, D = 2, 3, 11, 16
+    inp = wl.make_custom(B, H, D, Sq, Sq, axes=(8, 8), qk_dtype="fp32", v_dtype="fp32", seed=23)
+    rng = np.random.default_rng(24)
+    cq, sq = _rand_tables(rng, (B, Sq, D))
+    mask = rng.uniform(size=(B, 1, Sq, Sq)) < 0.7
+    mask[..., 0] = True
+    args = (_np(inp.q), _np(inp.k), _np(inp.v), _np(inp.wq), _np(inp.wk), inp.eps)
+    o, lse = oracle.fwd_tab(*args, cq, sq, mask=mask)
+    grads = oracle.bwd_tab(*args, cq, sq, _np(inp.do), mask=mask)
+
+    q, k, v, wq, wk = (t.double().requires_grad_() for t in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    c = torch.from_numpy(cq)[:, :, None, :]
+    s = torch.from_numpy(sq)[:, :, None, :]
+
+    def rot(x):
+        xp = x.reshape(*x.shape[:-1], D // 2, 2)
+        return torch.stack((-xp[..., 1], xp[..., 0]), dim=-1).reshape(x.shape)
+
+    def tr(x, w):
+        n = F.rms_norm(x, (D,), w, inp.eps)
+        return (n * c + rot(n) * s).transpose(1, 2)
+
+    am = torch.from_numpy(mask)
+    ro = F.scaled_dot_product_attention(tr(q, wq), tr(k, wk), v.transpose(1, 2), attn_mask=am).transpose(1, 2)
+    sc = tr(q, wq) @ tr(k, wk).transpose(-1, -2) / math.sqrt(D)
+    rl = torch.logsumexp(sc.masked_fill(~am, -math.inf), -1)
+    (ro * inp.do.double()).sum().backward()
+    np.testing.assert_allclose(o, ro.detach().numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(lse, rl.detach().numpy(), rtol=1e-10, atol=1e-12)
+    for got, t in zip(grads, (q, k, v, wq, wk)):
+        np.testing.assert_allclose(got, t.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_table_form_gradients_match_central_differences():
+    B, H, Sq, Skv, D = 1, 2, 5, 6, 8
+    inp = wl.make_custom(B, H, D, Sq, Skv, axes=(4, 4), qk_dtype="fp32", v_dtype="fp32", seed=25)
+    rng = np.random.default_rng(26)
+    cq, sq = _rand_tables(rng, (Sq, D))
+    ck, sk = _rand_tables(rng, (Skv, D))
+    q, k, v, wq, wk, dout = (_np(t).copy() for t in (inp.q, inp.k, inp.v, inp.wq, inp.wk, inp.do))
+
+    def loss():
+        o, _ = oracle.fwd_tab(q, k, v, wq, wk, inp.eps, cq, sq, cos_k=ck, sin_k=sk, causal=False)
+        return float(np.sum(o * dout))
+
+    grads = oracle.bwd_tab(q, k, v, wq, wk, inp.eps, cq, sq, dout, cos_k=ck, sin_k=sk)
+    h = 1e-6
+    for arr, grad in zip((q, k, v, wq, wk), grads):
+        fd = np.zeros_like(arr)
+        flat, fdf = arr.reshape(-1), fd.reshape(-1)
+        for i in range(flat.size):
+            x0 = flat[i]
+            flat[i] = x0 + h
+            lp = loss()
+            flat[i] = x0 - h
+            lm = loss()
+            flat[i] = x0
+            fdf[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-7)
+
+
+def test_table_form_transform_rows():
+    """qk_transform_tab on duplicated tables equals qk_transform on the angles,
+    and unit tables (cos 1, sin 0) leave the normalised rows unrotated."""
+    rng = np.random.default_rng(27)
+    x = rng.normal(size=(6, 8))
+    w = 1 + 0.1 * rng.normal(size=8)
+    phi = rng.uniform(-3, 3, (6, 4))
+    c, s = _dup_tables(phi)
+    np.testing.assert_allclose(oracle.qk_transform_tab(x, w, 1e-6, c, s), oracle.qk_transform(x, w, 1e-6, phi),
+                               rtol=1e-14, atol=1e-15)
+    r = 1 / np.sqrt(np.mean(x * x, -1, keepdims=True) + 1e-6)
+    np.testing.assert_allclose(oracle.qk_transform_tab(x, w, 1e-6, np.ones_like(x), np.zeros_like(x)), x * r * w,
+                               rtol=1e-14, atol=1e-15)
