@@ -22,10 +22,11 @@
  *    dispatch counters (get_dispatch_stats) become st_get_stats().
  *
  * Differences from that entry point: tensors are [B, S, H, D] (any strides on
- * B/S/H, unit stride on D) instead of BHSD; the rotation angles are built on the
- * device from per-token position ids, axis widths and theta instead of being
- * passed as cos/sin tables; the RMSNorm of q and k is fused in; the backward
- * also returns the two norm-weight gradients.
+ * B/S/H, unit stride on D) instead of BHSD (a BHSD tensor passes as its
+ * transpose(1, 2) view, without a copy); the rotation comes either from
+ * per-token position ids, axis widths and theta (built on the device) or from
+ * the entry point's own pair-duplicated cos/sin tables; the RMSNorm of q and k
+ * is fused in; the backward also returns the two norm-weight gradients.
  *
  * Per token t and head h (D = 128):
  *   r      = 1 / sqrt(mean_d x[d]^2 + eps)                 (x = q or k row)
@@ -91,18 +92,31 @@ typedef struct {
   int64_t stride[4];
 } st_tensor;
 
-/* Multi-axis rotary specification.
+/* Rotary specification: either position ids (the first five fields) or the
+ * cos/sin tables of "Metal Flash Attention", section "Fused RoPE + SDPA"
+ * (the last four fields); exactly one of `ids` and `cos` is set.
  * ids:   [B|1, S_q, n_axes], int32 or fp32, device; position id of each token
  *        on each axis (Flux: text (0,0,0), image (0,row,col)).
  * ids_k: the same for the keys ([B|1, S_kv, n_axes]); NULL means "same as ids"
  *        and requires S_q == S_kv.
- * axes_dim: width of each axis in head dims (even, summing to D); theta: base. */
+ * axes_dim: width of each axis in head dims (even, summing to D); theta: base.
+ * cos, sin: pair-duplicated tables (cos[..., 2j] == cos[..., 2j+1]) of shape
+ *        [S_q, D], [1, S_q, D] or [B, S_q, D]; fp32, bf16 or fp16 (the same for
+ *        both), any element strides, device. Entry 2j of each pair is read and
+ *        converted to fp32 (entry 2j+1 is not read: the tables promise it is
+ *        equal); n_axes, axes_dim and theta are then ignored.
+ * cos_k, sin_k: the same for the keys ([S_kv, D], [1, S_kv, D] or
+ *        [B, S_kv, D]); NULL means "same as cos/sin" and requires S_q == S_kv. */
 typedef struct {
   const st_tensor* ids;
   const st_tensor* ids_k;
-  int32_t n_axes; /* 1..8 */
+  int32_t n_axes; /* 1..8 (ids form) */
   int32_t axes_dim[8];
   double theta;
+  const st_tensor* cos;
+  const st_tensor* sin;
+  const st_tensor* cos_k;
+  const st_tensor* sin_k;
 } st_rope;
 
 /* Counters after the pages' dispatch statistics. Bumped only after a launch

@@ -9,6 +9,11 @@ Names follow the C-ABI: ``st_rope_attn_fwd``, ``st_rope_attn_bwd``,
 ``st_rope_attn_workspace_size``, ``st_get_stats``, ``st_reset_stats``,
 ``st_check_status``, ``st_last_error``. ``rope_attention`` wraps the pair in a
 ``torch.autograd.Function``.
+
+The rotation is given either by position ids (``ids``, ``axes_dim``,
+``theta``) or, in the form of the "Fused RoPE + SDPA" entry point, by
+pair-duplicated cos/sin tables: pass ``RopeTables(cos, sin)`` in place of
+``ids`` (``axes_dim`` and ``theta`` are then ignored).
 """
 from __future__ import annotations
 
@@ -37,7 +42,23 @@ class st_tensor(ctypes.Structure):
 
 class st_rope(ctypes.Structure):
     _fields_ = [("ids", ctypes.POINTER(st_tensor)), ("ids_k", ctypes.POINTER(st_tensor)),
-                ("n_axes", ctypes.c_int32), ("axes_dim", ctypes.c_int32 * 8), ("theta", ctypes.c_double)]
+                ("n_axes", ctypes.c_int32), ("axes_dim", ctypes.c_int32 * 8), ("theta", ctypes.c_double),
+                ("cos", ctypes.POINTER(st_tensor)), ("sin", ctypes.POINTER(st_tensor)),
+                ("cos_k", ctypes.POINTER(st_tensor)), ("sin_k", ctypes.POINTER(st_tensor))]
+
+
+class RopeTables:
+    """Pair-duplicated cos/sin tables ([S, D], [1, S, D] or [B, S, D]; fp32,
+    bf16 or fp16) for q, and optionally separate ones for k (required when
+    S_q != S_kv). Stands in for ``ids`` in every call of this module."""
+
+    def __init__(self, cos, sin, cos_k=None, sin_k=None):
+        if (cos is None) != (sin is None) or (cos_k is None) != (sin_k is None):
+            raise StError(ST_ERR_INVALID_ARG, "cos and sin come in pairs")
+        self.cos, self.sin, self.cos_k, self.sin_k = cos, sin, cos_k, sin_k
+
+    def tensors(self):
+        return [t for t in (self.cos, self.sin, self.cos_k, self.sin_k) if t is not None]
 
 
 class st_stats(ctypes.Structure):
@@ -127,6 +148,12 @@ def _check(status: int):
 
 def _rope(ids, axes_dim, theta, ids_k):
     r = st_rope()
+    if isinstance(ids, RopeTables):
+        if ids_k is not None:
+            raise StError(ST_ERR_INVALID_ARG, "ids_k cannot be combined with RopeTables (use cos_k/sin_k)")
+        r._keep = [_t(x) for x in (ids.cos, ids.sin, ids.cos_k, ids.sin_k)]  # alive with the rope object
+        r.cos, r.sin, r.cos_k, r.sin_k = (_p(x) for x in r._keep)
+        return r
     r._ids = _t(ids)            # keep the structs alive with the rope object
     r._ids_k = _t(ids_k)
     r.ids = _p(r._ids)
@@ -144,8 +171,9 @@ def _stream():
 
 def _require_cuda(*ts):
     for t in ts:
-        if t is not None and not t.is_cuda:
-            raise StError(ST_ERR_INVALID_ARG, "all tensors must live on a CUDA device")
+        for x in (t.tensors() if isinstance(t, RopeTables) else [t]):
+            if x is not None and not x.is_cuda:
+                raise StError(ST_ERR_INVALID_ARG, "all tensors must live on a CUDA device")
 
 
 def st_rope_attn_workspace_size(q, k, v, ids, axes_dim, theta, mask=None, causal=False, ids_k=None,
@@ -262,24 +290,40 @@ class RopeAttention(torch.autograd.Function):
     def forward(ctx, q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mask, causal, scale, ids_k):
         o, lse = st_rope_attn_fwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mask, causal, scale,
                                   ids_k)
-        ctx.save_for_backward(q, k, v, q_norm_w, k_norm_w, ids, mask, ids_k, o, lse)
-        ctx.cfg = (eps, tuple(axes_dim), theta, causal, scale)
+        tables = ids if isinstance(ids, RopeTables) else None  # no gradient flows to the tables
+        ctx.save_for_backward(q, k, v, q_norm_w, k_norm_w, None if tables else ids, mask, ids_k, o, lse)
+        ctx.cfg = (eps, tuple(axes_dim), theta, causal, scale, tables)
         return o
 
     @staticmethod
     def backward(ctx, d_o):
         q, k, v, q_norm_w, k_norm_w, ids, mask, ids_k, o, lse = ctx.saved_tensors
-        eps, axes_dim, theta, causal, scale = ctx.cfg
+        eps, axes_dim, theta, causal, scale, tables = ctx.cfg
+        if tables is not None:
+            ids = tables
         dq, dk, dv, dwq, dwk = st_rope_attn_bwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, o, lse,
                                                 d_o.contiguous(), mask, causal, scale, ids_k)
         return dq, dk, dv, dwq, dwk, None, None, None, None, None, None, None, None
 
 
-def rope_attention(q, k, v, q_norm_w, k_norm_w, ids, axes_dim, theta=1e4, eps=1e-6, mask=None, causal=False,
+def rope_attention(q, k, v, q_norm_w, k_norm_w, ids, axes_dim=(), theta=1e4, eps=1e-6, mask=None, causal=False,
                    scale=None, ids_k=None):
-    """O = SDPA(RoPE(RMSNorm_q(q)), RoPE(RMSNorm_k(k)), v, mask | causal, scale), differentiable."""
+    """O = SDPA(RoPE(RMSNorm_q(q)), RoPE(RMSNorm_k(k)), v, mask | causal, scale), differentiable.
+    ``ids`` may be a RopeTables (then ``axes_dim`` and ``theta`` are ignored)."""
     return RopeAttention.apply(q, k, v, q_norm_w, k_norm_w, eps, ids, tuple(axes_dim), theta, mask, causal, scale,
                                ids_k)
+
+
+def rope_attention_bhsd(query, key, value, rope_cos, rope_sin, q_norm_w, k_norm_w, attn_mask=None,
+                        is_causal=False, scale=None, eps=1e-6):
+    """The "Fused RoPE + SDPA" calling convention: BHSD tensors (strided views
+    such as transpose(1, 2) of a BSHD projection are consumed without copies)
+    and pair-duplicated cos/sin tables; here q and k are RMS-normalised first.
+    Returns O as a BHSD view."""
+    q, k, v = (t.transpose(1, 2) for t in (query, key, value))
+    o = rope_attention(q, k, v, q_norm_w, k_norm_w, RopeTables(rope_cos, rope_sin), eps=eps, mask=attn_mask,
+                       causal=is_causal, scale=scale)
+    return o.transpose(1, 2)
 
 
 def default_scale(D: int = 128) -> float:

@@ -167,9 +167,13 @@ st_status check_vec(const st_tensor* t, const char* name, int D) {
   return ST_OK;
 }
 
+// The rotation source of q or of k: position ids (t), or in the table form
+// the caller's cos (t) and sin tables.
 struct Ids {
   const st_tensor* t;
   int Bt, S;
+  const st_tensor* sin = nullptr;
+  bool table = false;
 };
 
 st_status check_ids(const st_tensor* t, const char* name, int B, int S, int n_axes, Ids* out) {
@@ -181,6 +185,33 @@ st_status check_ids(const st_tensor* t, const char* name, int B, int S, int n_ax
   if (t->dtype != ST_I32 && t->dtype != ST_F32) return fail(ST_ERR_DTYPE, "%s must be int32 or fp32", name);
   out->t = t;
   out->Bt = static_cast<int>(t->shape[0]);
+  out->S = S;
+  return ST_OK;
+}
+
+static_assert(kTabBF16 == ST_BF16 && kTabF16 == ST_F16 && kTabF32 == ST_F32, "table dtype codes");
+
+// The pages' table form: pair-duplicated cos/sin of shape [S, D], [1, S, D]
+// or [B, S, D], fp32, bf16 or fp16 (the same for both), any element strides.
+st_status check_tables(const st_tensor* c, const st_tensor* sn, const char* name, int B, int S, Ids* out) {
+  if (!c || !sn) return fail(ST_ERR_INVALID_ARG, "%s: cos and sin must both be given", name);
+  if (c->ndim != sn->ndim || (c->ndim != 2 && c->ndim != 3))
+    return fail(ST_ERR_SHAPE, "%s must both be [S, D] or [B|1, S, D]", name);
+  const int o = c->ndim - 2;
+  const int64_t bt = c->ndim == 3 ? c->shape[0] : 1;
+  for (const st_tensor* t : {c, sn}) {
+    if ((c->ndim == 3 && t->shape[0] != bt) || t->shape[o] != S || t->shape[o + 1] != kD)
+      return fail(ST_ERR_SHAPE, "%s must have shape [%d, %d] or [%d|1, %d, %d]", name, S, kD, B, S, kD);
+  }
+  if (!(bt == 1 || bt == B)) return fail(ST_ERR_SHAPE, "%s batch dim is %lld, expected 1 or %d", name, (long long)bt, B);
+  if (c->dtype != sn->dtype) return fail(ST_ERR_DTYPE, "%s must have the same dtype", name);
+  if (c->dtype != ST_F32 && c->dtype != ST_BF16 && c->dtype != ST_F16)
+    return fail(ST_ERR_DTYPE, "%s must be fp32, bf16 or fp16", name);
+  if ((!c->data || !sn->data) && bt * S > 0) return fail(ST_ERR_INVALID_ARG, "%s data is NULL", name);
+  out->t = c;
+  out->sin = sn;
+  out->table = true;
+  out->Bt = static_cast<int>(bt);
   out->S = S;
   return ST_OK;
 }
@@ -223,22 +254,35 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
   if ((st = check_bshd(k, "k", s.B, s.Skv, s.H, s.D, ST_BF16, ST_F32, &P->k)) != ST_OK) return st;
   if ((st = check_bshd(v, "v", s.B, s.Skv, s.H, s.D, ST_BF16, ST_BF16, &P->v)) != ST_OK) return st;
   if (!rope) return fail(ST_ERR_INVALID_ARG, "rope is NULL");
-  if (rope->n_axes < 1 || rope->n_axes > 8) return fail(ST_ERR_INVALID_ARG, "rope.n_axes must be 1..8");
-  int dsum = 0;
-  for (int a = 0; a < rope->n_axes; ++a) {
-    if (rope->axes_dim[a] <= 0 || (rope->axes_dim[a] & 1))
-      return fail(ST_ERR_INVALID_ARG, "rope.axes_dim[%d]=%d must be positive and even", a, rope->axes_dim[a]);
-    dsum += rope->axes_dim[a];
-  }
-  if (dsum != s.D) return fail(ST_ERR_INVALID_ARG, "rope axes sum to %d, expected D=%d", dsum, s.D);
-  if (!(rope->theta > 0.0) || !std::isfinite(rope->theta)) return fail(ST_ERR_INVALID_ARG, "rope.theta must be > 0");
-  if ((st = check_ids(rope->ids, "rope.ids", s.B, s.Sq, rope->n_axes, &P->ids_q)) != ST_OK) return st;
-  if (rope->ids_k) {
-    if ((st = check_ids(rope->ids_k, "rope.ids_k", s.B, s.Skv, rope->n_axes, &P->ids_k)) != ST_OK) return st;
-    P->separate_k_table = true;
+  if (rope->cos || rope->sin) {  // the pages' table form
+    if (rope->ids || rope->ids_k) return fail(ST_ERR_INVALID_ARG, "rope: give either ids or cos/sin tables, not both");
+    if ((st = check_tables(rope->cos, rope->sin, "rope.cos/sin", s.B, s.Sq, &P->ids_q)) != ST_OK) return st;
+    if (rope->cos_k || rope->sin_k) {
+      if ((st = check_tables(rope->cos_k, rope->sin_k, "rope.cos_k/sin_k", s.B, s.Skv, &P->ids_k)) != ST_OK) return st;
+      P->separate_k_table = true;
+    } else {
+      if (s.Sq != s.Skv) return fail(ST_ERR_INVALID_ARG, "rope.cos_k/sin_k are required when S_q != S_kv");
+      P->ids_k = P->ids_q;
+    }
   } else {
-    if (s.Sq != s.Skv) return fail(ST_ERR_INVALID_ARG, "rope.ids_k is required when S_q != S_kv");
-    P->ids_k = P->ids_q;
+    if (rope->cos_k || rope->sin_k) return fail(ST_ERR_INVALID_ARG, "rope.cos_k/sin_k need rope.cos/sin");
+    if (rope->n_axes < 1 || rope->n_axes > 8) return fail(ST_ERR_INVALID_ARG, "rope.n_axes must be 1..8");
+    int dsum = 0;
+    for (int a = 0; a < rope->n_axes; ++a) {
+      if (rope->axes_dim[a] <= 0 || (rope->axes_dim[a] & 1))
+        return fail(ST_ERR_INVALID_ARG, "rope.axes_dim[%d]=%d must be positive and even", a, rope->axes_dim[a]);
+      dsum += rope->axes_dim[a];
+    }
+    if (dsum != s.D) return fail(ST_ERR_INVALID_ARG, "rope axes sum to %d, expected D=%d", dsum, s.D);
+    if (!(rope->theta > 0.0) || !std::isfinite(rope->theta)) return fail(ST_ERR_INVALID_ARG, "rope.theta must be > 0");
+    if ((st = check_ids(rope->ids, "rope.ids", s.B, s.Sq, rope->n_axes, &P->ids_q)) != ST_OK) return st;
+    if (rope->ids_k) {
+      if ((st = check_ids(rope->ids_k, "rope.ids_k", s.B, s.Skv, rope->n_axes, &P->ids_k)) != ST_OK) return st;
+      P->separate_k_table = true;
+    } else {
+      if (s.Sq != s.Skv) return fail(ST_ERR_INVALID_ARG, "rope.ids_k is required when S_q != S_kv");
+      P->ids_k = P->ids_q;
+    }
   }
   if (mask && causal) return fail(ST_ERR_INVALID_ARG, "mask and causal cannot be combined");
   if (mask) {
@@ -348,13 +392,30 @@ void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float 
 
 void fill_table(const Ids& ids, const st_rope* rope, float2* out, __half2* out16, unsigned* ctrl, TableParams* t) {
   memset(t, 0, sizeof(*t));
+  t->Bt = ids.Bt;
+  t->S = ids.S;
+  t->out = out;
+  t->out16 = out16;
+  t->ctrl = ctrl;
+  if (ids.table) {
+    const st_tensor *c = ids.t, *sn = ids.sin;
+    const int o = c->ndim - 2;
+    t->cos = c->data;
+    t->sin = sn->data;
+    t->tab_dtype = c->dtype;
+    t->c_sb = (c->ndim == 3 && ids.Bt > 1) ? c->stride[0] : 0;
+    t->c_ss = c->stride[o];
+    t->c_sd = c->stride[o + 1];
+    t->s_sb = (sn->ndim == 3 && ids.Bt > 1) ? sn->stride[0] : 0;
+    t->s_ss = sn->stride[o];
+    t->s_sd = sn->stride[o + 1];
+    return;
+  }
   t->ids = ids.t->data;
   t->ids_f32 = ids.t->dtype == ST_F32;
   t->i_sb = ids.t->stride[0];
   t->i_ss = ids.t->stride[1];
   t->i_sa = ids.t->stride[2];
-  t->Bt = ids.Bt;
-  t->S = ids.S;
   int pair = 0;
   for (int a = 0; a < rope->n_axes; ++a) {
     const int da = rope->axes_dim[a];
@@ -363,9 +424,6 @@ void fill_table(const Ids& ids, const st_rope* rope, float2* out, __half2* out16
       t->axis_of[pair] = a;
     }
   }
-  t->out = out;
-  t->out16 = out16;
-  t->ctrl = ctrl;
 }
 
 st_status cuda_check(cudaError_t e, const char* what) {
@@ -419,7 +477,13 @@ st_status check_out(const st_tensor* t, const char* name, int B, int S, int H, i
   return check_bshd(t, name, B, S, H, kD, dtype, dtype, rt);
 }
 
+// The encoder is a driver call and needs a context current on the calling
+// thread. A thread that has made no runtime call yet (an autograd worker
+// thread running the backward) has none: cudaSetDevice binds the current
+// device's primary context to it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaSetDevice(dev);
   static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* f = nullptr;
     cudaDriverEntryPointQueryResult q;

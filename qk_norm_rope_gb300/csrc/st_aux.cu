@@ -13,8 +13,16 @@ namespace st {
 
 namespace {
 
+// Element e of a caller table as fp32.
+__device__ __forceinline__ float table_elem(const void* t, int dtype, int64_t e) {
+  if (dtype == kTabF32) return static_cast<const float*>(t)[e];
+  if (dtype == kTabBF16) return __bfloat162float(static_cast<const __nv_bfloat16*>(t)[e]);
+  return __half2float(static_cast<const __half*>(t)[e]);
+}
+
 // (cos, sin) of id * omega_p, the angle reduced to [-pi, pi] in fp64 before
-// the fp32 sincosf so that large ids keep full fp32 accuracy.
+// the fp32 sincosf so that large ids keep full fp32 accuracy; or, in the table
+// form, entry 2p of the caller's pair-duplicated cos/sin rows.
 __global__ void table_kernel(const __grid_constant__ TableParams p) {
   if (blockIdx.x == 0 && threadIdx.x < kCtrlWords && p.ctrl) p.ctrl[threadIdx.x] = 0u;
   const int64_t n = (int64_t)p.Bt * p.S * kPairs;
@@ -23,6 +31,13 @@ __global__ void table_kernel(const __grid_constant__ TableParams p) {
     const int64_t tok = e / kPairs;
     const int s = static_cast<int>(tok % p.S);
     const int bt = static_cast<int>(tok / p.S);
+    if (p.cos) {
+      const float cs = table_elem(p.cos, p.tab_dtype, bt * p.c_sb + (int64_t)s * p.c_ss + (int64_t)(2 * pr) * p.c_sd);
+      const float sn = table_elem(p.sin, p.tab_dtype, bt * p.s_sb + (int64_t)s * p.s_ss + (int64_t)(2 * pr) * p.s_sd);
+      p.out[e] = make_float2(cs, sn);
+      p.out16[e] = __floats2half2_rn(cs, sn);
+      continue;
+    }
     const int a = p.axis_of[pr];
     const int64_t off = bt * p.i_sb + (int64_t)s * p.i_ss + (int64_t)a * p.i_sa;
     const double id = p.ids_f32 ? static_cast<double>(static_cast<const float*>(p.ids)[off])

@@ -17,10 +17,19 @@ inline int dw_reduce_blocks(int n_q, int n_k) {
   return std::max(1, std::max(a, b));
 }
 
+// st_dtype codes of a caller table (the C header's ST_BF16, ST_F16, ST_F32).
+constexpr int kTabBF16 = 0, kTabF16 = 1, kTabF32 = 2;
+
 struct TableParams {
   const void* ids;
   int ids_f32;
   int64_t i_sb, i_ss, i_sa;  // element strides of ids [Bt, S, A]
+  // table form (cos non-null): the caller's pair-duplicated cos/sin [Bt, S, D]
+  const void* cos;
+  const void* sin;
+  int tab_dtype;             // st_dtype of cos and sin (fp32, bf16 or fp16)
+  int64_t c_sb, c_ss, c_sd;  // element strides of cos (0 on a broadcast batch)
+  int64_t s_sb, s_ss, s_sd;  // element strides of sin
   int Bt, S;
   double omega[kPairs];      // frequency of each pair
   int axis_of[kPairs];       // axis that owns each pair

@@ -67,10 +67,13 @@ class Call:
         self.causal = 0
         self.ws_bytes = 1 << 30
         self.ws = FAKE
+        self.tabs = None  # (cos, sin, cos_k, sin_k) for the table form
 
     def rope(self):
         r = api.st_rope()
-        r.ids = ctypes.pointer(self.ids)
+        if self.tabs is not None:
+            r.cos, r.sin, r.cos_k, r.sin_k = (None if t is None else ctypes.pointer(t) for t in self.tabs)
+        r.ids = ctypes.pointer(self.ids) if self.ids is not None else None
         r.ids_k = ctypes.pointer(self.ids_k) if self.ids_k is not None else None
         r.n_axes = len(self.axes)
         for a, d in enumerate(self.axes):
@@ -158,3 +161,54 @@ def test_workspace_errors():
     c.ws_bytes = need - 1
     expect(c, api.ST_ERR_WORKSPACE, "smaller")
     c = Call(); c.ws = 0; expect(c, api.ST_ERR_WORKSPACE, "NULL")
+
+
+def tables(c, S=256, B=None, dtype=api.ST_BF16, k=None):
+    """The table form on a Call: [S, D] tables (or [B, S, D]), optional key tables."""
+    shape = [S, 128] if B is None else [B, S, 128]
+    kt = (None, None) if k is None else (T(k, dtype), T(k, dtype))
+    c.ids = None
+    c.tabs = (T(shape, dtype), T(shape, dtype)) + kt
+    return c
+
+
+def test_table_form_validation():
+    """The pages' cos/sin table form: accepted shapes and dtypes, and every
+    rejected combination with its status (no launch)."""
+    for shape_b in (None, 1):
+        for dt in (api.ST_F32, api.ST_BF16, api.ST_F16):
+            c = tables(Call(), B=shape_b, dtype=dt)
+            assert c.ws_size(0) > 0, api.lib().st_last_error().decode()
+    assert tables(Call(B=2), B=2).ws_size(0) > tables(Call(B=2)).ws_size(0)  # per-sample tables take more room
+    c = tables(Call()); c.ids = T([1, 256, 3], api.ST_I32); expect(c, api.ST_ERR_INVALID_ARG, "not both")
+    c = tables(Call()); c.tabs = (c.tabs[0], None, None, None); expect(c, api.ST_ERR_INVALID_ARG, "both be given")
+    c = tables(Call(), S=255); expect(c, api.ST_ERR_SHAPE, "rope.cos/sin")
+    c = tables(Call()); c.tabs = (T([256, 64], api.ST_BF16), T([256, 64], api.ST_BF16), None, None)
+    expect(c, api.ST_ERR_SHAPE, "rope.cos/sin")
+    c = tables(Call(B=2), B=3); expect(c, api.ST_ERR_SHAPE, "batch dim")
+    c = tables(Call()); c.tabs = (T([256, 128], api.ST_BF16), T([1, 256, 128], api.ST_BF16), None, None)
+    expect(c, api.ST_ERR_SHAPE)
+    c = tables(Call(), dtype=api.ST_I32); expect(c, api.ST_ERR_DTYPE, "fp32, bf16 or fp16")
+    c = tables(Call()); c.tabs = (T([256, 128], api.ST_F32), T([256, 128], api.ST_BF16), None, None)
+    expect(c, api.ST_ERR_DTYPE, "same dtype")
+    c = tables(Call(S=256, Skv=200)); expect(c, api.ST_ERR_INVALID_ARG, "cos_k/sin_k are required")
+    c = tables(Call(S=256, Skv=200), k=[200, 128])
+    assert c.ws_size(0) > tables(Call()).ws_size(0) - 1  # separate key tables are planned
+    c = tables(Call(S=256, Skv=200), k=[256, 128]); expect(c, api.ST_ERR_SHAPE, "rope.cos_k/sin_k")
+    c = Call(); c.tabs = (None, None, T([256, 128]), T([256, 128])); expect(c, api.ST_ERR_INVALID_ARG, "need rope.cos")
+    c = tables(Call()); c.tabs = (T([256, 128], data=0), T([256, 128]), None, None)
+    expect(c, api.ST_ERR_INVALID_ARG, "NULL")
+
+
+def test_python_rope_tables_marshalling():
+    """RopeTables fills the table fields of the struct and nothing else."""
+    cpu = torch.zeros(4, 128, dtype=torch.bfloat16)
+    r = api._rope(api.RopeTables(cpu, cpu), (), 1e4, None)
+    assert bool(r.cos) and bool(r.sin) and not r.cos_k and not r.ids and r.n_axes == 0
+    assert r.cos.contents.shape[0] == 4 and r.cos.contents.dtype == api.ST_BF16
+    with pytest.raises(api.StError):
+        api._rope(api.RopeTables(cpu, cpu), (), 1e4, cpu)
+    with pytest.raises(api.StError):
+        api.RopeTables(cpu, None)
+    with pytest.raises(api.StError):
+        api._require_cuda(api.RopeTables(cpu, cpu))
