@@ -93,28 +93,6 @@ struct BwdParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// Loads the 128-element row at element offset `off` of a bf16 or fp32 tensor.
-__device__ __forceinline__ void load_row(const void* base, int64_t off, int is_f32, float (&x)[kD]) {
-  if (is_f32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off);
-#pragma unroll
-    for (int c = 0; c < kD / 4; ++c) {
-      const float4 v = __ldg(p + c);
-      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-    }
-  } else {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
-#pragma unroll
-    for (int c = 0; c < kD / 8; ++c) {
-      const uint4 v = __ldg(p + c);
-      x[8 * c + 0] = bf16_lo(v.x); x[8 * c + 1] = bf16_hi(v.x);
-      x[8 * c + 2] = bf16_lo(v.y); x[8 * c + 3] = bf16_hi(v.y);
-      x[8 * c + 4] = bf16_lo(v.z); x[8 * c + 5] = bf16_hi(v.z);
-      x[8 * c + 6] = bf16_lo(v.w); x[8 * c + 7] = bf16_hi(v.w);
-    }
-  }
-}
-
 // Reciprocal RMS of a row: 1 / sqrt(mean(x^2) + eps).
 __device__ __forceinline__ float row_rrms(const float (&x)[kD], float eps) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
@@ -126,59 +104,10 @@ __device__ __forceinline__ float row_rrms(const float (&x)[kD], float eps) {
   return rsqrtf(((a0 + a1) + (a2 + a3)) * (1.0f / kD) + eps);
 }
 
-// RMSNorm + interleaved-pair rotation of one row, rounded to bf16 and written
-// as row `row` of a K-major 128B-swizzled operand tile (two 64-column halves,
-// kHalfBytes apart). tab: the row's 64 (cos, sin) pairs.
-__device__ __forceinline__ void norm_rope_store(const float (&x)[kD], const float* __restrict__ w, float eps,
-                                                const float2* __restrict__ tab, uint8_t* tile, int row) {
-  const float r = row_rrms(x, eps);
-  const float4* t4 = reinterpret_cast<const float4*>(tab);
-  const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {  // 8 elements = 4 pairs = one 16-byte chunk
-    uint32_t packed[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float4 cs = __ldg(t4 + 2 * c + h);  // (cos, sin) of two pairs
-      const float4 ww = __ldg(w4 + 2 * c + h);
-      const int d = 8 * c + 4 * h;
-      const float n0 = x[d] * r * ww.x, n1 = x[d + 1] * r * ww.y;
-      const float n2 = x[d + 2] * r * ww.z, n3 = x[d + 3] * r * ww.w;
-      packed[2 * h] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
-      packed[2 * h + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
-    }
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  }
-}
-
-// Raw bf16 row copy into a 128B-swizzled tile (used for v and dO).
-__device__ __forceinline__ void copy_row_bf16(const void* base, int64_t off, uint8_t* tile, int row) {
-  const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off);
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c)
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7)) = __ldg(p + c);
-}
-
 __device__ __forceinline__ void zero_row(uint8_t* tile, int row, uint32_t half = kHalfBytes) {
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c)
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) = make_uint4(0, 0, 0, 0);
-}
-
-// Stores a 128-element fp32 row to a bf16 or fp32 destination.
-__device__ __forceinline__ void store_row(void* base, int64_t off, int is_f32, const float (&y)[kD]) {
-  if (is_f32) {
-    float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off);
-#pragma unroll
-    for (int c = 0; c < kD / 4; ++c) p[c] = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
-  } else {
-    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off);
-#pragma unroll
-    for (int c = 0; c < kD / 8; ++c)
-      p[c] = make_uint4(pack_bf16(y[8 * c], y[8 * c + 1]), pack_bf16(y[8 * c + 2], y[8 * c + 3]),
-                        pack_bf16(y[8 * c + 4], y[8 * c + 5]), pack_bf16(y[8 * c + 6], y[8 * c + 7]));
-  }
 }
 
 // Stores elements [32*q4, 32*q4 + 32) of a row to a bf16 or fp32 destination.
@@ -273,20 +202,6 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-// 2^x on the FMA and integer pipes, for finite x (clamped below at -126, where
-// the result is ~1e-38): x = n + f with n = round(x) taken from the low
-// mantissa bits of x + 1.5*2^23 (no conversion instruction), 2^f from a cubic
-// fitted on [-1/2, 1/2] (coefficients from csrc/derive_exp2_poly.py, maximum
-// relative error 7.6e-5), and n added to the exponent field. Used for a share
-// of the softmax exponentials so that the MUFU unit is not the bottleneck.
-__device__ __forceinline__ float ex2_fma(float x) {
-  x = fmaxf(x, -126.0f);
-  const float t = x + 12582912.0f;
-  const float f = x - (t - 12582912.0f);
-  const float p = fmaf(fmaf(fmaf(5.521666631e-02f, f, 2.426148951e-01f), f, 6.932526827e-01f), f, 9.999276400e-01f);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 __device__ __forceinline__ void record_timeout(const Common& c) {

@@ -303,65 +303,6 @@ struct HalfRowPrologue {
   }
 };
 
-// Quarter-row variant for tiles whose rows are shared inside a cluster: four
-// lanes (l & 7 equal) split one row, lane part `q` = l >> 3 owning head dims
-// [32q, 32q + 32) (half q >> 1 of the swizzled tile, 16-byte chunks
-// 4*(q & 1) .. +3). finish() writes the result in place and, when `remote` is
-// non-zero, to the same offsets of the peer CTA's tile (DSMEM); rows that do
-// not exist are sent as zeros so the peer never sees stale data.
-struct QuarterRowPrologue {
-  uint4 cs[4];  // (cos, sin) fp16 of this lane's 16 pairs
-  __device__ __forceinline__ void prefetch(const __half2* __restrict__ tab16_row, int q) {
-    const uint4* t16 = reinterpret_cast<const uint4*>(tab16_row) + 4 * q;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) cs[c] = ldg_nc_v4(t16 + c);
-  }
-  __device__ __forceinline__ void finish(uint8_t* tile, uint32_t remote, int row, int q, const float* w, float eps,
-                                         bool valid) const {
-    const uint32_t hoff = (q >> 1) * kHalfBytes;
-    const int c0 = (q & 1) * 4;
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + hoff + sw128_off(row, c0 + c));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
-        a0 = fmaf(lo, lo, a0);
-        a1 = fmaf(hi, hi, a1);
-      }
-    }
-    float ss = a0 + a1;
-    ss += __shfl_xor_sync(0xffffffffu, ss, 8);
-    ss += __shfl_xor_sync(0xffffffffu, ss, 16);
-    const float r = rsqrtf(ss * (1.0f / kD) + eps);
-    const float4* w4 = reinterpret_cast<const float4*>(w + 32 * q);
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint32_t off = hoff + sw128_off(row, c0 + c);
-      uint4 res = make_uint4(0u, 0u, 0u, 0u);
-      if (valid) {
-        const uint4 v = *reinterpret_cast<const uint4*>(tile + off);
-        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-        const uint32_t t[4] = {cs[c].x, cs[c].y, cs[c].z, cs[c].w};
-        const float4 wa = w4[2 * c], wb = w4[2 * c + 1];
-        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-        uint32_t out[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
-          const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
-          out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
-        }
-        res = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(tile + off) = res;
-      }
-      if (remote) st_cluster_v4(remote + off, res);
-    }
-  }
-};
-
 // Thread-per-row prologue reading the raw row (bf16 or fp32) from global
 // memory; used when q/k are fp32 (no in-place TMA staging) and for rows that
 // a TMA load does not cover. The raw row is read twice (sum of squares, then
