@@ -12,6 +12,12 @@ buffer before every timed step, outside the timed events.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
   python bench.py --impl reference ...   # the fp64 oracle on the host cores
+  python bench.py --impl eager ...       # eager torch: rms_norm + rotation + SDPA
+
+The eager arm is the comparison "Metal Flash Attention" (section "Fused RoPE +
+SDPA") reports for its fused entry point: the same step with the norm and the
+rotation as separate torch operations feeding torch's scaled_dot_product_attention
+(whichever backend torch picks), forward and backward through autograd.
 
 Under torchrun (N > 1) every rank runs its own replica of the workload (the
 path shards over independent (b, h) heads; there is no exchange step), the
@@ -308,6 +314,94 @@ def run_ours(args, rank, world, dev):
     return line
 
 
+def rope_tables_torch(ids, axes, theta):
+    """Pair-duplicated (cos, sin) [Bt, S, D] fp32 of the ids' angles, built with
+    torch operations as a model's rotary module would (the eager arm's own
+    tables; angle of pair j of axis a: id_a * theta^(-2j/d_a))."""
+    parts = []
+    for a, d_a in enumerate(axes):
+        j = torch.arange(d_a // 2, dtype=torch.float64, device=ids.device)
+        parts.append(ids[..., a:a + 1].double() * theta ** (-2.0 * j / d_a))
+    phi = torch.cat(parts, -1)
+    return (torch.cos(phi).float().repeat_interleave(2, -1), torch.sin(phi).float().repeat_interleave(2, -1))
+
+
+def eager_attention(q, k, v, wq, wk, eps, cos, sin, mask=None, causal=False):
+    """The eager composition on [B, S, H, D] tensors: rms_norm in fp32, the
+    rotation x * cos + rot(x) * sin (rot(x) = (-x1, x0) per interleaved pair),
+    a cast to v's dtype, then torch SDPA. cos, sin: [Bt, S, D] fp32."""
+    import torch.nn.functional as F
+    D = q.shape[-1]
+
+    def tr(x, w):
+        n = F.rms_norm(x.float(), (D,), w, eps)
+        p = n.unflatten(-1, (D // 2, 2))
+        r = torch.stack((-p[..., 1], p[..., 0]), -1).flatten(-2)
+        return (n * cos[:, :, None, :] + r * sin[:, :, None, :]).to(v.dtype).transpose(1, 2)
+
+    o = F.scaled_dot_product_attention(tr(q, wq), tr(k, wk), v.transpose(1, 2), attn_mask=mask, is_causal=causal)
+    return o.transpose(1, 2)
+
+
+def run_eager(args, rank, world, dev):
+    """The eager arm: the same step and timing rules as run_ours."""
+    inp = wl.make(args.workload)
+    B, Sq, H, D = inp.q.shape
+    f_fwd, f_bwd = nominal_flops(inp)
+    g = lambda t: None if t is None else t.to(dev)
+    q, k, v, do, wq, wk, ids = (g(t) for t in (inp.q, inp.k, inp.v, inp.do, inp.wq, inp.wk, inp.ids))
+    mask = g(inp.mask)
+    if inp.meta.get("mask_per_head"):
+        mask = torch.empty(B, H, Sq, inp.k.shape[1], dtype=torch.float32, device=dev)
+        for b in range(B):
+            for h in range(H):
+                mask[b, h].copy_(wl.additive_mask_head(args.workload, b, h))
+    cos, sin = rope_tables_torch(ids, inp.axes, inp.theta)   # built once, as a model caches them
+    leaves = [t.detach().requires_grad_() for t in (q, k, v, wq, wk)]
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        o = eager_attention(*leaves, inp.eps, cos, sin, mask=mask, causal=inp.causal)
+        torch.autograd.grad(o, leaves, do)
+
+    def timed(n):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            step()
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs)
+
+    for _ in range(args.warmup):
+        step()
+    vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    clocks = ClockSampler(vis[torch.cuda.current_device()] if vis else torch.cuda.current_device())
+    clocks.start()
+    time.sleep(0.2)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ms = timed(args.steps)
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms_max = reduce_max(ms, world, dev)
+    value = job_tflops(world, f_fwd + f_bwd, args.steps, ms_max)
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) inputs, norm weights 1+N(0,0.1))",
+        "config": {"workload": describe(args.workload, inp), "global_batch": B * world, "seq_len": Sq, "heads": H,
+                   "head_dim": D, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "flushed (256 MB write) before every timed step"},
+        "impl": "eager", "eager": "torch rms_norm + table rotation (fp32) + scaled_dot_product_attention, autograd",
+        "clocks": clk,
+    }
+
+
 def oracle_step_flops(Sq_rows, Skv, D, causal=False):
     f = 4.0 * Sq_rows * Skv * D
     if causal:
@@ -435,7 +529,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--impl", choices=["ours", "reference", "eager"], default="ours")
     ap.add_argument("--workload", default="flux1_1024", choices=sorted(wl.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -458,7 +552,7 @@ def main():
     dev = torch.device("cuda", local)
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=dev)
-    line = run_ours(args, rank, world, dev)
+    line = run_eager(args, rank, world, dev) if args.impl == "eager" else run_ours(args, rank, world, dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -10,6 +10,14 @@ w_q, w_k ~ 1 + N(0, 0.1) fp32; then the mask. Position ids are integers:
 Flux text tokens (0, 0, 0) followed by the image grid (0, row, col) in
 row-major order; the 4-axis long sequence uses (0, 0, 0, 0) / (0, 0, row, col);
 the causal workload uses a single axis with ids 0..S-1.
+
+The pages' own probe shapes ("Metal Flash Attention", sections "FLUX Sequence
+Lengths" and "Synthetic Memory Probe": B=1 H=24 D=128 with S=6144 at 1024px
+and S=24576 at 2048px; section "Fused RoPE + SDPA": the Z-Image DiT shape
+(1, 30, 4128, 128) in bf16) are included as well. The pages do not give their
+token composition; ids are inputs and do not change the cost, so the probe
+shapes take a rectangular image grid without text (64 x 96 and 128 x 192) and
+the DiT shape 32 text tokens plus a 64 x 64 grid, all with the Flux axes.
 """
 from __future__ import annotations
 
@@ -37,6 +45,14 @@ WORKLOADS = {
     # Flux2-style long sequence: B=1 H=48, 512 text + 128x128 image = 16896, 4 axes
     "flux2_long": dict(B=1, H=48, D=128, n_text=512, grid=128, axes=(32, 32, 32, 32), theta=2e3,
                        qk_dtype="bf16", v_dtype="bf16", mask="none", causal=False, seed=4),
+    # the pages' probe shapes: B=1 H=24 S=6144 (1024px) and S=24576 (2048px), no mask
+    "flux1_probe_6144": dict(B=1, H=24, D=128, n_text=0, grid=64, grid_w=96, axes=(16, 56, 56), theta=1e4,
+                             qk_dtype="bf16", v_dtype="bf16", mask="none", causal=False, seed=5),
+    "flux1_probe_24576": dict(B=1, H=24, D=128, n_text=0, grid=128, grid_w=192, axes=(16, 56, 56), theta=1e4,
+                              qk_dtype="bf16", v_dtype="bf16", mask="none", causal=False, seed=6),
+    # the Z-Image DiT shape (1, 30, 4128, 128) bf16: 32 text + 64x64 image
+    "zimage_dit": dict(B=1, H=30, D=128, n_text=32, grid=64, axes=(16, 56, 56), theta=1e4,
+                       qk_dtype="bf16", v_dtype="bf16", mask="none", causal=False, seed=7),
 }
 
 _DT = {"bf16": torch.bfloat16, "fp32": torch.float32, "fp16": torch.float16}
@@ -65,12 +81,14 @@ class Inputs:
         return tuple(self.q.shape)
 
 
-def flux_ids(n_text: int, grid: int, n_axes: int) -> torch.Tensor:
-    """[1, n_text + grid*grid, n_axes] int32: text (0,..,0), image (0,..,row,col)."""
-    S = n_text + grid * grid
+def flux_ids(n_text: int, grid: int, n_axes: int, grid_w: int | None = None) -> torch.Tensor:
+    """[1, n_text + grid*grid_w, n_axes] int32: text (0,..,0), then an image of
+    `grid` rows by `grid_w` (default `grid`) columns, (0,..,row,col) row-major."""
+    grid_w = grid if grid_w is None else grid_w
+    S = n_text + grid * grid_w
     ids = torch.zeros(1, S, n_axes, dtype=torch.int32)
-    rows = torch.arange(grid, dtype=torch.int32).repeat_interleave(grid)
-    cols = torch.arange(grid, dtype=torch.int32).repeat(grid)
+    rows = torch.arange(grid, dtype=torch.int32).repeat_interleave(grid_w)
+    cols = torch.arange(grid_w, dtype=torch.int32).repeat(grid)
     ids[0, n_text:, n_axes - 2] = rows
     ids[0, n_text:, n_axes - 1] = cols
     return ids
@@ -123,7 +141,7 @@ def make(name: str, with_mask: bool = True) -> Inputs:
     c = WORKLOADS[name]
     B, H, D = c["B"], c["H"], c["D"]
     if "grid" in c:
-        ids = flux_ids(c["n_text"], c["grid"], len(c["axes"]))
+        ids = flux_ids(c["n_text"], c["grid"], len(c["axes"]), c.get("grid_w"))
     else:
         ids = linear_ids(c["S"])
     S = ids.shape[1]
