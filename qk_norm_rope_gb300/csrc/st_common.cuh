@@ -74,8 +74,8 @@ struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
   CUtensorMap tmap_do;  // dO rows, 64-row boxes
-  CUtensorMap tmap_q;   // raw q rows, 32-row boxes / raw k rows, 128-row boxes (bf16 only; see qk_tma)
-  CUtensorMap tmap_k;
+  CUtensorMap tmap_q;   // raw q rows, 32-row boxes (bf16 only; see qk_tma)
+  CUtensorMap tmap_k;   // raw k rows, 128-row boxes (bf16 only)
   CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 64 rows (reduce target)
   int v_s_first, do_s_first, q_s_first, k_s_first;
   int qk_tma;
@@ -84,6 +84,7 @@ struct BwdParams {
   const float* lse;    // [B, H, Sq]
   const float* delta;  // [B, H, Sq]
   float* dq_acc;       // [B, Sq, H, D] fp32, zeroed: scale * dS K' (gradient of the rotated, normed q)
+                       // (TMA reduce target through tmap_dq)
   float* dk_acc;       // [B, Skv, H, D] fp32: scale * dS^T Q' (gradient of the rotated, normed k)
   void* dv;
   int64_t dv_sb, dv_ss, dv_sh;
@@ -92,17 +93,6 @@ struct BwdParams {
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Reciprocal RMS of a row: 1 / sqrt(mean(x^2) + eps).
-__device__ __forceinline__ float row_rrms(const float (&x)[kD], float eps) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int d = 0; d < kD; d += 4) {
-    a0 = fmaf(x[d], x[d], a0); a1 = fmaf(x[d + 1], x[d + 1], a1);
-    a2 = fmaf(x[d + 2], x[d + 2], a2); a3 = fmaf(x[d + 3], x[d + 3], a3);
-  }
-  return rsqrtf(((a0 + a1) + (a2 + a3)) * (1.0f / kD) + eps);
-}
 
 __device__ __forceinline__ void zero_row(uint8_t* tile, int row, uint32_t half = kHalfBytes) {
 #pragma unroll
