@@ -58,7 +58,7 @@ def _load():
             lib.oracle_rope_angles.restype = None
             lib.oracle_qk_transform.argtypes = [dp, c_i64, c_int, dp, c_dbl, dp, dp]
             lib.oracle_qk_transform.restype = None
-            common = [c_int, c_int, c_int, c_int, c_int, dp, dp, dp, dp, dp, c_dbl, dp, c_int, dp, c_int,
+            common = [c_int, c_int, c_int, c_int, c_int, c_int, dp, dp, dp, dp, dp, c_dbl, dp, c_int, dp, c_int,
                       c_int, vp, i64p, c_int, c_dbl]
             lib.oracle_fwd.argtypes = common + [ip, c_int, dp, dp]
             lib.oracle_fwd.restype = c_int
@@ -66,7 +66,7 @@ def _load():
             lib.oracle_bwd.restype = c_int
             lib.oracle_qk_transform_tab.argtypes = [dp, c_i64, c_int, dp, c_dbl, dp, dp, dp]
             lib.oracle_qk_transform_tab.restype = None
-            common_tab = [c_int, c_int, c_int, c_int, c_int, dp, dp, dp, dp, dp, c_dbl, dp, dp, c_int, dp, dp,
+            common_tab = [c_int, c_int, c_int, c_int, c_int, c_int, dp, dp, dp, dp, dp, c_dbl, dp, dp, c_int, dp, dp,
                           c_int, c_int, vp, i64p, c_int, c_dbl]
             lib.oracle_fwd_tab.argtypes = common_tab + [ip, c_int, dp, dp]
             lib.oracle_fwd_tab.restype = c_int
@@ -138,15 +138,15 @@ def _mask_args(mask, B, H, Sq, Skv):
 def _prep(q, k, v, wq, wk, ids_q, ids_k, axes_dim, theta):
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, H, D = q.shape
-    Skv = k.shape[1]
-    assert k.shape == (B, Skv, H, D) and v.shape == (B, Skv, H, D)
+    Skv, Hkv = k.shape[1], k.shape[2]
+    assert k.shape == (B, Skv, Hkv, D) and v.shape == k.shape and H % Hkv == 0
     assert sum(axes_dim) == D
     phi_q = rope_angles(ids_q, axes_dim, theta)
     phi_k = rope_angles(ids_q if ids_k is None else ids_k, axes_dim, theta)
     assert phi_q.shape[-2] == Sq and phi_k.shape[-2] == Skv
     phi_q = phi_q.reshape(-1, Sq, D // 2)
     phi_k = phi_k.reshape(-1, Skv, D // 2)
-    return q, k, v, _f64(wq), _f64(wk), phi_q, phi_k, B, Sq, Skv, H, D
+    return q, k, v, _f64(wq), _f64(wk), phi_q, phi_k, B, Sq, Skv, H, Hkv, D
 
 
 def _heads_arg(heads, B, H):
@@ -158,18 +158,19 @@ def _heads_arg(heads, B, H):
 
 def fwd(q, k, v, wq, wk, eps, ids_q, axes_dim, theta, mask=None, causal=False, scale=None, ids_k=None,
         heads=None):
-    """O [B,Sq,H,D] and LSE [B,H,Sq] (natural log), fp64.
+    """O [B,Sq,H,D] and LSE [B,H,Sq] (natural log), fp64. k, v may have fewer heads
+    (H_kv dividing H): query head h then uses K/V head h // (H // H_kv).
 
     heads: optional list of (b, h) to compute; other entries are left as NaN.
     """
-    q, k, v, wq, wk, phi_q, phi_k, B, Sq, Skv, H, D = _prep(q, k, v, wq, wk, ids_q, ids_k, axes_dim, theta)
+    q, k, v, wq, wk, phi_q, phi_k, B, Sq, Skv, H, Hkv, D = _prep(q, k, v, wq, wk, ids_q, ids_k, axes_dim, theta)
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     kind, marr, mst = _mask_args(mask, B, H, Sq, Skv)
     o = np.full((B, Sq, H, D), np.nan)
     lse = np.full((B, H, Sq), np.nan)
     hp, nh = _heads_arg(heads, B, H)
-    rc = _load().oracle_fwd(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(phi_q),
+    rc = _load().oracle_fwd(B, Sq, Skv, H, Hkv, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(phi_q),
                             phi_q.shape[0], _dp(phi_k), phi_k.shape[0], kind,
                             None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale), hp, nh,
                             _dp(o), _dp(lse))
@@ -180,8 +181,9 @@ def fwd(q, k, v, wq, wk, eps, ids_q, axes_dim, theta, mask=None, causal=False, s
 
 def bwd(q, k, v, wq, wk, eps, ids_q, axes_dim, theta, dout, mask=None, causal=False, scale=None, ids_k=None,
         heads=None):
-    """dq, dk, dv [.., H, D] and dwq, dwk [D], fp64 (dw summed over `heads`)."""
-    q, k, v, wq, wk, phi_q, phi_k, B, Sq, Skv, H, D = _prep(q, k, v, wq, wk, ids_q, ids_k, axes_dim, theta)
+    """dq [.., H, D], dk, dv [.., H_kv, D] and dwq, dwk [D], fp64 (dw summed over
+    `heads`; dk, dv of a K/V head summed over the listed query heads of its group)."""
+    q, k, v, wq, wk, phi_q, phi_k, B, Sq, Skv, H, Hkv, D = _prep(q, k, v, wq, wk, ids_q, ids_k, axes_dim, theta)
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     dout = _f64(dout)
@@ -193,7 +195,7 @@ def bwd(q, k, v, wq, wk, eps, ids_q, axes_dim, theta, dout, mask=None, causal=Fa
     dwq = np.zeros(D)
     dwk = np.zeros(D)
     hp, nh = _heads_arg(heads, B, H)
-    rc = _load().oracle_bwd(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(phi_q),
+    rc = _load().oracle_bwd(B, Sq, Skv, H, Hkv, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(phi_q),
                             phi_q.shape[0], _dp(phi_k), phi_k.shape[0], kind,
                             None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale),
                             _dp(dout), hp, nh, _dp(dq), _dp(dk), _dp(dv), _dp(dwq), _dp(dwk))
@@ -234,28 +236,28 @@ def qk_transform_tab(x, w, eps: float, cos_t, sin_t) -> np.ndarray:
 def _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k):
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Sq, H, D = q.shape
-    Skv = k.shape[1]
-    assert k.shape == (B, Skv, H, D) and v.shape == (B, Skv, H, D)
+    Skv, Hkv = k.shape[1], k.shape[2]
+    assert k.shape == (B, Skv, Hkv, D) and v.shape == k.shape and H % Hkv == 0
     if cos_k is None:
         assert Sq == Skv, "cos_k/sin_k are required when S_q != S_kv"
         cos_k, sin_k = cos_q, sin_q
     cq, sq = _tables(cos_q, sin_q, Sq, D)
     ck, sk = _tables(cos_k, sin_k, Skv, D)
     assert cq.shape[0] in (1, B) and ck.shape[0] in (1, B)
-    return q, k, v, _f64(wq), _f64(wk), cq, sq, ck, sk, B, Sq, Skv, H, D
+    return q, k, v, _f64(wq), _f64(wk), cq, sq, ck, sk, B, Sq, Skv, H, Hkv, D
 
 
 def fwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, mask=None, causal=False, scale=None, cos_k=None, sin_k=None,
             heads=None):
     """As fwd, with the rotation given by cos/sin tables instead of ids."""
-    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
+    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, Hkv, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     kind, marr, mst = _mask_args(mask, B, H, Sq, Skv)
     o = np.full((B, Sq, H, D), np.nan)
     lse = np.full((B, H, Sq), np.nan)
     hp, nh = _heads_arg(heads, B, H)
-    rc = _load().oracle_fwd_tab(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
+    rc = _load().oracle_fwd_tab(B, Sq, Skv, H, Hkv, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
                                 _dp(sq), cq.shape[0], _dp(ck), _dp(sk), ck.shape[0], kind,
                                 None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale), hp,
                                 nh, _dp(o), _dp(lse))
@@ -267,7 +269,7 @@ def fwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, mask=None, causal=False, scale=N
 def bwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, dout, mask=None, causal=False, scale=None, cos_k=None, sin_k=None,
             heads=None):
     """As bwd, with the rotation given by cos/sin tables instead of ids."""
-    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
+    q, k, v, wq, wk, cq, sq, ck, sk, B, Sq, Skv, H, Hkv, D = _prep_tab(q, k, v, wq, wk, cos_q, sin_q, cos_k, sin_k)
     if scale is None:
         scale = 1.0 / np.sqrt(D)
     dout = _f64(dout)
@@ -279,7 +281,7 @@ def bwd_tab(q, k, v, wq, wk, eps, cos_q, sin_q, dout, mask=None, causal=False, s
     dwq = np.zeros(D)
     dwk = np.zeros(D)
     hp, nh = _heads_arg(heads, B, H)
-    rc = _load().oracle_bwd_tab(B, Sq, Skv, H, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
+    rc = _load().oracle_bwd_tab(B, Sq, Skv, H, Hkv, D, _dp(q), _dp(k), _dp(v), _dp(wq), _dp(wk), float(eps), _dp(cq),
                                 _dp(sq), cq.shape[0], _dp(ck), _dp(sk), ck.shape[0], kind,
                                 None if marr is None else marr.ctypes.data, mst, int(bool(causal)), float(scale),
                                 _dp(dout), hp, nh, _dp(dq), _dp(dk), _dp(dv), _dp(dwq), _dp(dwk))

@@ -24,8 +24,11 @@
  * Readings where the pages are silent (frequency formula, rotation sign,
  * fully-masked rows, causal alignment) are stated beside the code below.
  *
- * Layouts: q, dq, o, do are [B, S_q, H, D]; k, v, dk, dv are [B, S_kv, H, D];
- * all contiguous fp64. The rotation comes either from angles phi [Bp, S, D/2]
+ * Layouts: q, dq, o, do are [B, S_q, H, D]; k, v, dk, dv are [B, S_kv, H_kv, D]
+ * with H a multiple of H_kv; all contiguous fp64. Grouped K/V heads (same page,
+ * section "Fused RoPE + SDPA": GQA inputs are rotated at the K/V head count and
+ * expanded afterwards): query head h attends with K/V head h / (H / H_kv), and
+ * dk, dv of a K/V head sum the gradients of its group of query heads. The rotation comes either from angles phi [Bp, S, D/2]
  * or from the pages' cos/sin tables [Bp, S, D] (same page, section "Fused
  * RoPE + SDPA": pair-duplicated tables of shape [S, D], [1, S, D] or
  * [B, S, D]), with Bp in {1, B}.
@@ -254,12 +257,19 @@ static void scatter_head(const double* m, int S, int H, int D, int b, int h, dou
   for (int s = 0; s < S; ++s)
     memcpy(x + (((int64_t)b * S + s) * H + h) * D, m + (int64_t)s * D, sizeof(double) * D);
 }
+static void add_head(const double* m, int S, int H, int D, int b, int h, double* x) {
+  for (int s = 0; s < S; ++s)
+    for (int d = 0; d < D; ++d) x[(((int64_t)b * S + s) * H + h) * D + d] += m[(int64_t)s * D + d];
+}
+static void zero_head(int S, int H, int D, int b, int h, double* x) {
+  for (int s = 0; s < S; ++s) memset(x + (((int64_t)b * S + s) * H + h) * D, 0, sizeof(double) * D);
+}
 
 /* Forward for the heads listed in `bh` (flattened b*H + h; NULL = all).
  * rot_q: Bpq x Sq rows, rot_k: Bpk x Skv rows (Bp* in {1, B}).
  * Writes o [B,Sq,H,D] and lse [B,H,Sq] at the listed heads only.
  * Returns 0, or -1 when a work buffer cannot be allocated. */
-static int fwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+static int fwd_impl(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                     const double* wq, const double* wk, double eps, rot_src rot_q, int bpq, rot_src rot_k, int bpk,
                     int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
                     const int* bh, int n_bh, double* o, double* lse) {
@@ -276,10 +286,11 @@ static int fwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const
   for (int t = 0; t < n; ++t) {
     const int idx = bh ? bh[t] : t;
     const int b = idx / H, h = idx % H;
+    const int hk = h / (H / Hkv);  /* the K/V head of query head h */
     const rot_src rq_b = rot_at(&rot_q, bpq, b, Sq, D), rk_b = rot_at(&rot_k, bpk, b, Skv, D);
     transform_head(q, Sq, H, D, b, h, wq, eps, &rq_b, qp, rq);
-    transform_head(k, Skv, H, D, b, h, wk, eps, &rk_b, kp, rk);
-    gather_head(v, Skv, H, D, b, h, vh);
+    transform_head(k, Skv, Hkv, D, b, hk, wk, eps, &rk_b, kp, rk);
+    gather_head(v, Skv, Hkv, D, b, hk, vh);
     head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P,
                lse + ((int64_t)b * H + h) * Sq);
     mat_ab(P, Sq, Skv, vh, D, oh);
@@ -291,33 +302,35 @@ done:
 }
 
 /* Forward with angles: phi_q [Bpq, Sq, D/2], phi_k [Bpk, Skv, D/2]. */
-int oracle_fwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+int oracle_fwd(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
                int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
                const int* bh, int n_bh, double* o, double* lse) {
   const rot_src rq = {phi_q, NULL, NULL}, rk = {phi_k, NULL, NULL};
-  return fwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+  return fwd_impl(B, Sq, Skv, H, Hkv, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
                   scale, bh, n_bh, o, lse);
 }
 
 /* Forward with the pages' tables: cos_q, sin_q [Bpq, Sq, D]; cos_k, sin_k [Bpk, Skv, D]. */
-int oracle_fwd_tab(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+int oracle_fwd_tab(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                    const double* wq, const double* wk, double eps, const double* cos_q, const double* sin_q, int bpq,
                    const double* cos_k, const double* sin_k, int bpk, int mask_kind, const void* mask,
                    const int64_t* mask_strides, int causal, double scale, const int* bh, int n_bh, double* o,
                    double* lse) {
   const rot_src rq = {NULL, cos_q, sin_q}, rk = {NULL, cos_k, sin_k};
-  return fwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+  return fwd_impl(B, Sq, Skv, H, Hkv, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
                   scale, bh, n_bh, o, lse);
 }
 
 /* RMSNorm + RoPE backward of one head. gp: gradient w.r.t. the rotated,
- * normalised rows [S][D]; x: raw input [B,S,H,D]. Writes dx into [B,S,H,D]
- * and adds sum_s (R^T gp) * x * r into dw.
+ * normalised rows [S][D]; x: raw input [B,S,H,D]. Adds dx into [B,S,H,D]
+ * and sum_s (R^T gp) * x * r into dw.
  *   dy = R^T gp (inverse rotation), g = w * dy,
  *   dx = r g - (r^3 / D) x (x . g),   dw += dy * x * r. */
 static void transform_head_bwd(const double* gp, const double* x, int S, int H, int D, int b, int h,
                                const double* w, const rot_src* rot, const double* r, double* dx, double* dw) {
+  /* dx is added to (the rows start at zero), so that the query heads of a
+   * K/V group sum into their K/V head's rows */
   double* dy_all = malloc(sizeof(double) * (size_t)S * D);
 #pragma omp parallel for schedule(static)
   for (int s = 0; s < S; ++s) {
@@ -332,7 +345,7 @@ static void transform_head_bwd(const double* gp, const double* x, int S, int H, 
       xg += xr[d] * g[d];
     }
     const double rs = r[s];
-    for (int d = 0; d < D; ++d) dxr[d] = rs * g[d] - (rs * rs * rs / (double)D) * xr[d] * xg;
+    for (int d = 0; d < D; ++d) dxr[d] += rs * g[d] - (rs * rs * rs / (double)D) * xr[d] * xg;
   }
   for (int s = 0; s < S; ++s) {
     const double* xr = x + (((int64_t)b * S + s) * H + h) * D;
@@ -344,9 +357,10 @@ static void transform_head_bwd(const double* gp, const double* x, int S, int H, 
 /* Backward for the listed heads, given dO [B,Sq,H,D]:
  *   dV = P^T dO, dP = dO V^T, Delta_i = sum_j P_ij dP_ij, dS = P (dP - Delta),
  *   dQ' = scale dS K', dK' = scale dS^T Q', then the RoPE/RMSNorm backward.
- * dwq/dwk [D] receive the sums over the listed heads only.
+ * dwq/dwk [D] receive the sums over the listed heads only, and dk/dv of a K/V
+ * head the sums over the listed query heads of its group.
  * Returns 0, or -1 when a work buffer cannot be allocated. */
-static int bwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+static int bwd_impl(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                     const double* wq, const double* wk, double eps, rot_src rot_q, int bpq, rot_src rot_k, int bpk,
                     int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
                     const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
@@ -367,18 +381,26 @@ static int bwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const
   if (!qp || !kp || !vh || !doh || !rq || !rk || !lse || !P || !dS || !dvh || !gq || !gk) { rc = -1; goto done; }
   for (int d = 0; d < D; ++d) { dwq[d] = 0.0; dwk[d] = 0.0; }
   const int n = bh ? n_bh : B * H;
+  for (int t = 0; t < n; ++t) { /* the gradient rows of the listed heads start at zero */
+    const int idx = bh ? bh[t] : t;
+    const int b = idx / H, h = idx % H, hk = h / (H / Hkv);
+    zero_head(Sq, H, D, b, h, dq);
+    zero_head(Skv, Hkv, D, b, hk, dk);
+    zero_head(Skv, Hkv, D, b, hk, dv);
+  }
   for (int t = 0; t < n; ++t) {
     const int idx = bh ? bh[t] : t;
     const int b = idx / H, h = idx % H;
+    const int hk = h / (H / Hkv);  /* the K/V head of query head h */
     const rot_src pq = rot_at(&rot_q, bpq, b, Sq, D), pk = rot_at(&rot_k, bpk, b, Skv, D);
     transform_head(q, Sq, H, D, b, h, wq, eps, &pq, qp, rq);
-    transform_head(k, Skv, H, D, b, h, wk, eps, &pk, kp, rk);
-    gather_head(v, Skv, H, D, b, h, vh);
+    transform_head(k, Skv, Hkv, D, b, hk, wk, eps, &pk, kp, rk);
+    gather_head(v, Skv, Hkv, D, b, hk, vh);
     gather_head(dout, Sq, H, D, b, h, doh);
     head_probs(qp, kp, Sq, Skv, D, scale, mask_kind, mask, mask_strides, causal, b, h, P, lse);
     /* dV = P^T dO */
     mat_atb(P, Sq, Skv, doh, D, dvh);
-    scatter_head(dvh, Skv, H, D, b, h, dv);
+    add_head(dvh, Skv, Hkv, D, b, hk, dv);
     /* dP = dO V^T, Delta, dS = P (dP - Delta) */
 #pragma omp parallel for schedule(static)
     for (int i = 0; i < Sq; ++i) {
@@ -400,7 +422,7 @@ static int bwd_impl(int B, int Sq, int Skv, int H, int D, const double* q, const
     for (int64_t e = 0; e < (int64_t)Sq * D; ++e) gq[e] *= scale;
     for (int64_t e = 0; e < (int64_t)Skv * D; ++e) gk[e] *= scale;
     transform_head_bwd(gq, q, Sq, H, D, b, h, wq, &pq, rq, dq, dwq);
-    transform_head_bwd(gk, k, Skv, H, D, b, h, wk, &pk, rk, dk, dwk);
+    transform_head_bwd(gk, k, Skv, Hkv, D, b, hk, wk, &pk, rk, dk, dwk);
   }
 done:
   free(qp); free(kp); free(vh); free(doh); free(rq); free(rk); free(lse);
@@ -409,23 +431,23 @@ done:
 }
 
 /* Backward with angles: phi_q [Bpq, Sq, D/2], phi_k [Bpk, Skv, D/2]. */
-int oracle_bwd(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+int oracle_bwd(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                const double* wq, const double* wk, double eps, const double* phi_q, int bpq, const double* phi_k,
                int bpk, int mask_kind, const void* mask, const int64_t* mask_strides, int causal, double scale,
                const double* dout, const int* bh, int n_bh, double* dq, double* dk, double* dv, double* dwq,
                double* dwk) {
   const rot_src rq = {phi_q, NULL, NULL}, rk = {phi_k, NULL, NULL};
-  return bwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+  return bwd_impl(B, Sq, Skv, H, Hkv, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
                   scale, dout, bh, n_bh, dq, dk, dv, dwq, dwk);
 }
 
 /* Backward with the pages' tables: cos_q, sin_q [Bpq, Sq, D]; cos_k, sin_k [Bpk, Skv, D]. */
-int oracle_bwd_tab(int B, int Sq, int Skv, int H, int D, const double* q, const double* k, const double* v,
+int oracle_bwd_tab(int B, int Sq, int Skv, int H, int Hkv, int D, const double* q, const double* k, const double* v,
                    const double* wq, const double* wk, double eps, const double* cos_q, const double* sin_q, int bpq,
                    const double* cos_k, const double* sin_k, int bpk, int mask_kind, const void* mask,
                    const int64_t* mask_strides, int causal, double scale, const double* dout, const int* bh, int n_bh,
                    double* dq, double* dk, double* dv, double* dwq, double* dwk) {
   const rot_src rq = {NULL, cos_q, sin_q}, rk = {NULL, cos_k, sin_k};
-  return bwd_impl(B, Sq, Skv, H, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
+  return bwd_impl(B, Sq, Skv, H, Hkv, D, q, k, v, wq, wk, eps, rq, bpq, rk, bpk, mask_kind, mask, mask_strides, causal,
                   scale, dout, bh, n_bh, dq, dk, dv, dwq, dwk);
 }

@@ -473,3 +473,109 @@ def test_table_form_transform_rows():
     r = 1 / np.sqrt(np.mean(x * x, -1, keepdims=True) + 1e-6)
     np.testing.assert_allclose(oracle.qk_transform_tab(x, w, 1e-6, np.ones_like(x), np.zeros_like(x)), x * r * w,
                                rtol=1e-14, atol=1e-15)
+
+
+# ------------------------------------------------------ grouped K/V heads (GQA)
+# "Metal Flash Attention", section "Fused RoPE + SDPA": GQA inputs (fewer K/V
+# heads) are rotated at the K/V head count and expanded afterwards.
+def _gqa(B=2, H=4, Hkv=2, Sq=7, Skv=6, D=8, axes=(2, 2, 4), seed=81):
+    inp = _tiny(B=B, H=H, Sq=Sq, Skv=Skv, D=D, axes=axes, seed=seed)
+    g = torch.Generator().manual_seed(seed + 1)
+    inp.k = torch.randn(B, Skv, Hkv, D, generator=g)
+    inp.v = torch.randn(B, Skv, Hkv, D, generator=g)
+    return inp
+
+
+def _ids_k(inp):
+    return None if inp.ids_k is None else inp.ids_k.numpy()
+
+
+def test_gqa_equals_expanded_heads():
+    """Grouped heads = the same call on K/V expanded head by head
+    (repeat_interleave), with dk, dv summed over each group."""
+    inp = _gqa()
+    H, Hkv = inp.q.shape[2], inp.k.shape[2]
+    grp = H // Hkv
+    rng = np.random.default_rng(82)
+    mask = rng.uniform(size=(2, H, inp.q.shape[1], inp.k.shape[1])) < 0.7
+    mask[..., 0] = True
+    kx, vx = (np.repeat(_np(t), grp, axis=2) for t in (inp.k, inp.v))
+    a = (_np(inp.q), _np(inp.k), _np(inp.v), _np(inp.wq), _np(inp.wk), inp.eps, inp.ids.numpy(), inp.axes, inp.theta)
+    ax = (_np(inp.q), kx, vx, _np(inp.wq), _np(inp.wk), inp.eps, inp.ids.numpy(), inp.axes, inp.theta)
+    o, lse = oracle.fwd(*a, mask=mask, ids_k=_ids_k(inp))
+    ox, lsex = oracle.fwd(*ax, mask=mask, ids_k=_ids_k(inp))
+    np.testing.assert_allclose(o, ox, rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(lse, lsex, rtol=1e-14, atol=1e-15)
+    dq, dk, dv, dwq, dwk = oracle.bwd(*a, _np(inp.do), mask=mask, ids_k=_ids_k(inp))
+    dqx, dkx, dvx, dwqx, dwkx = oracle.bwd(*ax, _np(inp.do), mask=mask, ids_k=_ids_k(inp))
+    B, Skv, _, D = dk.shape
+    np.testing.assert_allclose(dq, dqx, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dk, dkx.reshape(B, Skv, Hkv, grp, D).sum(3), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dv, dvx.reshape(B, Skv, Hkv, grp, D).sum(3), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dwq, dwqx, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dwk, dwkx, rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_matches_torch_enable_gqa():
+    """Library special case: torch fp64 rms_norm, complex-multiply RoPE at the
+    K/V head count, SDPA with enable_gqa, autograd."""
+    B, H, Hkv, S, D = 2, 6, 2, 9, 16
+    inp = wl.make_custom(B, H, D, S, S, axes=(8, 8), qk_dtype="fp32", v_dtype="fp32", seed=83)
+    g = torch.Generator().manual_seed(84)
+    inp.k = torch.randn(B, S, Hkv, D, generator=g)
+    inp.v = torch.randn(B, S, Hkv, D, generator=g)
+    q, k, v, wq, wk = (t.double().requires_grad_() for t in (inp.q, inp.k, inp.v, inp.wq, inp.wk))
+    phi = torch.from_numpy(oracle.rope_angles(inp.ids.numpy(), inp.axes, inp.theta))
+
+    def rot(x):
+        xc = torch.view_as_complex(x.reshape(*x.shape[:-1], D // 2, 2))
+        return torch.view_as_real(xc * torch.polar(torch.ones_like(phi), phi)[:, :, None, :]).reshape(x.shape)
+
+    qp = rot(F.rms_norm(q, (D,), wq, inp.eps)).transpose(1, 2)
+    kp = rot(F.rms_norm(k, (D,), wk, inp.eps)).transpose(1, 2)
+    ro = F.scaled_dot_product_attention(qp, kp, v.transpose(1, 2), is_causal=True, enable_gqa=True).transpose(1, 2)
+    (ro * inp.do.double()).sum().backward()
+    a = (_np(inp.q), _np(inp.k), _np(inp.v), _np(inp.wq), _np(inp.wk), inp.eps, inp.ids.numpy(), inp.axes, inp.theta)
+    o, _ = oracle.fwd(*a, causal=True)
+    grads = oracle.bwd(*a, _np(inp.do), causal=True)
+    np.testing.assert_allclose(o, ro.detach().numpy(), rtol=1e-10, atol=1e-12)
+    for got, t in zip(grads, (q, k, v, wq, wk)):
+        np.testing.assert_allclose(got, t.grad.numpy(), rtol=1e-9, atol=1e-11)
+
+
+def test_gqa_gradients_match_central_differences():
+    inp = _gqa(B=1, H=4, Hkv=2, Sq=5, Skv=6, seed=85)
+    q, k, v, wq, wk, dout = (_np(t).copy() for t in (inp.q, inp.k, inp.v, inp.wq, inp.wk, inp.do))
+
+    def loss():
+        o, _ = oracle.fwd(q, k, v, wq, wk, inp.eps, inp.ids.numpy(), inp.axes, inp.theta, ids_k=_ids_k(inp))
+        return float(np.sum(o * dout))
+
+    grads = oracle.bwd(q, k, v, wq, wk, inp.eps, inp.ids.numpy(), inp.axes, inp.theta, dout, ids_k=_ids_k(inp))
+    h = 1e-6
+    for arr, grad in zip((q, k, v, wq, wk), grads):
+        fd = np.zeros_like(arr)
+        flat, fdf = arr.reshape(-1), fd.reshape(-1)
+        for i in range(flat.size):
+            x0 = flat[i]
+            flat[i] = x0 + h
+            lp = loss()
+            flat[i] = x0 - h
+            lm = loss()
+            flat[i] = x0
+            fdf[i] = (lp - lm) / (2 * h)
+        np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-7)
+
+
+def test_gqa_heads_subset_sums_its_listed_group():
+    """With every query head of one group listed, that K/V head's dk, dv equal
+    the full call's; the other K/V head stays untouched (NaN)."""
+    inp = _gqa(B=1, H=4, Hkv=2, seed=86)
+    a = (_np(inp.q), _np(inp.k), _np(inp.v), _np(inp.wq), _np(inp.wk), inp.eps, inp.ids.numpy(), inp.axes, inp.theta,
+         _np(inp.do))
+    full = oracle.bwd(*a, ids_k=_ids_k(inp))
+    part = oracle.bwd(*a, ids_k=_ids_k(inp), heads=[(0, 2), (0, 3)])   # the group of K/V head 1
+    np.testing.assert_allclose(part[1][:, :, 1], full[1][:, :, 1], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(part[2][:, :, 1], full[2][:, :, 1], rtol=1e-13, atol=1e-14)
+    assert np.all(np.isnan(part[1][:, :, 0])) and np.all(np.isnan(part[2][:, :, 0]))
+    np.testing.assert_allclose(part[0][:, :, 2:], full[0][:, :, 2:], rtol=1e-13, atol=1e-14)
