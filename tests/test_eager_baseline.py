@@ -34,3 +34,23 @@ def test_eager_composition_matches_oracle():
     np.testing.assert_allclose(o.detach().numpy(), ro, rtol=1e-4, atol=1e-5)
     for got, ref in zip(grads, rg):
         np.testing.assert_allclose(got.numpy(), ref, rtol=1e-4, atol=2e-5)
+
+
+def test_probe_workload_shapes():
+    """The pages' probe shapes: B=1 H=24 D=128 at S=6144 and S=24576, and the
+    Z-Image DiT shape (1, 30, 4128, 128) in bf16."""
+    want = {"flux1_probe_6144": (1, 24, 6144), "flux1_probe_24576": (1, 24, 24576), "zimage_dit": (1, 30, 4128)}
+    for name, (B, H, S) in want.items():
+        c = wl.WORKLOADS[name]
+        ids = wl.flux_ids(c["n_text"], c["grid"], len(c["axes"]), c.get("grid_w"))
+        assert (c["B"], c["H"], ids.shape[1], c["D"]) == (B, H, S, 128), name
+        assert ids.shape[2] == len(c["axes"]) and sum(c["axes"]) == 128
+        assert c["qk_dtype"] == c["v_dtype"] == "bf16" and c["mask"] == "none" and not c["causal"]
+        # distinct image positions, text tokens at the origin
+        img = ids[0, c["n_text"]:]
+        assert len({tuple(r) for r in img.tolist()}) == img.shape[0]
+        assert int(ids[0, :c["n_text"]].abs().sum()) == 0
+    inp = wl.make("zimage_dit")
+    assert tuple(inp.q.shape) == (1, 4128, 30, 128) and inp.q.dtype == torch.bfloat16 and inp.mask is None
+    flops_f, flops_b = bench.nominal_flops(inp)
+    assert flops_f == 4.0 * 30 * 4128 * 4128 * 128 and flops_b == 2.5 * flops_f
