@@ -485,8 +485,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       fence_proxy_async_smem();
       mbar_arrive(&bars[kBarKFull]);
     }
-    named_bar(3, kProlThreads);
-    ok = !*abort_flag;  // uniform over the prologue threads
+    // the same decision in every prologue thread: a flag read after a plain
+    // barrier could differ between threads if another role aborts meanwhile,
+    // and the loop below has named barriers of its own
+    ok = !named_bar_any(3, kProlThreads, *abort_flag != 0);
     const uint32_t peer_q = mapa_shared(smem_u32(sm + kOffQ), peer);
     const uint32_t peer_qfull = mapa_shared(smem_u32(&bars[kBarQFull]), peer);
     // Q' rows: eight lanes per row (see OctRow), four rows per warp and pass;
