@@ -1,9 +1,10 @@
 """Benchmark of the fused QK-RMSNorm + multi-axis RoPE + attention call.
 
 One step = the whole hot path over one batch: st_rope_attn_fwd (rotary table,
-mask tile classes, forward attention) followed by st_rope_attn_bwd (table,
-mask classes, Delta, backward attention, dq post-pass, norm-weight gradient
-reduction). Default workload: Flux1 1024px, B=1 H=24 S=4608 D=128 bf16, 3-axis
+mask tile classes, forward attention) followed by st_rope_attn_bwd (Delta,
+backward attention with the dk epilogue, dq post-pass, norm-weight gradient
+reduction; the tables and mask tile classes of the forward are reused from the
+shared workspace, as the autograd Function does). Default workload: Flux1 1024px, B=1 H=24 S=4608 D=128 bf16, 3-axis
 RoPE (16,56,56) theta 1e4, all-True bool mask [1,1,1,4608], forward+backward.
 
 Metric: TFLOP/s with nominal FLOPs 4*B*H*S_q*S_kv*D forward (halved when
@@ -184,17 +185,18 @@ def run_ours(args, rank, world, dev):
     lse = torch.empty(B, H, Sq, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dwq, dwk = torch.empty_like(wq), torch.empty_like(wk)
-    ws_f = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal),
-                       dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal,
-                                                       for_backward=True), dtype=torch.uint8, device=dev)
+    # one backward-sized workspace serves both calls, as in the autograd
+    # Function: the backward reuses the forward's rotary tables and mask tiles
+    ws = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal,
+                                                     for_backward=True), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def step(q=q, k=k, v=v, do=do, wq=wq, wk=wk, ids=ids, mask=mask):
         api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal,
-                             o=o, lse=lse, workspace=ws_f)
+                             o=o, lse=lse, workspace=ws)
         api.st_rope_attn_bwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o, lse, do, mask=mask,
-                             causal=inp.causal, workspace=ws_b, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk)
+                             causal=inp.causal, workspace=ws, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk,
+                             reuse_tables=True)
 
     def barrier():
         if world > 1:

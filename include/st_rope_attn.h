@@ -106,7 +106,15 @@ typedef struct {
  *        converted to fp32 (entry 2j+1 is not read: the tables promise it is
  *        equal); n_axes, axes_dim and theta are then ignored.
  * cos_k, sin_k: the same for the keys ([S_kv, D], [1, S_kv, D] or
- *        [B, S_kv, D]); NULL means "same as cos/sin" and requires S_q == S_kv. */
+ *        [B, S_kv, D]); NULL means "same as cos/sin" and requires S_q == S_kv.
+ * reuse_tables: read by st_rope_attn_bwd only. 1 states that the workspace
+ *        passed to the backward already holds the device tables of exactly
+ *        this rotation and the tile classes of exactly this mask, written by
+ *        an st_rope_attn_fwd call on the same workspace pointer that is stream-
+ *        ordered before the backward (a backward-sized workspace serves both
+ *        calls: its first bytes have the forward's layout); the backward then
+ *        skips rebuilding them. Anything else is undefined results (not a
+ *        fault). 0: the backward rebuilds them. */
 typedef struct {
   const st_tensor* ids;
   const st_tensor* ids_k;
@@ -117,6 +125,7 @@ typedef struct {
   const st_tensor* sin;
   const st_tensor* cos_k;
   const st_tensor* sin_k;
+  int32_t reuse_tables;
 } st_rope;
 
 /* Counters after the pages' dispatch statistics. Bumped only after a launch
@@ -138,12 +147,12 @@ enum {
   ST_K_CLASSIFY = 1,  /* bool mask tile classification */
   ST_K_FWD = 2,       /* forward attention */
   ST_K_BWD_PRE = 3,   /* Delta = rowsum(dO * O), zero the dQ accumulator */
-  ST_K_BWD = 4,       /* backward attention (dV, dK' and dQ' accumulation) */
+  ST_K_BWD = 4,       /* backward attention: dV, dK (inverse rotation and RMSNorm
+                         backward in its epilogue), dQ' accumulation */
   ST_K_DQ_POST = 5,   /* dQ: inverse rotation + RMSNorm backward */
   ST_K_DW = 6,        /* norm-weight gradient reduction */
-  ST_K_DK_POST = 7,   /* dK: inverse rotation + RMSNorm backward */
-  ST_K_PROBE = 8,     /* bounded-wait self-test */
-  ST_K_COUNT = 9
+  ST_K_PROBE = 7,     /* bounded-wait self-test */
+  ST_K_COUNT = 8
 };
 
 /* Per-kernel device time between two st_timing_read calls. */
@@ -159,9 +168,14 @@ ST_API size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k
                                    const st_tensor* mask, int causal, const st_rope* rope, int for_backward);
 
 /* Forward.
- *  q, k:   [B, S_q, H, D] / [B, S_kv, H, D], bf16 or fp32 (fp32 is rounded to
- *          bf16 after the norm and rotation, as an autocast SDPA would).
- *  v:      [B, S_kv, H, D] bf16.
+ *  q, k:   [B, S_q, H, D] / [B, S_kv, H_kv, D], bf16 or fp32 (fp32 is rounded
+ *          to bf16 after the norm and rotation, as an autocast SDPA would).
+ *  v:      [B, S_kv, H_kv, D] bf16.
+ *          H_kv divides H (grouped K/V heads; H_kv = H is plain multi-head
+ *          attention): query head h attends with K/V head h / (H / H_kv), and
+ *          k is normalised and rotated at the K/V head count ("Metal Flash
+ *          Attention", section "Fused RoPE + SDPA": GQA inputs are rotated at
+ *          the K/V head count and expanded afterwards).
  *  q_norm_w, k_norm_w: [D] fp32 RMSNorm weights; eps: RMSNorm epsilon.
  *  rope:   rotary specification (above).
  *  mask:   NULL, or [B|1, H|1, S_q|1, S_kv] bool (True = attend) or additive
@@ -180,10 +194,13 @@ ST_API st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const 
 
 /* Backward. Inputs as for the forward plus o and lse from it and d_o
  * ([B, S_q, H, D], dtype of v). Outputs:
- *  dq, dk: dtype of q / k; dv: dtype of v; same shapes as q / k / v.
+ *  dq, dk: dtype of q / k; dv: dtype of v; same shapes as q / k / v (with
+ *          grouped K/V heads, dk and dv of a K/V head sum the gradients of
+ *          all the query heads that use it).
  *  d_q_norm_w, d_k_norm_w: [D] fp32 (overwritten, not accumulated).
- * dq/dk/dv/dw are deterministic except dq, whose fp32 accumulation across key
- * tiles uses atomic adds. */
+ * dk/dv/dw are deterministic; dq is not bit-reproducible: its fp32
+ * accumulation across key tiles is a sum of TMA bulk reduce-adds (fp32 adds in
+ * L2) whose order varies from run to run. */
 ST_API st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* q_norm_w,
                            const st_tensor* k_norm_w, float eps, const st_rope* rope, const st_tensor* mask,
                            int causal, float scale, const st_tensor* o, const st_tensor* lse, const st_tensor* d_o,

@@ -44,7 +44,8 @@ class st_rope(ctypes.Structure):
     _fields_ = [("ids", ctypes.POINTER(st_tensor)), ("ids_k", ctypes.POINTER(st_tensor)),
                 ("n_axes", ctypes.c_int32), ("axes_dim", ctypes.c_int32 * 8), ("theta", ctypes.c_double),
                 ("cos", ctypes.POINTER(st_tensor)), ("sin", ctypes.POINTER(st_tensor)),
-                ("cos_k", ctypes.POINTER(st_tensor)), ("sin_k", ctypes.POINTER(st_tensor))]
+                ("cos_k", ctypes.POINTER(st_tensor)), ("sin_k", ctypes.POINTER(st_tensor)),
+                ("reuse_tables", ctypes.c_int32)]
 
 
 class RopeTables:
@@ -67,11 +68,11 @@ class st_stats(ctypes.Structure):
                                                 "kernel_launches")]
 
 
-KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce", "dk_post", "probe"]
+KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce", "probe"]
 
 
 class st_kernel_times(ctypes.Structure):
-    _fields_ = [("launches", ctypes.c_uint64 * 9), ("ms", ctypes.c_double * 9)]
+    _fields_ = [("launches", ctypes.c_uint64 * len(KERNEL_KINDS)), ("ms", ctypes.c_double * len(KERNEL_KINDS))]
 
 
 class StError(RuntimeError):
@@ -146,8 +147,9 @@ def _check(status: int):
         raise StError(status, lib().st_last_error().decode())
 
 
-def _rope(ids, axes_dim, theta, ids_k):
+def _rope(ids, axes_dim, theta, ids_k, reuse_tables=False):
     r = st_rope()
+    r.reuse_tables = int(bool(reuse_tables))
     if isinstance(ids, RopeTables):
         if ids_k is not None:
             raise StError(ST_ERR_INVALID_ARG, "ids_k cannot be combined with RopeTables (use cos_k/sin_k)")
@@ -213,8 +215,13 @@ def st_rope_attn_fwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mas
 
 
 def st_rope_attn_bwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, o, lse, d_o, mask=None, causal=False,
-                     scale=None, ids_k=None, workspace=None, dq=None, dk=None, dv=None, dwq=None, dwk=None):
-    """Returns (dq, dk, dv, d_q_norm_w, d_k_norm_w)."""
+                     scale=None, ids_k=None, workspace=None, dq=None, dk=None, dv=None, dwq=None, dwk=None,
+                     reuse_tables=False):
+    """Returns (dq, dk, dv, d_q_norm_w, d_k_norm_w). reuse_tables: the given
+    workspace was passed to the forward of this call (same rotation and mask),
+    so its tables and mask tile classes are reused instead of rebuilt."""
+    if reuse_tables and workspace is None:
+        raise StError(ST_ERR_INVALID_ARG, "reuse_tables needs the forward's workspace")
     _require_cuda(q, k, v, q_norm_w, k_norm_w, ids, mask, ids_k, o, lse, d_o)
     dq = torch.empty_like(q, memory_format=torch.contiguous_format) if dq is None else dq
     dk = torch.empty_like(k, memory_format=torch.contiguous_format) if dk is None else dk
@@ -222,7 +229,9 @@ def st_rope_attn_bwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, o, 
     dwq = torch.empty_like(q_norm_w) if dwq is None else dwq
     dwk = torch.empty_like(k_norm_w) if dwk is None else dwk
     ws = _workspace(q, k, v, ids, axes_dim, theta, mask, causal, ids_k, True, workspace)
-    r = _rope(ids, axes_dim, theta, ids_k)
+    if reuse_tables and ws is not workspace:
+        raise StError(ST_ERR_WORKSPACE, "reuse_tables: the workspace is smaller than the backward needs")
+    r = _rope(ids, axes_dim, theta, ids_k, reuse_tables)
     st = lib().st_rope_attn_bwd(_p(_t(q)), _p(_t(k)), _p(_t(v)), _p(_t(q_norm_w)), _p(_t(k_norm_w)), float(eps),
                                 ctypes.byref(r), _p(_t(mask)), int(bool(causal)),
                                 float(scale) if scale else 0.0, _p(_t(o)), _p(_t(lse)), _p(_t(d_o)),
@@ -288,11 +297,15 @@ def st_timing_read() -> dict:
 class RopeAttention(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mask, causal, scale, ids_k):
+        # one backward-sized workspace for both calls: the backward reuses the
+        # rotary tables and mask tile classes the forward built in it
+        ws = _workspace(q, k, v, ids, axes_dim, theta, mask, causal, ids_k, True, None)
         o, lse = st_rope_attn_fwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, mask, causal, scale,
-                                  ids_k)
+                                  ids_k, workspace=ws)
         tables = ids if isinstance(ids, RopeTables) else None  # no gradient flows to the tables
         ctx.save_for_backward(q, k, v, q_norm_w, k_norm_w, None if tables else ids, mask, ids_k, o, lse)
         ctx.cfg = (eps, tuple(axes_dim), theta, causal, scale, tables)
+        ctx.ws = ws
         return o
 
     @staticmethod
@@ -302,7 +315,9 @@ class RopeAttention(torch.autograd.Function):
         if tables is not None:
             ids = tables
         dq, dk, dv, dwq, dwk = st_rope_attn_bwd(q, k, v, q_norm_w, k_norm_w, eps, ids, axes_dim, theta, o, lse,
-                                                d_o.contiguous(), mask, causal, scale, ids_k)
+                                                d_o.contiguous(), mask, causal, scale, ids_k, workspace=ctx.ws,
+                                                reuse_tables=True)
+        ctx.ws = None
         return dq, dk, dv, dwq, dwk, None, None, None, None, None, None, None, None
 
 

@@ -126,9 +126,15 @@ st_status device_globals(Dev* d) {
 // ------------------------------------------------------------- validation
 struct Shape {
   int B = 0, Sq = 0, Skv = 0, H = 0, D = 0;
+  int Hkv = 0;  // K/V heads: H is a multiple of it (grouped K/V heads)
 };
 
-st_status check_bshd(const st_tensor* t, const char* name, int B, int S, int H, int D, int dt_a, int dt_b,
+static_assert(kDtBF16 == ST_BF16 && kDtF16 == ST_F16 && kDtF32 == ST_F32, "row dtype codes");
+
+constexpr unsigned bit(int dt) { return 1u << dt; }
+
+// A [B, S, H, D] tensor whose dtype is one of `dts` (a set of bit(st_dtype)).
+st_status check_bshd(const st_tensor* t, const char* name, int B, int S, int H, int D, unsigned dts,
                      RowTensor* out) {
   if (!t) return fail(ST_ERR_INVALID_ARG, "%s is NULL", name);
   if (t->ndim != 4) return fail(ST_ERR_SHAPE, "%s must be 4-D [B,S,H,D], got ndim=%d", name, t->ndim);
@@ -136,7 +142,8 @@ st_status check_bshd(const st_tensor* t, const char* name, int B, int S, int H, 
     return fail(ST_ERR_SHAPE, "%s has shape [%lld,%lld,%lld,%lld], expected [%d,%d,%d,%d]", name,
                 (long long)t->shape[0], (long long)t->shape[1], (long long)t->shape[2], (long long)t->shape[3], B,
                 S, H, D);
-  if (t->dtype != dt_a && t->dtype != dt_b) return fail(ST_ERR_DTYPE, "%s has unsupported dtype %d", name, t->dtype);
+  if (t->dtype < 0 || t->dtype > 31 || !(dts & bit(t->dtype)))
+    return fail(ST_ERR_DTYPE, "%s has unsupported dtype %d", name, t->dtype);
   const int64_t n = (int64_t)B * S * H;
   if (n > 0) {
     if (!t->data) return fail(ST_ERR_INVALID_ARG, "%s data is NULL", name);
@@ -153,7 +160,7 @@ st_status check_bshd(const st_tensor* t, const char* name, int B, int S, int H, 
     out->sb = t->shape[0] > 1 ? t->stride[0] : 0;
     out->ss = t->shape[1] > 1 ? t->stride[1] : 0;
     out->sh = t->shape[2] > 1 ? t->stride[2] : 0;
-    out->is_f32 = t->dtype == ST_F32;
+    out->dt = t->dtype;
   }
   return ST_OK;
 }
@@ -227,7 +234,6 @@ struct Plan {
   int nQt = 0, nKt = 0, nQtm = 1;
   // workspace offsets
   size_t off_tab16_q = 0, off_tab16_k = 0;
-  size_t off_dkacc = 0;
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
          off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
   int n_dwq = 0, n_dwk = 0;
@@ -250,9 +256,19 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     return fail(ST_ERR_SHAPE, "sizes out of range");
   if (s.D != kD) return fail(ST_ERR_UNSUPPORTED, "head dimension %d is not supported (this build handles D=128)", s.D);
   st_status st;
-  if ((st = check_bshd(q, "q", s.B, s.Sq, s.H, s.D, ST_BF16, ST_F32, &P->q)) != ST_OK) return st;
-  if ((st = check_bshd(k, "k", s.B, s.Skv, s.H, s.D, ST_BF16, ST_F32, &P->k)) != ST_OK) return st;
-  if ((st = check_bshd(v, "v", s.B, s.Skv, s.H, s.D, ST_BF16, ST_BF16, &P->v)) != ST_OK) return st;
+  const unsigned qk_types = bit(ST_BF16) | bit(ST_F16) | bit(ST_F32), v_types = bit(ST_BF16) | bit(ST_F16);
+  if ((st = check_bshd(q, "q", s.B, s.Sq, s.H, s.D, qk_types, &P->q)) != ST_OK) return st;
+  // grouped K/V heads: k and v carry H_kv heads, H a multiple of H_kv
+  s.Hkv = static_cast<int>(k->shape[2]);
+  if (s.H == 0 ? k->shape[2] != 0 : (k->shape[2] < 1 || k->shape[2] > 65535 || s.H % s.Hkv != 0))
+    return fail(ST_ERR_SHAPE, "k has %lld heads: the K/V head count must divide H=%d", (long long)k->shape[2], s.H);
+  if ((st = check_bshd(k, "k", s.B, s.Skv, s.Hkv, s.D, qk_types, &P->k)) != ST_OK) return st;
+  if ((st = check_bshd(v, "v", s.B, s.Skv, s.Hkv, s.D, v_types, &P->v)) != ST_OK) return st;
+  // the MMA operands take v's 16-bit type; 16-bit q/k must have it already
+  // (they are staged as raw operand rows), fp32 q/k are cast to it on load
+  if (q->dtype != k->dtype) return fail(ST_ERR_DTYPE, "q and k must have the same dtype");
+  if (q->dtype != ST_F32 && q->dtype != v->dtype)
+    return fail(ST_ERR_DTYPE, "16-bit q/k must have v's dtype (or be fp32, cast on load)");
   if (!rope) return fail(ST_ERR_INVALID_ARG, "rope is NULL");
   if (rope->cos || rope->sin) {  // the pages' table form
     if (rope->ids || rope->ids_k) return fail(ST_ERR_INVALID_ARG, "rope: give either ids or cos/sin tables, not both");
@@ -335,9 +351,7 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     off = align_up(off + (size_t)s.B * s.H * s.Sq * sizeof(float), 256);
     P->off_dqacc = off;
     off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * sizeof(float), 256);
-    P->off_dkacc = off;
-    off = align_up(off + (size_t)s.B * s.Skv * s.H * kD * sizeof(float), 256);
-    P->n_dwk = static_cast<int>(((int64_t)s.B * s.Skv * s.H + kTile - 1) / kTile);
+    P->n_dwk = s.B * s.Hkv * P->nKt;  // one partial per backward CTA (key tile, K/V head, batch)
     P->off_dwk = off;
     off = align_up(off + (size_t)P->n_dwk * kD * sizeof(float), 256);
     P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kTile - 1) / kTile);
@@ -376,11 +390,14 @@ void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float 
     c->f_sq = P.nQtm > 1 ? P.nKt : 0;
   }
   c->causal = causal ? 1 : 0;
+  c->f16 = P.v.dt == kDtF16 ? 1 : 0;
   const float sc = scale > 0.f ? scale : 1.0f / std::sqrt(static_cast<float>(kD));
   c->scale = sc;
   c->scale_log2 = sc * kLog2e;
   c->B = P.sh.B;
   c->H = P.sh.H;
+  c->Hkv = P.sh.Hkv;
+  c->group = P.sh.Hkv > 0 ? P.sh.H / P.sh.Hkv : 1;
   c->Sq = P.sh.Sq;
   c->Skv = P.sh.Skv;
   c->nQt = P.nQt;
@@ -474,7 +491,7 @@ st_status check_workspace(const Plan& P, void* ws, size_t bytes) {
 }
 
 st_status check_out(const st_tensor* t, const char* name, int B, int S, int H, int dtype, RowTensor* rt) {
-  return check_bshd(t, name, B, S, H, kD, dtype, dtype, rt);
+  return check_bshd(t, name, B, S, H, kD, bit(dtype), rt);
 }
 
 // The encoder is a driver call and needs a context current on the calling
@@ -496,14 +513,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 4-D tiled map over a bf16 [B, S, H, D] tensor for 64-column x box_rows boxes
-// with 128-byte swizzle. The two middle dims are ordered by stride (s before h
-// when the sequence stride is the smaller one, as in a BHSD view).
+// 4-D tiled map over a bf16, fp16 or fp32 [B, S, H, D] tensor for boxes of
+// 128 bytes (64 16-bit or 32 fp32 columns) x box_rows rows with 128-byte
+// swizzle. The two
+// middle dims are ordered by stride (s before h when the sequence stride is the
+// smaller one, as in a BHSD view).
 st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, int box_rows = kTile) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const int64_t B = t->shape[0], S = t->shape[1], H = t->shape[2];
-  const int64_t eb = 2;
+  const bool f32 = t->dtype == ST_F32;
+  const int64_t eb = f32 ? 4 : 2;
   // strides in bytes; a size-1 dim gets the packed stride (any valid value works)
   int64_t ss = S > 1 ? t->stride[1] * eb : H * kD * eb;
   int64_t sh = H > 1 ? t->stride[2] * eb : kD * eb;
@@ -513,7 +533,7 @@ st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, in
   if (sb == 0) sb = S * H * kD * eb;
   *s_first = ss < sh;
   cuuint64_t dims[4], strides[3];
-  cuuint32_t box[4] = {64, 1, 1, 1}, es[4] = {1, 1, 1, 1};
+  cuuint32_t box[4] = {f32 ? 32u : 64u, 1, 1, 1}, es[4] = {1, 1, 1, 1};
   dims[0] = kD;
   if (*s_first) {
     dims[1] = S; dims[2] = H; strides[0] = ss; strides[1] = sh; box[1] = box_rows;
@@ -522,10 +542,28 @@ st_status encode_rows_map(const st_tensor* t, CUtensorMap* map, int* s_first, in
   }
   dims[3] = B;
   strides[2] = sb;
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, t->data, dims, strides, box, es,
+  const CUtensorMapDataType ty = f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : (t->dtype == ST_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  CUresult r = enc(map, ty, 4, t->data, dims,
+                   strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(ST_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the layout (error %d)", (int)r);
+  return ST_OK;
+}
+
+// 2-D tiled map over an fp32 rotary table [rows, 64] float2 (cos, sin) seen as
+// [rows, 128] floats, for 32-float x 128-row boxes with 128-byte swizzle: the
+// backward's epilogue stages a key tile's table rows with it.
+st_status encode_table_map(const float2* tab, int64_t rows, CUtensorMap* map) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
+  cuuint32_t box[2] = {32, kTile}, es[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float2*>(tab), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(ST_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the layout (error %d)", (int)r);
+  if (r != CUDA_SUCCESS) return fail(ST_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled rejected the rotary table (error %d)", (int)r);
   return ST_OK;
 }
 
@@ -597,10 +635,10 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
   fp.o_sb = ro.sb;
   fp.o_ss = ro.ss;
   fp.o_sh = ro.sh;
-  fp.o_f32 = ro.is_f32;
+  fp.o_dt = ro.dt;
   fp.lse = static_cast<float*>(lse->data);
   if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
-  fp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+  fp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
   if (fp.qk_tma) {
     if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
     if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
@@ -608,7 +646,7 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
   if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch")) != ST_OK) return st;
   ++h_fwd_calls;
-  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  if (q->dtype == ST_F32) ++h_mixed;
   return ST_OK;
 }
 
@@ -632,8 +670,8 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   if ((st = check_out(o, "o", s.B, s.Sq, s.H, v->dtype, &ro)) != ST_OK) return st;
   if ((st = check_out(d_o, "d_o", s.B, s.Sq, s.H, v->dtype, &rdo)) != ST_OK) return st;
   if ((st = check_out(dq, "dq", s.B, s.Sq, s.H, q->dtype, &rdq)) != ST_OK) return st;
-  if ((st = check_out(dk, "dk", s.B, s.Skv, s.H, k->dtype, &rdk)) != ST_OK) return st;
-  if ((st = check_out(dv, "dv", s.B, s.Skv, s.H, v->dtype, &rdv)) != ST_OK) return st;
+  if ((st = check_out(dk, "dk", s.B, s.Skv, s.Hkv, k->dtype, &rdk)) != ST_OK) return st;
+  if ((st = check_out(dv, "dv", s.B, s.Skv, s.Hkv, v->dtype, &rdv)) != ST_OK) return st;
   if (!lse || lse->ndim != 3 || lse->shape[0] != s.B || lse->shape[1] != s.H || lse->shape[2] != s.Sq)
     return fail(ST_ERR_SHAPE, "lse must be [B,H,S_q] = [%d,%d,%d]", s.B, s.H, s.Sq);
   if (lse->dtype != ST_F32) return fail(ST_ERR_DTYPE, "lse must be fp32");
@@ -655,14 +693,22 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     if ((st = encode_rows_map(v, &bp.tmap_v, &bp.v_s_first)) != ST_OK) return st;
     if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first, kTile / 2)) != ST_OK)
       return st;
-    bp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+    bp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
+    // raw k rows: the prologue's TMA source (bf16) and the epilogue's (both dtypes)
+    if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
     if (bp.qk_tma) {
-      if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
       if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first, kTile / 4)) != ST_OK)
         return st;
     }
+    if ((st = encode_table_map(reinterpret_cast<const float2*>(ws + P.off_tab_k), (int64_t)P.ids_k.Bt * s.Skv,
+                               &bp.tmap_tab_k)) != ST_OK)
+      return st;
   }
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  // the forward's tables and mask tile classes, when the caller says the
+  // workspace holds them (the pre kernel then clears the control words that
+  // the table kernel would have cleared)
+  const bool reuse = rope->reuse_tables != 0 && (int64_t)s.B * s.Sq * s.H > 0;
+  if (!reuse && (st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
 
   float* delta = reinterpret_cast<float*>(ws + P.off_delta);
   float* dq_acc = reinterpret_cast<float*>(ws + P.off_dqacc);
@@ -670,11 +716,12 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     PreParams pp;
     memset(&pp, 0, sizeof(pp));
     pp.o = o->data;
-    pp.o_sb = ro.sb; pp.o_ss = ro.ss; pp.o_sh = ro.sh; pp.o_f32 = ro.is_f32;
+    pp.o_sb = ro.sb; pp.o_ss = ro.ss; pp.o_sh = ro.sh; pp.o_dt = ro.dt;
     pp.dout = d_o->data;
     pp.do_sb = rdo.sb; pp.do_ss = rdo.ss; pp.do_sh = rdo.sh;
     pp.delta = delta;
     pp.dq_acc = dq_acc;
+    pp.ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
     pp.B = s.B; pp.H = s.H; pp.Sq = s.Sq;
     if ((st = cuda_check(launch_counted(ST_K_BWD_PRE, stream, [&] { return launch_bwd_pre(pp, stream); }), "backward pre launch")) != ST_OK) return st;
   }
@@ -688,22 +735,10 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     bp.dq_acc = dq_acc;
     if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_dq_acc_map(dq_acc, s.B, s.Sq, s.H, &bp.tmap_dq)) != ST_OK)
       return st;
-    bp.dv = dv->data; bp.dv_sb = rdv.sb; bp.dv_ss = rdv.ss; bp.dv_sh = rdv.sh; bp.dv_f32 = rdv.is_f32;
-    bp.dk_acc = reinterpret_cast<float*>(ws + P.off_dkacc);
+    bp.dv = dv->data; bp.dv_sb = rdv.sb; bp.dv_ss = rdv.ss; bp.dv_sh = rdv.sh; bp.dv_dt = rdv.dt;
+    bp.dk = dk->data; bp.dk_sb = rdk.sb; bp.dk_ss = rdk.ss; bp.dk_sh = rdk.sh; bp.dk_dt = rdk.dt;
+    bp.dwk_part = reinterpret_cast<float*>(ws + P.off_dwk);
     if ((st = cuda_check(launch_counted(ST_K_BWD, stream, [&] { return launch_bwd(bp, stream); }), "backward kernel launch")) != ST_OK) return st;
-    // dK' -> dK: the same row transform as for dQ, on the key side
-    PostParams pk;
-    memset(&pk, 0, sizeof(pk));
-    pk.dq_acc = bp.dk_acc;
-    pk.q = P.k;
-    pk.tab_q = reinterpret_cast<const float2*>(ws + P.off_tab_k);
-    pk.tab_q_sb = P.ids_k.Bt > 1 ? (int64_t)s.Skv * kPairs : 0;
-    pk.wq = static_cast<const float*>(k_norm_w->data);
-    pk.eps = eps;
-    pk.dq = dk->data; pk.dq_sb = rdk.sb; pk.dq_ss = rdk.ss; pk.dq_sh = rdk.sh; pk.dq_f32 = rdk.is_f32;
-    pk.dwq_part = reinterpret_cast<float*>(ws + P.off_dwk);
-    pk.B = s.B; pk.H = s.H; pk.Sq = s.Skv;
-    if ((st = cuda_check(launch_counted(ST_K_DK_POST, stream, [&] { return launch_dq_post(pk, stream); }), "dk post launch")) != ST_OK) return st;
   }
   if ((int64_t)s.B * s.Sq * s.H > 0) {
     PostParams pq;
@@ -714,7 +749,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     pq.tab_q_sb = P.ids_q.Bt > 1 ? (int64_t)s.Sq * kPairs : 0;
     pq.wq = static_cast<const float*>(q_norm_w->data);
     pq.eps = eps;
-    pq.dq = dq->data; pq.dq_sb = rdq.sb; pq.dq_ss = rdq.ss; pq.dq_sh = rdq.sh; pq.dq_f32 = rdq.is_f32;
+    pq.dq = dq->data; pq.dq_sb = rdq.sb; pq.dq_ss = rdq.ss; pq.dq_sh = rdq.sh; pq.dq_dt = rdq.dt;
     pq.dwq_part = reinterpret_cast<float*>(ws + P.off_dwq);
     pq.B = s.B; pq.H = s.H; pq.Sq = s.Sq;
     if ((st = cuda_check(launch_counted(ST_K_DQ_POST, stream, [&] { return launch_dq_post(pq, stream); }), "dq post launch")) != ST_OK) return st;
@@ -731,7 +766,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   dp.dwk = static_cast<float*>(d_k_norm_w->data);
   if ((st = cuda_check(launch_counted(ST_K_DW, stream, [&] { return launch_dw_reduce(dp, stream); }), "weight-gradient reduce launch")) != ST_OK) return st;
   ++h_bwd_calls;
-  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  if (q->dtype == ST_F32) ++h_mixed;
   return ST_OK;
 }
 
@@ -816,10 +851,10 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   fp.o_sb = ro.sb;
   fp.o_ss = ro.ss;
   fp.o_sh = ro.sh;
-  fp.o_f32 = ro.is_f32;
+  fp.o_dt = ro.dt;
   fp.lse = static_cast<float*>(lse->data);
   if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
-  fp.qk_tma = (q->dtype == ST_BF16 && k->dtype == ST_BF16) ? 1 : 0;
+  fp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
   if (fp.qk_tma) {
     if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
     if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
@@ -829,7 +864,7 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
                        "forward kernel launch")) != ST_OK)
     return st;
   ++h_fwd_calls;
-  if (q->dtype == ST_F32 && v->dtype == ST_BF16) ++h_mixed;
+  if (q->dtype == ST_F32) ++h_mixed;
   return ST_OK;
 }
 

@@ -13,6 +13,29 @@ namespace st {
 
 namespace {
 
+// (b, i, h) of row `row` of a [B, S, H] row space; 32-bit arithmetic when the
+// row count allows it (a 64-bit division is a long software sequence).
+struct RowIdx {
+  int b, i, h;
+};
+__device__ __forceinline__ RowIdx row_idx(int64_t row, int S, int H, bool small) {
+  RowIdx r;
+  if (small) {
+    const uint32_t rw = static_cast<uint32_t>(row), t = rw / static_cast<uint32_t>(H);
+    r.h = static_cast<int>(rw - t * static_cast<uint32_t>(H));
+    r.b = static_cast<int>(t / static_cast<uint32_t>(S));
+    r.i = static_cast<int>(t - static_cast<uint32_t>(r.b) * static_cast<uint32_t>(S));
+  } else {
+    const int64_t t = row / H;
+    r.h = static_cast<int>(row - t * H);
+    r.b = static_cast<int>(t / S);
+    r.i = static_cast<int>(t - static_cast<int64_t>(r.b) * S);
+  }
+  return r;
+}
+
+static_assert(kPairs == 64, "the table kernel indexes pairs with shifts");
+
 // Element e of a caller table as fp32.
 __device__ __forceinline__ float table_elem(const void* t, int dtype, int64_t e) {
   if (dtype == kTabF32) return static_cast<const float*>(t)[e];
@@ -27,10 +50,10 @@ __global__ void table_kernel(const __grid_constant__ TableParams p) {
   if (blockIdx.x == 0 && threadIdx.x < kCtrlWords && p.ctrl) p.ctrl[threadIdx.x] = 0u;
   const int64_t n = (int64_t)p.Bt * p.S * kPairs;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
-    const int pr = static_cast<int>(e % kPairs);
-    const int64_t tok = e / kPairs;
-    const int s = static_cast<int>(tok % p.S);
-    const int bt = static_cast<int>(tok / p.S);
+    const int pr = static_cast<int>(e & (kPairs - 1));
+    const int64_t tok = e >> 6;  // kPairs = 64
+    const int bt = p.Bt == 1 ? 0 : static_cast<int>(tok / p.S);
+    const int s = static_cast<int>(tok - static_cast<int64_t>(bt) * p.S);
     if (p.cos) {
       const float cs = table_elem(p.cos, p.tab_dtype, bt * p.c_sb + (int64_t)s * p.c_ss + (int64_t)(2 * pr) * p.c_sd);
       const float sn = table_elem(p.sin, p.tab_dtype, bt * p.s_sb + (int64_t)s * p.s_ss + (int64_t)(2 * pr) * p.s_sd);
@@ -87,34 +110,70 @@ __global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
   }
 }
 
-// One warp per (b, i, h) row.
-__global__ void bwd_pre_kernel(const __grid_constant__ PreParams p) {
+// Four (b, i, h) rows per warp and pass, their loads issued together; lane l
+// owns head dims 4l..4l+3 of each row. Block 0 also clears the weight-gradient
+// reduction counters (the table kernel, which clears them otherwise, may be
+// skipped by a backward that reuses the forward's tables).
+constexpr int kPreRows = 4;
+
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ PreParams p) {
+  if (blockIdx.x == 0 && threadIdx.x < 2 && p.ctrl) p.ctrl[kCtrlDwDone + threadIdx.x] = 0u;
   const int lane = threadIdx.x & 31;
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
-  if (row >= nrows) return;
-  const int h = static_cast<int>(row % p.H);
-  const int i = static_cast<int>((row / p.H) % p.Sq);
-  const int b = static_cast<int>(row / ((int64_t)p.H * p.Sq));
-  float o[4], g[4];
-  const int64_t oo = b * p.o_sb + (int64_t)i * p.o_ss + h * p.o_sh + 4 * lane;
-  const int64_t go = b * p.do_sb + (int64_t)i * p.do_ss + h * p.do_sh + 4 * lane;
-  if (p.o_f32) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.o) + oo));
-    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
-    const float4 w = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.dout) + go));
-    g[0] = w.x; g[1] = w.y; g[2] = w.z; g[3] = w.w;
-  } else {
-    const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.o) + oo));
-    o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
-    const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.dout) + go));
-    g[0] = bf16_lo(w.x); g[1] = bf16_hi(w.x); g[2] = bf16_lo(w.y); g[3] = bf16_hi(w.y);
-  }
-  float acc = o[0] * g[0] + o[1] * g[1] + o[2] * g[2] + o[3] * g[3];
+  const bool small = nrows < (int64_t(1) << 31);
+  const int64_t row0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kPreRows;
+  float o[kPreRows][4], g[kPreRows][4];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) p.delta[((int64_t)b * p.H + h) * p.Sq + i] = acc;
-  reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int u = 0; u < kPreRows; ++u) {
+    const int64_t row = row0 + u;
+    if (row >= nrows) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[u][e] = g[u][e] = 0.f;
+      continue;
+    }
+    const RowIdx x = row_idx(row, p.Sq, p.H, small);
+    const int b = x.b, i = x.i, h = x.h;
+    const int64_t oo = b * p.o_sb + (int64_t)i * p.o_ss + h * p.o_sh + 4 * lane;
+    const int64_t go = b * p.do_sb + (int64_t)i * p.do_ss + h * p.do_sh + 4 * lane;
+    if (p.o_dt == kDtF32) {
+      const float4 v = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.o) + oo));
+      const float4 w = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.dout) + go));
+      o[u][0] = v.x; o[u][1] = v.y; o[u][2] = v.z; o[u][3] = v.w;
+      g[u][0] = w.x; g[u][1] = w.y; g[u][2] = w.z; g[u][3] = w.w;
+    } else {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.o) + oo));
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.dout) + go));
+      const bool h = p.o_dt == kDtF16;
+      o[u][0] = h ? f16_lo(v.x) : bf16_lo(v.x); o[u][1] = h ? f16_hi(v.x) : bf16_hi(v.x);
+      o[u][2] = h ? f16_lo(v.y) : bf16_lo(v.y); o[u][3] = h ? f16_hi(v.y) : bf16_hi(v.y);
+      g[u][0] = h ? f16_lo(w.x) : bf16_lo(w.x); g[u][1] = h ? f16_hi(w.x) : bf16_hi(w.x);
+      g[u][2] = h ? f16_lo(w.y) : bf16_lo(w.y); g[u][3] = h ? f16_hi(w.y) : bf16_hi(w.y);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPreRows; ++u) {
+    const int64_t row = row0 + u;
+    if (row < nrows) reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float acc[kPreRows];
+#pragma unroll
+  for (int u = 0; u < kPreRows; ++u) acc[u] = o[u][0] * g[u][0] + o[u][1] * g[u][1] + o[u][2] * g[u][2] + o[u][3] * g[u][3];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+#pragma unroll
+    for (int u = 0; u < kPreRows; ++u) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+  }
+  if (lane < kPreRows) {
+    float a = acc[0];
+#pragma unroll
+    for (int u = 1; u < kPreRows; ++u)
+      if (lane == u) a = acc[u];
+    const int64_t row = row0 + lane;
+    if (row < nrows) {
+      const RowIdx x = row_idx(row, p.Sq, p.H, small);
+      p.delta[((int64_t)x.b * p.H + x.h) * p.Sq + x.i] = a;
+    }
+  }
 }
 
 // One warp per (b, i, h) row, 128 rows per block (8 warps x 16 rows). Lane l
@@ -131,47 +190,81 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+constexpr int kPostRows = 4;  // rows per warp and pass, their loads issued together
+
 __global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_constant__ PostParams p) {
   __shared__ float4 part[kPostWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  const bool small = nrows < (int64_t(1) << 31);
   const int64_t row0 = (int64_t)blockIdx.x * kTile;
   const float4 w = __ldg(reinterpret_cast<const float4*>(p.wq) + lane);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int k = warp; k < kTile; k += kPostWarps) {
-    const int64_t row = row0 + k;
-    if (row >= nrows) break;
-    const int h = static_cast<int>(row % p.H);
-    const int i = static_cast<int>((row / p.H) % p.Sq);
-    const int b = static_cast<int>(row / ((int64_t)p.H * p.Sq));
-    const float4 g = __ldg(reinterpret_cast<const float4*>(p.dq_acc + row * kD) + lane);
-    const int64_t xoff = b * p.q.sb + (int64_t)i * p.q.ss + h * p.q.sh + 4 * lane;
-    float4 x;
-    if (p.q.is_f32) {
-      x = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.q.p) + xoff));
-    } else {
-      const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(p.q.p) + xoff));
-      x = make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+#pragma unroll 1
+  for (int k0 = warp * kPostRows; k0 < kTile; k0 += kPostWarps * kPostRows) {
+    float4 g[kPostRows], x[kPostRows], cs[kPostRows];
+    int64_t yoff[kPostRows];
+    bool valid[kPostRows];
+#pragma unroll
+    for (int u = 0; u < kPostRows; ++u) {
+      const int64_t row = row0 + k0 + u;
+      valid[u] = row < nrows;
+      const int64_t rr = valid[u] ? row : 0;
+      const RowIdx x3 = row_idx(rr, p.Sq, p.H, small);
+      const int b = x3.b, i = x3.i, h = x3.h;
+      g[u] = __ldg(reinterpret_cast<const float4*>(p.dq_acc + rr * kD) + lane);
+      const int64_t xoff = b * p.q.sb + (int64_t)i * p.q.ss + h * p.q.sh + 4 * lane;
+      if (p.q.dt == kDtF32) {
+        x[u] = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(p.q.p) + xoff));
+      } else {
+        const uint2 t = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(p.q.p) + xoff));
+        x[u] = p.q.dt == kDtF16 ? make_float4(f16_lo(t.x), f16_hi(t.x), f16_lo(t.y), f16_hi(t.y))
+                                : make_float4(bf16_lo(t.x), bf16_hi(t.x), bf16_lo(t.y), bf16_hi(t.y));
+      }
+      cs[u] = __ldg(reinterpret_cast<const float4*>(p.tab_q + b * p.tab_q_sb + (int64_t)i * kPairs) + lane);
+      yoff[u] = b * p.dq_sb + (int64_t)i * p.dq_ss + h * p.dq_sh + 4 * lane;
     }
-    const float4 cs = __ldg(reinterpret_cast<const float4*>(p.tab_q + b * p.tab_q_sb + (int64_t)i * kPairs) + lane);
-    const float r = rsqrtf(warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) * (1.0f / kD) + p.eps);
+    float ss[kPostRows];
+#pragma unroll
+    for (int u = 0; u < kPostRows; ++u)
+      ss[u] = x[u].x * x[u].x + x[u].y * x[u].y + x[u].z * x[u].z + x[u].w * x[u].w;
     // inverse rotation of the two pairs: (cos, sin) = (cs.x, cs.y), (cs.z, cs.w)
-    const float d0 = g.x * cs.x + g.y * cs.y, d1 = -g.x * cs.y + g.y * cs.x;
-    const float d2 = g.z * cs.z + g.w * cs.w, d3 = -g.z * cs.w + g.w * cs.z;
-    acc.x = fmaf(d0, x.x * r, acc.x);
-    acc.y = fmaf(d1, x.y * r, acc.y);
-    acc.z = fmaf(d2, x.z * r, acc.z);
-    acc.w = fmaf(d3, x.w * r, acc.w);
-    const float g0 = w.x * d0, g1 = w.y * d1, g2 = w.z * d2, g3 = w.w * d3;
-    const float xg = warp_sum(x.x * g0 + x.y * g1 + x.z * g2 + x.w * g3);
-    const float c3 = r * r * r * xg * (1.0f / kD);
-    const float y0 = r * g0 - c3 * x.x, y1 = r * g1 - c3 * x.y, y2 = r * g2 - c3 * x.z, y3 = r * g3 - c3 * x.w;
-    const int64_t yoff = b * p.dq_sb + (int64_t)i * p.dq_ss + h * p.dq_sh + 4 * lane;
-    if (p.dq_f32) {
-      *reinterpret_cast<float4*>(static_cast<float*>(p.dq) + yoff) = make_float4(y0, y1, y2, y3);
-    } else {
-      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dq) + yoff) = make_uint2(pack_bf16(y0, y1), pack_bf16(y2, y3));
+    float4 gw[kPostRows];
+    float xg[kPostRows];
+#pragma unroll
+    for (int u = 0; u < kPostRows; ++u) {
+      const float4 gg = g[u], c4 = cs[u];
+      const float d0 = gg.x * c4.x + gg.y * c4.y, d1 = -gg.x * c4.y + gg.y * c4.x;
+      const float d2 = gg.z * c4.z + gg.w * c4.w, d3 = -gg.z * c4.w + gg.w * c4.z;
+      g[u] = make_float4(d0, d1, d2, d3);  // dy
+      gw[u] = make_float4(w.x * d0, w.y * d1, w.z * d2, w.w * d3);
+      xg[u] = x[u].x * gw[u].x + x[u].y * gw[u].y + x[u].z * gw[u].z + x[u].w * gw[u].w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < kPostRows; ++u) {
+        ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+        xg[u] += __shfl_xor_sync(0xffffffffu, xg[u], o);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPostRows; ++u) {
+      if (!valid[u]) continue;
+      const float r = rsqrtf(ss[u] * (1.0f / kD) + p.eps);
+      const float4 xx = x[u], dy = g[u], q = gw[u];
+      acc.x = fmaf(dy.x, xx.x * r, acc.x);
+      acc.y = fmaf(dy.y, xx.y * r, acc.y);
+      acc.z = fmaf(dy.z, xx.z * r, acc.z);
+      acc.w = fmaf(dy.w, xx.w * r, acc.w);
+      const float c3 = r * r * r * xg[u] * (1.0f / kD);
+      const float y0 = r * q.x - c3 * xx.x, y1 = r * q.y - c3 * xx.y, y2 = r * q.z - c3 * xx.z, y3 = r * q.w - c3 * xx.w;
+      if (p.dq_dt == kDtF32) {
+        *reinterpret_cast<float4*>(static_cast<float*>(p.dq) + yoff[u]) = make_float4(y0, y1, y2, y3);
+      } else {
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.dq) + yoff[u]) =
+            make_uint2(pack_dt(p.dq_dt, y0, y1), pack_dt(p.dq_dt, y2, y3));
+      }
     }
   }
   part[warp][lane] = acc;
@@ -197,8 +290,17 @@ __global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ 
   const int n = which ? p.n_k : p.n_q;
   float* scratch = p.scratch + (int64_t)which * gridDim.x * kD;
   const int p0 = blockIdx.x * kDwChunk;
+  const int p1 = min(n, p0 + kDwChunk);
   float acc = 0.f;
-  for (int q = p0; q < min(n, p0 + kDwChunk); ++q) acc += part[(int64_t)q * kD + tid];
+  int q = p0;
+  for (; q + 8 <= p1; q += 8) {  // loads of eight partials in flight, added in index order
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) v[u] = __ldcg(part + (int64_t)(q + u) * kD + tid);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc += v[u];
+  }
+  for (; q < p1; ++q) acc += __ldcg(part + (int64_t)q * kD + tid);
   scratch[(int64_t)blockIdx.x * kD + tid] = acc;
   __threadfence();
   __syncthreads();
@@ -252,7 +354,8 @@ cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
 
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
-  const int64_t blocks = (nrows * 32 + 255) / 256;
+  const int64_t warps = (nrows + kPreRows - 1) / kPreRows;
+  const int64_t blocks = (warps * 32 + 255) / 256;
   bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }

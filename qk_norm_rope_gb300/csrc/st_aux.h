@@ -50,11 +50,12 @@ struct ClassifyParams {
 struct PreParams {
   const void* o;
   int64_t o_sb, o_ss, o_sh;
-  int o_f32;
+  int o_dt;       // element type of O and dO (kDtBF16, kDtF16 or kDtF32)
   const void* dout;
   int64_t do_sb, do_ss, do_sh;
   float* delta;   // [B, H, Sq]
   float* dq_acc;  // [B, Sq, H, D]
+  unsigned* ctrl; // control words: the weight-gradient counters are cleared
   int B, H, Sq;
 };
 
@@ -67,7 +68,7 @@ struct PostParams {
   float eps;
   void* dq;
   int64_t dq_sb, dq_ss, dq_sh;
-  int dq_f32;
+  int dq_dt;
   float* dwq_part;  // [n_blocks, D]
   int B, H, Sq;
 };

@@ -1,6 +1,8 @@
-// Backward main kernel: one CTA per (key tile of 128 rows, head, batch), in
-// clusters of two CTAs over adjacent key tiles (kt0 = 2p, kt0 + 1) that walk
-// the same query tiles in lockstep. Query tiles are processed as two 64-query
+// Backward main kernel: one CTA per (key tile of 128 rows, K/V head, batch),
+// in clusters of two CTAs over adjacent key tiles (kt0 = 2p, kt0 + 1) that
+// walk the same query tiles in lockstep, for every query head that shares the
+// K/V head (grouped K/V heads: dK' and dV accumulate over the whole group in
+// TMEM, so dk and dv leave the epilogue final). Query tiles are processed as two 64-query
 // sub-tiles; per sub-tile, with Q' = RoPE(RMSNorm(q)) and K' the same for k
 // (bf16, 128B-swizzled operand tiles):
 //   S^T = K' Q'^T, dP^T = V dO^T                      (tensor core, TMEM)
@@ -40,6 +42,10 @@
 #include "st_kernels.h"
 #include "st_prologue.cuh"
 
+#ifndef ST_OPERAND_F16
+#define ST_OPERAND_F16 false  // this unit's 16-bit operand type: bf16 (st_bwd_f16.cu: fp16)
+#endif
+
 namespace st {
 
 namespace {
@@ -60,6 +66,8 @@ constexpr uint32_t kSubHalf = kSubBytes / 2;
 constexpr int kPeerRows = kSub / kCluster;                 // Q' rows produced per CTA per sub-tile
 constexpr uint32_t kPeerRowsBytes = kPeerRows * 128;       // those rows in one column half
 constexpr uint32_t kRBoxBytes = kSub * 32 * 4;             // one [64 queries][32 head dims] fp32 box
+constexpr int kBarIdEpi = 4, kEpiThreads = kComputeWarps * 32;  // named barrier of the epilogue warps
+constexpr uint32_t kBoxBytes = 128 * 128;                  // a [128 rows][128 bytes] TMA box
 
 // shared memory layout (offsets from the 1024-byte aligned dynamic base)
 constexpr uint32_t kOffK = 0;
@@ -91,6 +99,7 @@ enum {
   kBarDQ = kBarCDone + 2,                // + buffer: dQ'^T in TMEM (and every earlier MMA done)
   kBarBFree = kBarDQ + 2,                // + buffer: dQ'^T read out (128 arrivals)
   kBarFinal = kBarBFree + 2,             // abort path: all issued MMAs done
+  kBarEpi,                               // epilogue: raw k rows and (cos, sin) rows staged
   kNumBars
 };
 static_assert(kNumBars * 8 + 12 <= kBarBytes, "barrier area");
@@ -113,27 +122,43 @@ __device__ __forceinline__ uint8_t own_flag(const Common& c, int b, int h, int q
   return kTileMixed;
 }
 
-// The query tiles a cluster visits: [begin, begin + len), walked from a
-// rotated start so that the clusters of one head (which all add into the same
-// dQ rows) do not work on the same query tile at the same time.
+// What a cluster visits: for each query head h0 .. h0 + group - 1 that shares
+// its K/V head (grouped K/V heads; group = 1 otherwise), the query tiles
+// [begin, begin + len), walked from a rotated start so that the clusters of
+// one head (which all add into the same dQ rows) do not work on the same query
+// tile at the same time. A position is (g, mm): step mm of the walk of head
+// h0 + g; every role steps through it without divisions.
+struct WPos {
+  int g, mm;
+};
 struct QWalk {
-  int begin, len, rot;
-  __device__ __forceinline__ int qt(int m) const {
-    const int x = rot + m;
+  int begin, len, rot, h0, group;
+  __device__ __forceinline__ WPos start() const { return WPos{len > 0 ? 0 : group, 0}; }
+  __device__ __forceinline__ bool more(const WPos& p) const { return p.g < group; }
+  __device__ __forceinline__ WPos step(WPos p) const {
+    if (++p.mm == len) {
+      p.mm = 0;
+      ++p.g;
+    }
+    return p;
+  }
+  __device__ __forceinline__ int qt(const WPos& p) const {
+    const int x = rot + p.mm;
     return begin + (x >= len ? x - len : x);
   }
+  __device__ __forceinline__ int head(const WPos& p) const { return h0 + p.g; }
 };
 
-// Next walk position at or after m whose query tile either key tile of the
+// Next walk position at or after p whose query tile either key tile of the
 // cluster needs.
 template <int MK>
-__device__ __forceinline__ int next_pos(const Common& c, int b, int h, const QWalk& w, int m, int kt0) {
+__device__ __forceinline__ WPos next_pos(const Common& c, int b, const QWalk& w, WPos p, int kt0) {
   if constexpr (MK == kMaskBool) {
-    while (m < w.len && own_flag<MK>(c, b, h, w.qt(m), kt0) == kTileAllFalse &&
-           own_flag<MK>(c, b, h, w.qt(m), kt0 + 1) == kTileAllFalse)
-      ++m;
+    while (w.more(p) && own_flag<MK>(c, b, w.head(p), w.qt(p), kt0) == kTileAllFalse &&
+           own_flag<MK>(c, b, w.head(p), w.qt(p), kt0 + 1) == kTileAllFalse)
+      p = w.step(p);
   }
-  return m;
+  return p;
 }
 
 // Base-2 score of key j against query iq (general path): s*scale*log2e plus
@@ -174,9 +199,140 @@ __device__ __forceinline__ float score2_term(const Common& c, float s, float key
   return s2;
 }
 
+// Reduce-scatter over the warp: lane l returns the sum over all 32 lanes of
+// their v[l] (recursive halving; the order of the additions is fixed).
+// v is clobbered.
+__device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+    const bool up = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = up ? v[i] : v[i + w];
+      const float keep = up ? v[i + w] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+    }
+  }
+  return v[0];
+}
+
+// dK of key row j, shared by two threads: the thread of warp w holds head
+// dims [64 hh, 64 hh + 64) (hh = w / 4) of the row in its TMEM lane (the dK'
+// accumulator, the gradient of the rotated, normed row divided by the softmax
+// scale). With x the raw k row, r = 1 / sqrt(mean x^2 + eps), g = scale dK',
+// dy = R^T g (the rotation with sin negated) and g' = w dy:
+//   dk = r g' - (r^3 / D) x (x . g'),   dW_k gathers dy x r.
+// The raw row (bf16: the two 64-column halves of kOffK; fp32: four 32-column
+// boxes over kOffK..kOffV) and the row's fp32 (cos, sin) (four 32-float boxes
+// at kOffQ) were staged by TMA, 128B-swizzled. The two row sums (x.x, x.g')
+// are completed through `ex` in shared memory, between named barriers of the
+// eight epilogue warps. colsum[q] receives, in lane l, the sum of dy x r at
+// column 64 hh + 32 q + l over the warp's 32 rows.
+template <bool QKT, bool F16>
+__device__ __forceinline__ void dk_half_rows(const BwdParams& P, const uint8_t* sm, uint32_t tacc, bool have, int b,
+                                             int hk, int j, int r, int hh, bool key_ok, int lane, float* ex,
+                                             float (&colsum)[2]) {
+  const Common& c = P.c;
+  // the chunk (16 bytes) of this thread's half row holding dims 64 hh + 4 t .. +3 (fp32)
+  // or 64 hh + 8 t .. +7 (bf16)
+  auto x_chunk = [&](int t) -> const uint4* {
+    if constexpr (QKT) return reinterpret_cast<const uint4*>(sm + kOffK + hh * kHalfBytes + sw128_off(r, t));
+    return reinterpret_cast<const uint4*>(sm + kOffK + (2 * hh + (t >> 3)) * kBoxBytes + sw128_off(r, t & 7));
+  };
+  // (cos, sin) of pairs 32 hh + 2 t, +1
+  auto tab_chunk = [&](int t) -> float4 {
+    return *reinterpret_cast<const float4*>(sm + kOffQ + (2 * hh + (t >> 3)) * kBoxBytes + sw128_off(r, t & 7));
+  };
+  // eight consecutive dims d0 .. d0 + 7 of the half (d0 a multiple of 8)
+  auto load_x8 = [&](int d0, float (&x8)[8]) {
+    if constexpr (QKT) {
+      const uint4 u = *x_chunk(d0 >> 3);
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x8[2 * e] = lo16<F16>(w[e]);
+        x8[2 * e + 1] = hi16<F16>(w[e]);
+      }
+    } else {
+      const float4 a = *reinterpret_cast<const float4*>(x_chunk(d0 >> 2));
+      const float4 bq = *reinterpret_cast<const float4*>(x_chunk((d0 >> 2) + 1));
+      x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w; x8[4] = bq.x; x8[5] = bq.y; x8[6] = bq.z; x8[7] = bq.w;
+    }
+  };
+  // the half row's sum of squares, completed with the partner's half
+  float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll
+  for (int d0 = 0; d0 < 64; d0 += 8) {
+    float x8[8];
+    load_x8(d0, x8);
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      ss0 = fmaf(x8[e], x8[e], ss0);
+      ss1 = fmaf(x8[e + 1], x8[e + 1], ss1);
+    }
+  }
+  ex[hh * kTile + r] = ss0 + ss1;
+  named_bar(kBarIdEpi, kEpiThreads);
+  const float rr = rsqrtf((ex[r] + ex[kTile + r]) * (1.0f / kD) + c.eps);
+  const float sc = c.scale;
+  const float4* w4 = reinterpret_cast<const float4*>(c.wk + 64 * hh);
+  float xg = 0.f;
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    if (pass == 1) {  // x . g' over the whole row
+      ex[2 * kTile + hh * kTile + r] = xg;
+      named_bar(kBarIdEpi, kEpiThreads);
+      xg = ex[2 * kTile + r] + ex[3 * kTile + r];
+    }
+    const float c3 = rr * rr * rr * xg * (1.0f / kD);
+#pragma unroll 1
+    for (int q = 0; q < 2; ++q) {
+      uint32_t v[32];
+      if (have) {
+        tmem_ld32(tacc + 32 * q, v);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 32; ++t) v[t] = 0u;
+      }
+      float u[32];
+#pragma unroll
+      for (int c8 = 0; c8 < 4; ++c8) {
+        const int d0 = 32 * q + 8 * c8;  // dims d0 .. d0 + 7 of the half: pairs d0/2 .. d0/2 + 3
+        float x8[8];
+        load_x8(d0, x8);
+        const float4 t0 = tab_chunk(d0 >> 2), t1 = tab_chunk((d0 >> 2) + 1);
+        const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        const float4 wa = __ldg(w4 + (d0 >> 2)), wb = __ldg(w4 + (d0 >> 2) + 1);
+        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 8 * c8 + 2 * e;
+          const float g0 = __uint_as_float(v[t]) * sc, g1 = __uint_as_float(v[t + 1]) * sc;
+          const float cc = cs[2 * e], sn = cs[2 * e + 1];
+          const float dy0 = fmaf(g0, cc, g1 * sn), dy1 = fmaf(g1, cc, -g0 * sn);
+          const float gw0 = wv[2 * e] * dy0, gw1 = wv[2 * e + 1] * dy1;
+          if (pass == 0) {
+            xg = fmaf(x8[2 * e], gw0, fmaf(x8[2 * e + 1], gw1, xg));
+            u[t] = key_ok ? dy0 * x8[2 * e] * rr : 0.f;
+            u[t + 1] = key_ok ? dy1 * x8[2 * e + 1] * rr : 0.f;
+          } else {
+            u[t] = fmaf(rr, gw0, -c3 * x8[2 * e]);
+            u[t + 1] = fmaf(rr, gw1, -c3 * x8[2 * e + 1]);
+          }
+        }
+      }
+      if (pass == 0) {
+        colsum[q] = warp_reduce_scatter32(u, lane);
+      } else if (key_ok) {
+        store_chunk32(P.dk, b * P.dk_sb + (int64_t)j * P.dk_ss + hk * P.dk_sh, P.dk_dt, 2 * hh + q, u);
+      }
+    }
+  }
+}
+
 // ELEM: the mask varies along the queries (per-element terms); a mask that is
 // broadcast over the queries reduces to one term per key.
-template <int MK, bool CAUSAL, bool QKT, bool ELEM>
+template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -193,7 +349,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 
   const Common& c = P.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
-  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;  // key tile, K/V head, batch
   const int kt0 = kt & ~1;
 
   if (warp == kWarpMma) {
@@ -221,6 +377,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       mbar_init(&bars[kBarBFree + u], kDrainWarps * 32);
     }
     mbar_init(&bars[kBarFinal], 1);
+    mbar_init(&bars[kBarEpi], 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -230,10 +387,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     tma_prefetch_desc(&P.tmap_v);
     tma_prefetch_desc(&P.tmap_do);
     tma_prefetch_desc(&P.tmap_dq);
-    if constexpr (QKT) {
-      tma_prefetch_desc(&P.tmap_q);
-      tma_prefetch_desc(&P.tmap_k);
-    }
+    tma_prefetch_desc(&P.tmap_k);
+    tma_prefetch_desc(&P.tmap_tab_k);
+    if constexpr (QKT) tma_prefetch_desc(&P.tmap_q);
   }
   tc_fence_before();
   __syncthreads();
@@ -247,7 +403,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   W.begin = CAUSAL ? min(c.nQt, kt0) : 0;
   W.len = c.nQt - W.begin;
   W.rot = W.len > 0 ? static_cast<int>((static_cast<int64_t>(kt0 / 2) * W.len) / ((c.nKt + 1) / 2)) : 0;
-  int useful = 0;  // query tiles this CTA's own key tile needed (compute warps)
+  W.h0 = hk * c.group;
+  W.group = c.group;
+  int useful = 0;  // (query head, query tile) pairs this CTA's own key tile needed (compute warps)
 
   if (warp < kComputeWarps) {
     // ------------------------------------------------------------ compute
@@ -256,22 +414,30 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     const int j = kt * kTile + r;
     const bool key_ok = j < c.Skv;
     const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
-    // masks that do not depend on the query row: one term per key for the CTA
-    float key_term = 0.f;
+    // masks that do not depend on the query row: one term per key and head
     const bool mask_bcast_q = MK != kMaskNone && c.m_sq == 0;
-    if (mask_bcast_q && key_ok) {
-      const int64_t off = b * c.m_sb + h * c.m_sh + j;
-      if constexpr (MK == kMaskBool) key_term = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0.f : -INFINITY;
-      else if constexpr (MK == kMaskF32) key_term = __ldg(static_cast<const float*>(c.mask) + off) * kLog2e;
-      else if constexpr (MK == kMaskBF16) key_term = __bfloat162float(static_cast<const __nv_bfloat16*>(c.mask)[off]) * kLog2e;
-    }
-    if (!key_ok) key_term = -INFINITY;
+    auto key_term_of = [&](int h) {
+      float t = 0.f;
+      if (mask_bcast_q && key_ok) {
+        const int64_t off = b * c.m_sb + h * c.m_sh + j;
+        if constexpr (MK == kMaskBool) t = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0.f : -INFINITY;
+        else if constexpr (MK == kMaskF32) t = __ldg(static_cast<const float*>(c.mask) + off) * kLog2e;
+        else if constexpr (MK == kMaskBF16) t = __bfloat162float(static_cast<const __nv_bfloat16*>(c.mask)[off]) * kLog2e;
+      }
+      return key_ok ? t : -INFINITY;
+    };
+    int key_h = W.h0;
+    float key_term = key_term_of(key_h);
     const float sc = c.scale_log2;
     const int q0 = 32 * hq;  // this warp's first query of a sub-tile
     bool ok = true;
     int n = 0;
-    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); ok && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
-      const int qt = W.qt(m);
+    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+      const int qt = W.qt(m), h = W.head(m);
+      if (h != key_h) {
+        key_h = h;
+        key_term = key_term_of(h);
+      }
       const uint8_t flag = own_flag<MK>(c, b, h, qt, kt);
       useful += (flag != kTileAllFalse && (!CAUSAL || qt >= kt)) ? 1 : 0;
       for (int s = 0; s < 2; ++s, ++n) {
@@ -302,8 +468,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
               const float2 x01 = __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4]), __uint_as_float(sv[4 * v4 + 1])), sc2, c01);
               const float2 x23 =
                   __ffma2_rn(make_float2(__uint_as_float(sv[4 * v4 + 2]), __uint_as_float(sv[4 * v4 + 3])), sc2, c23);
-              pw[2 * v4] = pack_bf16(ex2(x01.x), ex2(x01.y));
-              pw[2 * v4 + 1] = pack_bf16(ex2(x23.x), ex2(x23.y));
+              pw[2 * v4] = pack16<F16>(ex2(x01.x), ex2(x01.y));
+              pw[2 * v4 + 1] = pack16<F16>(ex2(x23.x), ex2(x23.y));
             }
           } else if constexpr (!ELEM) {
 #pragma unroll
@@ -316,7 +482,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
                                                     flag, mask_bcast_q);
                 p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
               }
-              pw[t2] = pack_bf16(p2[0], p2[1]);
+              pw[t2] = pack16<F16>(p2[0], p2[1]);
             }
           } else {
             // per-element mask terms of the 32 queries, 16 at a time (loads pinned)
@@ -350,7 +516,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
                   const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mterm, iq0 + q0 + t, j, flag);
                   p2[e] = ex2(s2 - st_lse[q0 + t]);
                 }
-                pw[8 * hh + t2] = pack_bf16(p2[0], p2[1]);
+                pw[8 * hh + t2] = pack16<F16>(p2[0], p2[1]);
               }
             }
           }
@@ -374,8 +540,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
             for (int e = 0; e < 4; ++e) {
               const uint32_t pp = pw[4 * u + e];
               const float2 dp = make_float2(__uint_as_float(dpv[8 * u + 2 * e]), __uint_as_float(dpv[8 * u + 2 * e + 1]));
-              const float2 ds = __fmul2_rn(make_float2(bf16_lo(pp), bf16_hi(pp)), __fadd2_rn(dp, ndl[e]));
-              out[e] = pack_bf16(ds.x, ds.y);
+              const float2 ds = __fmul2_rn(make_float2(lo16<F16>(pp), hi16<F16>(pp)), __fadd2_rn(dp, ndl[e]));
+              out[e] = pack16<F16>(ds.x, ds.y);
             }
             *reinterpret_cast<uint4*>(dsb + sw128_off(r, 4 * hq + u)) = make_uint4(out[0], out[1], out[2], out[3]);
           }
@@ -386,30 +552,62 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         mbar_arrive(&bars[kBarCDone + bf]);
       }
     }
-    // ---- epilogue: warps of query half 0 write dV, half 1 scale * dK' (fp32;
-    // the inverse rotation and the RMSNorm backward run in a row kernel after)
+    // ---- epilogue of the eight compute warps: warp w holds key rows
+    // 32 (w % 4) .. (its TMEM lanes) and head dims [64 hq, 64 hq + 64) of dV
+    // and dK'. Once every MMA has completed, the K tile and the Q' ring are
+    // free: the raw k rows and the tile's fp32 (cos, sin) rows are staged
+    // there by TMA while dV is written; then dk (inverse rotation + RMSNorm
+    // backward) and the CTA's partial sums of the k norm-weight gradient.
     if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
-    if (ok) {
+    // one decision for the eight warps (they share named barriers below)
+    if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok)) {
       tc_fence_after();
-      const uint32_t tacc = tmem + (hq == 0 ? 256 : 384) + lanebits;
-      const int64_t off = hq == 0 ? b * P.dv_sb + (int64_t)j * P.dv_ss + h * P.dv_sh
-                                  : (((int64_t)b * c.Skv + j) * c.H + h) * kD;
-      const float mul = hq == 0 ? 1.f : c.scale;
-#pragma unroll 1
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t v[32];
-        if (n > 0) {
-          tmem_ld32(tacc + 32 * q4, v);
+      if (tid == 0 && !phantom) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars[kBarEpi], (QKT ? kTileBytes : 2 * kTileBytes) + 4 * kBoxBytes);
+        const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
+        if constexpr (QKT) {
+          tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarEpi], 0, y, z, b);
+          tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarEpi], 64, y, z, b);
         } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = 0u;
+          for (int x = 0; x < 4; ++x) tma_load_4d(sm + kOffK + x * kBoxBytes, &P.tmap_k, &bars[kBarEpi], 32 * x, y, z, b);
         }
-        float y[32];
+        const int trow = (c.tab_k_sb != 0 ? b * c.Skv : 0) + kt * kTile;
 #pragma unroll
-        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(v[t]) * mul;
-        if (key_ok) {
-          if (hq == 0) store_chunk32(P.dv, off, P.dv_f32, q4, y);
-          else store_chunk32(P.dk_acc, off, 1, q4, y);
+        for (int x = 0; x < 4; ++x) tma_load_2d(sm + kOffQ + x * kBoxBytes, &P.tmap_tab_k, &bars[kBarEpi], 32 * x, trow);
+      }
+      {
+        const uint32_t tacc = tmem + 256 + lanebits + 64 * hq;
+        const int64_t off = b * P.dv_sb + (int64_t)j * P.dv_ss + hk * P.dv_sh;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          uint32_t v[32];
+          if (n > 0) {
+            tmem_ld32(tacc + 32 * q, v);
+          } else {
+#pragma unroll
+            for (int t = 0; t < 32; ++t) v[t] = 0u;
+          }
+          float y[32];
+#pragma unroll
+          for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(v[t]);
+          if (key_ok) store_chunk32(P.dv, off, P.dv_dt, 2 * hq + q, y);
+        }
+      }
+      if (!phantom &&
+          !named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
+        float* ex = reinterpret_cast<float*>(sm + kOffDS);  // the dS buffers are idle: row-sum exchange
+        float* red = ex + 4 * kTile;                          // and the four row groups' column sums
+        float colsum[2];
+        dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq, key_ok, lane_id, ex,
+                          colsum);
+#pragma unroll
+        for (int q = 0; q < 2; ++q) red[qd * kD + 64 * hq + 32 * q + lane_id] = colsum[q];
+        named_bar(kBarIdEpi, kEpiThreads);
+        if (tid < kD) {  // column tid, the row groups added in a fixed order
+          const float sum = ((red[tid] + red[kD + tid]) + red[2 * kD + tid]) + red[3 * kD + tid];
+          P.dwk_part[(((int64_t)b * c.Hkv + hk) * c.nKt + kt) * kD + tid] = sum;
         }
       }
     }
@@ -429,8 +627,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     const uint32_t chunk = static_cast<uint32_t>(lane_id) >> 2, word = (lane_id & 3) * 4;
     int n = 0;
     bool ok = true;
-    for (int m = next_pos<MK>(c, b, h, W, 0, kt0); ok && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
-      const int qt = W.qt(m);
+    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+      const int qt = W.qt(m), h = W.head(m);
       for (int s = 0; s < 2; ++s, ++n) {
         const int bf = n & 1;
         if (!(ok = wait_bar_warp(&bars[kBarDQ + bf], (n >> 1) & 1, abort_flag, budget))) break;
@@ -472,9 +670,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         const int jj = kt * kTile + row;
         if constexpr (QKT) {
           if (jj < c.Skv)  // rows past S_kv stay TMA zeros
-            rope_norm_inplace(sm + kOffK, row, c.wk, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)jj * kPairs);
+            rope_norm_inplace<F16>(sm + kOffK, row, c.wk, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)jj * kPairs);
         } else if (jj < c.Skv) {
-          rope_norm_global(c.k.p, b * c.k.sb + (int64_t)jj * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps,
+          rope_norm_global<F16>(c.k.p, b * c.k.sb + (int64_t)jj * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
                            c.tab_k + b * c.tab_k_sb + (int64_t)jj * kPairs, sm + kOffK, row);
         } else {
           zero_row(sm + kOffK, row);
@@ -502,10 +700,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     const int part = (((lane_id >> 2) & 1) << 2) | (lane_id >> 3), pw = warp - kWarpProl0;
     const int ra = kPeerRows * static_cast<int>(crank) + 4 * pw + (lane_id & 3), rb = ra + 16;
     const __half2* tab16 = c.tab16_q + b * c.tab_q_sb;
-    OctRow rp[2];
+    OctRow<F16> rp[2];
     // LSE and Delta of row p of the current sub-tile, loaded one sub-tile ahead
     float lse_c = -INFINITY, dl_c = 0.f;
-    auto load_stats = [&](int iq0) {
+    auto load_stats = [&](int iq0, int h) {
       lse_c = -INFINITY;
       dl_c = 0.f;
       if (p < kSub && iq0 + p < c.Sq) {
@@ -514,19 +712,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         dl_c = ldg_nc_f32(P.delta + ri);
       }
     };
-    int m = next_pos<MK>(c, b, h, W, 0, kt0), s = 0;
-    if (m < W.len) load_stats(W.qt(m) * kTile);
+    WPos m = next_pos<MK>(c, b, W, W.start(), kt0);
+    int s = 0;
+    if (W.more(m)) load_stats(W.qt(m) * kTile, W.head(m));
     if constexpr (QKT) {
-      if (m < W.len) {
+      if (W.more(m)) {
         const int i0 = W.qt(m) * kTile;
         if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
         if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
       }
     }
-    for (int n = 0; ok && m < W.len; ++n) {
-      const int qt = W.qt(m);
+    for (int n = 0; ok && W.more(m); ++n) {
+      const int qt = W.qt(m), h = W.head(m);
       // the next sub-tile of the walk
-      const int m_next = s == 0 ? m : next_pos<MK>(c, b, h, W, m + 1, kt0), s_next = s ^ 1;
+      const WPos m_next = s == 0 ? m : next_pos<MK>(c, b, W, W.step(m), kt0);
+      const int s_next = s ^ 1;
       const int sq = n % kQStages;
       uint8_t* stage = sm + kOffQ + sq * kSubBytes;
       const int iq0 = qt * kTile + kSub * s;
@@ -538,8 +738,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       if constexpr (QKT) {
         if (wait_bar_warp(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) {
           // rows past S_q stay TMA zeros
-          OctRow::finish2(rp[0], rp[1], stage, ra, rb, part, sWq, c.eps, iq0 + ra < c.Sq, iq0 + rb < c.Sq, kSubHalf);
-          if (m_next < W.len) {
+          OctRow<F16>::finish2(rp[0], rp[1], stage, ra, rb, part, sWq, c.eps, iq0 + ra < c.Sq, iq0 + rb < c.Sq, kSubHalf);
+          if (W.more(m_next)) {
             const int i0 = W.qt(m_next) * kTile + kSub * s_next;
             if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
             if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
@@ -553,7 +753,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
           const int row = kPeerRows * static_cast<int>(crank) + (p >> 2);
           const bool valid = iq0 + row < c.Sq;
           const int i = valid ? iq0 + row : 0;
-          rope_norm_global_quad(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
+          rope_norm_global_quad<F16>(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.dt, c.wq, c.eps,
                                 c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, stage, row, p & 3, valid, kSubHalf);
         }
       }
@@ -561,7 +761,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         stat[sq * 2 * kSub + p] = l2;
         stat[sq * 2 * kSub + kSub + p] = dl;
       }
-      if (m_next < W.len) load_stats(W.qt(m_next) * kTile + kSub * s_next);
+      if (W.more(m_next)) load_stats(W.qt(m_next) * kTile + kSub * s_next, W.head(m_next));
       // this CTA's 32 rows are final: one bulk copy per column half to the
       // same offsets of the peer's stage, completing on its Q' barrier
       fence_proxy_async_smem();
@@ -584,12 +784,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     if (lane_id == 0) {
       if (!phantom) {
         if constexpr (QKT) {
-          const int y = P.k_s_first ? kt * kTile : h, z = P.k_s_first ? h : kt * kTile;
+          const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
           mbar_arrive_expect_tx(&bars[kBarKRaw], kTileBytes);
           tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarKRaw], 0, y, z, b);
           tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarKRaw], 64, y, z, b);
         }
-        const int vy = P.v_s_first ? kt * kTile : h, vz = P.v_s_first ? h : kt * kTile;
+        const int vy = P.v_s_first ? kt * kTile : hk, vz = P.v_s_first ? hk : kt * kTile;
         mbar_arrive_expect_tx(&bars[kBarVFull], kTileBytes);
         tma_load_4d(sm + kOffV, &P.tmap_v, &bars[kBarVFull], 0, vy, vz, b);
         tma_load_4d(sm + kOffV + kHalfBytes, &P.tmap_v, &bars[kBarVFull], 64, vy, vz, b);
@@ -599,8 +799,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       int n = 0, q_issued = 0;
       bool stop = false;
       if constexpr (QKT) {
-        for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
-          const int qt = W.qt(m);
+        for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+          const int qt = W.qt(m), h = W.head(m);
           for (int s = 0; s < 2; ++s, ++n) {  // this CTA's 32 raw rows of the sub-tile
             const int sq = n % kQStages;
             if (n >= kQStages &&
@@ -632,8 +832,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     if (lane_id == 0) {
       int n = 0, do_issued = 0;
       bool stop = false;
-      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); !stop && m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) {
-        const int qt = W.qt(m);
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+        const int qt = W.qt(m), h = W.head(m);
         for (int s = 0; s < 2; ++s, ++n) {
           const int sd = n % kDOStages;
           if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) {
@@ -655,9 +855,9 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     if (lane_id == 0) {
-      constexpr uint32_t idesc_sdp = idesc_bf16(128, kSub, 0, 0);  // S^T, dP^T: N = 64 queries
-      constexpr uint32_t idesc_kv = idesc_bf16(128, 128, 0, 1);    // dV, dK': N = 128 head dims
-      constexpr uint32_t idesc_q = idesc_bf16(128, kSub, 1, 1);    // dQ'^T = K'^T dS^T
+      constexpr uint32_t idesc_sdp = idesc16(F16, 128, kSub, 0, 0);  // S^T, dP^T: N = 64 queries
+      constexpr uint32_t idesc_kv = idesc16(F16, 128, 128, 0, 1);    // dV, dK': N = 128 head dims
+      constexpr uint32_t idesc_q = idesc16(F16, 128, kSub, 1, 1);    // dQ'^T = K'^T dS^T
       const uint64_t dKk = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
       const uint64_t dKm = sdesc_sw128(smem_u32(sm + kOffK), kHalfBytes, 1024);
       const uint64_t dVk = sdesc_sw128(smem_u32(sm + kOffV), 16, 1024);
@@ -669,7 +869,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       const uint64_t dSm0 = sdesc_sw128(smem_u32(sm + kOffDS), kSubHalf, 1024);
       const uint32_t tdV = tmem + 256, tdK = tmem + 384;
       int nsub = 0;  // sub-tiles in the walk
-      for (int m = next_pos<MK>(c, b, h, W, 0, kt0); m < W.len; m = next_pos<MK>(c, b, h, W, m + 1, kt0)) nsub += 2;
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) nsub += 2;
       auto issue_s = [&](int n) -> bool {  // S^T(n) into its half of buffer n % 2
         const int sq = n % kQStages;
         if (!wait_bar(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
@@ -743,8 +943,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   __syncthreads();
   if (!*abort_flag) {
     if (!phantom && tid == 0) {
-      atomicAdd(c.counters + kCtrTilesSkipped, (unsigned long long)(c.nQt - useful));
-      atomicAdd(c.counters + kCtrTilesTotal, (unsigned long long)c.nQt);
+      atomicAdd(c.counters + kCtrTilesSkipped, (unsigned long long)(c.group * c.nQt - useful));
+      atomicAdd(c.counters + kCtrTilesTotal, (unsigned long long)(c.group * c.nQt));
     }
   } else if (tid == 0) {
     record_timeout(c);
@@ -759,42 +959,45 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 
 }  // namespace
 
-template <int MK, bool CAUSAL, bool QKT, bool ELEM>
+template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
 cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
-  auto kern = bwd_kernel<MK, CAUSAL, QKT, ELEM>;
-  static unsigned configured = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured & (1u << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kBwdSmem);
-    if (e != cudaSuccess) return e;
-    configured |= 1u << (dev & 31);
-  }
-  dim3 grid((p.c.nKt + kCluster - 1) / kCluster * kCluster, p.c.H, p.c.B);  // whole clusters
+  auto kern = bwd_kernel<MK, CAUSAL, QKT, ELEM, F16>;
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = opt_in_smem(kern, kBwdSmem, configured);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.c.nKt + kCluster - 1) / kCluster * kCluster, p.c.Hkv, p.c.B);  // whole clusters
   kern<<<grid, kBwdThreads, kBwdSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <bool QKT>
+template <bool QKT, bool F16>
 cudaError_t launch_bwd_q(const BwdParams& p, cudaStream_t stream) {
-  if (p.c.causal) return launch_bwd_t<kMaskNone, true, QKT, false>(p, stream);  // masks and causal never combine
+  if (p.c.causal) return launch_bwd_t<kMaskNone, true, QKT, false, F16>(p, stream);  // masks and causal never combine
   const bool elem = p.c.m_sq != 0;  // the mask varies along the queries
   switch (p.c.mask_kind) {
     case kMaskBool:
-      return elem ? launch_bwd_t<kMaskBool, false, QKT, true>(p, stream) : launch_bwd_t<kMaskBool, false, QKT, false>(p, stream);
+      return elem ? launch_bwd_t<kMaskBool, false, QKT, true, F16>(p, stream)
+                  : launch_bwd_t<kMaskBool, false, QKT, false, F16>(p, stream);
     case kMaskF32:
-      return elem ? launch_bwd_t<kMaskF32, false, QKT, true>(p, stream) : launch_bwd_t<kMaskF32, false, QKT, false>(p, stream);
+      return elem ? launch_bwd_t<kMaskF32, false, QKT, true, F16>(p, stream)
+                  : launch_bwd_t<kMaskF32, false, QKT, false, F16>(p, stream);
     case kMaskBF16:
-      return elem ? launch_bwd_t<kMaskBF16, false, QKT, true>(p, stream) : launch_bwd_t<kMaskBF16, false, QKT, false>(p, stream);
-    default: return launch_bwd_t<kMaskNone, false, QKT, false>(p, stream);
+      return elem ? launch_bwd_t<kMaskBF16, false, QKT, true, F16>(p, stream)
+                  : launch_bwd_t<kMaskBF16, false, QKT, false, F16>(p, stream);
+    default: return launch_bwd_t<kMaskNone, false, QKT, false, F16>(p, stream);
   }
 }
 
 // Kernels are specialised on the mask kind, causal masking, whether q/k are
-// staged by TMA and whether the mask varies along the queries, so that each
-// carries only its own code.
-cudaError_t launch_bwd(const BwdParams& p, cudaStream_t stream) {
-  return p.qk_tma ? launch_bwd_q<true>(p, stream) : launch_bwd_q<false>(p, stream);
+// staged by TMA, whether the mask varies along the queries and the 16-bit
+// operand type, so that each carries only its own code. This translation
+// unit holds one operand type (ST_OPERAND_F16).
+#if ST_OPERAND_F16
+cudaError_t launch_bwd_f16(const BwdParams& p, cudaStream_t stream) {
+#else
+cudaError_t launch_bwd_bf16(const BwdParams& p, cudaStream_t stream) {
+#endif
+  return p.qk_tma ? launch_bwd_q<true, ST_OPERAND_F16>(p, stream) : launch_bwd_q<false, ST_OPERAND_F16>(p, stream);
 }
 
 }  // namespace st

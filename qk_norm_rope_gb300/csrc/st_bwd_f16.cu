@@ -1,0 +1,5 @@
+// The backward kernels with fp16 MMA operands (fp16 v and dO, and fp16 or
+// fp32 q/k): the same source as st_bwd.cu, compiled as its own translation
+// unit.
+#define ST_OPERAND_F16 true
+#include "st_bwd.cu"

@@ -26,10 +26,13 @@ enum { kCtrMaskAllTrue = 0, kCtrTilesSkipped = 1, kCtrTilesTotal = 2, kCtrTimeou
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Element types of rows in global memory (the codes of st_dtype).
+enum : int { kDtBF16 = 0, kDtF16 = 1, kDtF32 = 2 };
+
 struct RowTensor {  // [B, S, H, D] view with unit stride on D
   const void* p;
   int64_t sb, ss, sh;
-  int is_f32;
+  int dt;  // kDtBF16, kDtF16 or kDtF32
 };
 
 struct Common {
@@ -48,9 +51,11 @@ struct Common {
   const uint8_t* flags;        // bool masks: tile classes
   int64_t f_sb, f_sh, f_sq;    // strides of the flag array (0 on broadcast dims)
   int causal;
+  int f16;           // MMA operand type: 0 bf16, 1 fp16 (v's dtype; q/k of 16 bits have it too)
   float scale;       // softmax scale
   float scale_log2;  // scale * log2(e)
   int B, H, Sq, Skv, nQt, nKt;
+  int Hkv, group;                 // K/V heads; query heads per K/V head (H / Hkv)
   unsigned* status;               // device status word
   unsigned long long* counters;   // device counters
   long long wait_budget;          // clock64 cycles per bounded wait
@@ -59,14 +64,14 @@ struct Common {
 struct FwdParams {
   Common c;
   CUtensorMap tmap_v;  // V as a 4-D tiled map, 128B swizzle, box 64 x 128 keys
-  CUtensorMap tmap_q;  // raw q / k rows (bf16 only; see qk_tma)
+  CUtensorMap tmap_q;  // raw q / k rows (16-bit only; see qk_tma)
   CUtensorMap tmap_k;
   int v_s_first;       // map dims are (d, s, h, b) instead of (d, h, s, b)
   int q_s_first, k_s_first;
-  int qk_tma;          // 1: q and k are bf16 and staged by TMA, normalised in place
+  int qk_tma;          // 1: q and k are 16-bit and staged by TMA, normalised in place
   void* o;
   int64_t o_sb, o_ss, o_sh;
-  int o_f32;
+  int o_dt;
   float* lse;  // [B, H, Sq]
 };
 
@@ -74,8 +79,9 @@ struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
   CUtensorMap tmap_do;  // dO rows, 64-row boxes
-  CUtensorMap tmap_q;   // raw q rows, 32-row boxes (bf16 only; see qk_tma)
-  CUtensorMap tmap_k;   // raw k rows, 128-row boxes (bf16 only)
+  CUtensorMap tmap_q;   // raw q rows, 32-row boxes (16-bit only; see qk_tma)
+  CUtensorMap tmap_k;   // raw k rows, 128-row boxes (16-bit: 64 columns; fp32: 32 columns, epilogue only)
+  CUtensorMap tmap_tab_k;  // the fp32 (cos, sin) table of the keys as [Bt_k * Skv, 128] floats, 32 x 128 boxes
   CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 64 rows (reduce target)
   int v_s_first, do_s_first, q_s_first, k_s_first;
   int qk_tma;
@@ -85,14 +91,43 @@ struct BwdParams {
   const float* delta;  // [B, H, Sq]
   float* dq_acc;       // [B, Sq, H, D] fp32, zeroed: scale * dS K' (gradient of the rotated, normed q)
                        // (TMA reduce target through tmap_dq)
-  float* dk_acc;       // [B, Skv, H, D] fp32: scale * dS^T Q' (gradient of the rotated, normed k)
   void* dv;
   int64_t dv_sb, dv_ss, dv_sh;
-  int dv_f32;
+  int dv_dt;
+  void* dk;            // dk, finished in the kernel's epilogue (inverse rotation + RMSNorm backward)
+  int64_t dk_sb, dk_ss, dk_sh;
+  int dk_dt;
+  float* dwk_part;     // [B, Hkv, nKt, D]: per-CTA partial sums of the k norm-weight gradient
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float f16_lo(uint32_t w) { return __half2float(__ushort_as_half(static_cast<unsigned short>(w))); }
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(w >> 16)));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// The 16-bit operand type of the tensor-core MMAs: bf16 (F16 = false) or fp16
+// (F16 = true). Element 2i of a packed word is in its low half.
+template <bool F16>
+__device__ __forceinline__ float lo16(uint32_t w) {
+  if constexpr (F16) return f16_lo(w);
+  else return bf16_lo(w);
+}
+template <bool F16>
+__device__ __forceinline__ float hi16(uint32_t w) {
+  if constexpr (F16) return f16_hi(w);
+  else return bf16_hi(w);
+}
+template <bool F16>
+__device__ __forceinline__ uint32_t pack16(float lo, float hi) {
+  if constexpr (F16) return pack_f16(lo, hi);
+  else return pack_bf16(lo, hi);
+}
 
 __device__ __forceinline__ void zero_row(uint8_t* tile, int row, uint32_t half = kHalfBytes) {
 #pragma unroll
@@ -100,31 +135,42 @@ __device__ __forceinline__ void zero_row(uint8_t* tile, int row, uint32_t half =
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) = make_uint4(0, 0, 0, 0);
 }
 
-// Stores elements [32*q4, 32*q4 + 32) of a row to a bf16 or fp32 destination.
-__device__ __forceinline__ void store_chunk32(void* base, int64_t off, int is_f32, int q4, const float (&y)[32]) {
-  if (is_f32) {
+// Two floats as a packed word of a 16-bit row type (kDtBF16 or kDtF16).
+__device__ __forceinline__ uint32_t pack_dt(int dt, float lo, float hi) {
+  return dt == kDtF16 ? pack_f16(lo, hi) : pack_bf16(lo, hi);
+}
+
+// Stores elements [32*q4, 32*q4 + 32) of a row to a bf16, fp16 or fp32
+// destination (dt).
+__device__ __forceinline__ void store_chunk32(void* base, int64_t off, int dt, int q4, const float (&y)[32]) {
+  if (dt == kDtF32) {
     float4* p = reinterpret_cast<float4*>(static_cast<float*>(base) + off) + 8 * q4;
 #pragma unroll
     for (int c = 0; c < 8; ++c) p[c] = make_float4(y[4 * c], y[4 * c + 1], y[4 * c + 2], y[4 * c + 3]);
   } else {
-    uint4* p = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(base) + off) + 4 * q4;
+    uint4* p = reinterpret_cast<uint4*>(static_cast<uint16_t*>(base) + off) + 4 * q4;
 #pragma unroll
     for (int c = 0; c < 4; ++c)
-      p[c] = make_uint4(pack_bf16(y[8 * c], y[8 * c + 1]), pack_bf16(y[8 * c + 2], y[8 * c + 3]),
-                        pack_bf16(y[8 * c + 4], y[8 * c + 5]), pack_bf16(y[8 * c + 6], y[8 * c + 7]));
+      p[c] = make_uint4(pack_dt(dt, y[8 * c], y[8 * c + 1]), pack_dt(dt, y[8 * c + 2], y[8 * c + 3]),
+                        pack_dt(dt, y[8 * c + 4], y[8 * c + 5]), pack_dt(dt, y[8 * c + 6], y[8 * c + 7]));
   }
 }
 
-// Loads elements [8c, 8c+8) of the row at element offset `off`.
-__device__ __forceinline__ void load_chunk8(const void* base, int64_t off, int is_f32, int c, float (&v)[8]) {
-  if (is_f32) {
+// Loads elements [8c, 8c+8) of the row at element offset `off` (bf16, fp16
+// or fp32 source, dt).
+__device__ __forceinline__ void load_chunk8(const void* base, int64_t off, int dt, int c, float (&v)[8]) {
+  if (dt == kDtF32) {
     const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(base) + off) + 2 * c;
     const float4 a = __ldg(p), b = __ldg(p + 1);
     v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
   } else {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(base) + off) + c);
-    v[0] = bf16_lo(u.x); v[1] = bf16_hi(u.x); v[2] = bf16_lo(u.y); v[3] = bf16_hi(u.y);
-    v[4] = bf16_lo(u.z); v[5] = bf16_hi(u.z); v[6] = bf16_lo(u.w); v[7] = bf16_hi(u.w);
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(base) + off) + c);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[2 * e] = dt == kDtF16 ? f16_lo(w[e]) : bf16_lo(w[e]);
+      v[2 * e + 1] = dt == kDtF16 ? f16_hi(w[e]) : bf16_hi(w[e]);
+    }
   }
 }
 
@@ -185,6 +231,13 @@ __device__ __forceinline__ bool named_bar_any(int id, int nthreads, bool pred) {
       : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(nthreads)
       : "memory");
   return r != 0;
+}
+
+// max(a, b, c) in one instruction (three-input form of max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // 2^x on the MUFU unit (flushes denormal results to zero).

@@ -8,26 +8,35 @@
 //               P = exp2(s*scale*log2e - max) with the scale folded into one FMA
 //   warps 8-15  operand prologue, two lanes per row (one per 64-column half):
 //               Q' for both query tiles, then K' for every key tile of a
-//               kStages-deep ring; bf16 rows arrive by TMA in the operand
+//               kKStages-deep ring; bf16 rows arrive by TMA in the operand
 //               layout and are normalised and rotated in place, their (cos,
 //               sin) rows being fetched while the TMA is in flight (fp32 rows
 //               are read from global memory, one thread per row)
 //   warp 16     TMEM allocation + tcgen05.mma issue (one thread)
-//   warp 17     TMA: raw Q and K rows, V tiles
+//   warp 17     TMA: lane 0 raw Q and K rows, lane 1 V tiles (separate rings:
+//               a K stage is released once both score MMAs of its tile are
+//               done, a V stage once both PV MMAs are)
 // TMEM (512 columns): S0 | S1 | O0 | O1, 128 fp32 columns each; P_i (bf16)
 // overwrites the first 64 columns of S_i and feeds PV from TMEM.
 // MMA issue order per key tile n: PV0(n-1), S0(n), PV1(n-1), S1(n), so that
 // while one softmax group works on its scores the tensor core computes the
-// other's.
+// other's. The K' ring is three tiles deep: the TMA load and the prologue of
+// a key tile (several thousand cycles together) run while the MMAs of the two
+// tiles before it are issued.
 #include "st_common.cuh"
 #include "st_kernels.h"
 #include "st_prologue.cuh"
+
+#ifndef ST_OPERAND_F16
+#define ST_OPERAND_F16 false  // this unit's 16-bit operand type: bf16 (st_fwd_f16.cu: fp16)
+#endif
 
 namespace st {
 
 namespace {
 
-constexpr int kStages = 2;
+constexpr int kKStages = 3;  // K' ring: TMA load + in-place prologue run ahead of the MMAs
+constexpr int kVStages = 2;
 constexpr int kSoftWarps = 8;
 constexpr int kWarpProl0 = 8, kProlWarps = 8;
 constexpr int kWarpMma = 16, kWarpTma = 17;
@@ -39,36 +48,69 @@ constexpr float kRescaleThreshold = 8.0f;
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                                  // 2 tiles
-constexpr uint32_t kOffK = 2 * kTileBytes;                     // kStages tiles
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;       // kStages tiles
-constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+constexpr uint32_t kOffK = 2 * kTileBytes;                     // kKStages tiles
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;      // kVStages tiles
+constexpr uint32_t kOffBar = kOffV + kVStages * kTileBytes;
 constexpr uint32_t kOffW = kOffBar + 256;                      // q and k norm weights, fp32
-constexpr uint32_t kFwdSmem = kOffW + 2 * kD * 4 + 1024;
+constexpr uint32_t kOffFlags = kOffW + 2 * kD * 4;             // bool masks: the two query tiles' tile classes
+constexpr int kMaxFlagTiles = 896;                             // key tiles whose classes fit (else read from global)
+constexpr uint32_t kFwdSmem = kOffFlags + 2 * kMaxFlagTiles;   // the base must be 1024-byte aligned
+static_assert(kFwdSmem <= 232448, "forward shared memory exceeds the per-block limit");
 
 enum {
   kBarQRaw = 0,                       // raw q rows landed (TMA)
   kBarQFull,                          // Q' ready (prologue)
-  kBarKRaw,                           // + stage: raw k rows landed (TMA)
-  kBarKFull = kBarKRaw + kStages,     // + stage: K' ready (prologue)
-  kBarVFull = kBarKFull + kStages,    // + stage
-  kBarKVEmpty = kBarVFull + kStages,  // + stage
-  kBarSFull = kBarKVEmpty + kStages,  // + tile (0/1)
-  kBarPFull = kBarSFull + 2,          // + tile, 256 arrivals
+  kBarKRaw,                           // + K stage: raw k rows landed (TMA)
+  kBarKFull = kBarKRaw + kKStages,    // + K stage: K' ready (prologue)
+  kBarKEmpty = kBarKFull + kKStages,  // + K stage: both score MMAs of the tile done
+  kBarVFull = kBarKEmpty + kKStages,  // + V stage
+  kBarVEmpty = kBarVFull + kVStages,  // + V stage: both PV MMAs of the tile done
+  kBarSFull = kBarVEmpty + kVStages,  // + tile (0/1)
+  kBarPFull = kBarSFull + 2,          // + tile, 128 arrivals
   kBarOFull = kBarPFull + 2,
   kNumBars = kBarOFull + 1
 };
+static_assert(kNumBars * 8 + 16 <= 256, "barrier area");
 
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-  return sdesc_sw128(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+// Byte offsets of K-step kk (16 elements) inside a K-major tile (two 64-column
+// halves) and inside an MN-major tile (16 rows of 128 B per step); the MMA
+// thread adds them to descriptors built once, so that each MMA costs it one add
+// (it shares its issue slots with four busy warps).
+__device__ __forceinline__ constexpr uint32_t kofs(int kk) { return (kk >> 2) * kHalfBytes + (kk & 3) * 32; }
+__device__ __forceinline__ constexpr uint32_t mofs(int kk) { return kk * 2048; }
+
+// S = Q' K'^T for one query tile: eight K-steps of 16.
+template <bool F16>
+__device__ __forceinline__ void issue_s(uint32_t tS, uint64_t dQ, uint64_t dK) {
+  constexpr uint32_t idesc = idesc16(F16, 128, 128, 0, 0);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) mma_ss(tS, sdesc_add(dQ, kofs(kk)), sdesc_add(dK, kofs(kk)), idesc, kk > 0);
 }
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
-  return sdesc_sw128(base + kk * 2048, kHalfBytes, 1024);
+// O (+)= P V with P (16-bit) in TMEM: eight K-steps of 16 keys.
+template <bool F16>
+__device__ __forceinline__ void issue_pv(uint32_t tO, uint32_t tP, uint64_t dV, bool acc) {
+  constexpr uint32_t idesc = idesc16(F16, 128, 128, 0, 1);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) mma_ts(tO, tP + kk * 8, sdesc_add(dV, mofs(kk)), idesc, acc || kk > 0);
 }
+
+// Tile classes of the CTA's two query tiles (bool masks): read from a
+// shared-memory copy made at the start (when the key-tile count fits), since
+// the MMA thread consults them on its critical path, else from global memory.
+struct PairFlags {
+  const uint8_t* sm;  // [2][kMaxFlagTiles] or nullptr
+  const uint8_t* g0;  // global rows of the two query tiles
+  const uint8_t* g1;
+  bool has1;          // the second query tile exists (the last pair may have one tile)
+};
 
 template <int MK>
-__device__ __forceinline__ uint8_t tile_flag(const Common& c, int b, int h, int qt, int kt) {
-  if (qt >= c.nQt) return kTileAllFalse;
-  if constexpr (MK == kMaskBool) return c.flags[b * c.f_sb + h * c.f_sh + qt * c.f_sq + kt];
+__device__ __forceinline__ uint8_t tile_flag(const PairFlags& f, int ti, int kt) {
+  if (ti && !f.has1) return kTileAllFalse;
+  if constexpr (MK == kMaskBool) {
+    if (f.sm) return f.sm[ti * kMaxFlagTiles + kt];
+    return (ti ? f.g1 : f.g0)[kt];
+  }
   if constexpr (MK == kMaskNone) return kTileAllTrue;
   return kTileMixed;  // additive masks are always applied
 }
@@ -78,10 +120,11 @@ __device__ __forceinline__ float c_wk(const Common& c, int d) { return __ldg(c.w
 
 // Next key tile at or after kt that at least one of the two query tiles needs.
 template <int MK>
-__device__ __forceinline__ int next_tile(const Common& c, int b, int h, int qt0, int kt, int kt_end) {
-  if constexpr (MK != kMaskBool) return kt;
-  for (; kt < kt_end; ++kt)
-    if (tile_flag<MK>(c, b, h, qt0, kt) != kTileAllFalse || tile_flag<MK>(c, b, h, qt0 + 1, kt) != kTileAllFalse) break;
+__device__ __forceinline__ int next_tile(const PairFlags& f, int kt, int kt_end) {
+  if constexpr (MK == kMaskBool) {
+    for (; kt < kt_end; ++kt)
+      if (tile_flag<MK>(f, 0, kt) != kTileAllFalse || tile_flag<MK>(f, 1, kt) != kTileAllFalse) break;
+  }
   return kt;
 }
 
@@ -173,10 +216,14 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
   }
 }
 
-template <int MK, bool CAUSAL, bool QKT>
+template <int MK, bool CAUSAL, bool QKT, bool F16>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = smem_raw;
+  if (smem_u32(sm) & 1023u) {  // the layout has no slack: refuse an unaligned base (uniform over the grid)
+    if (threadIdx.x == 0) atomicOr(P.c.status, kStatusLayout);
+    return;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
@@ -184,6 +231,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   const Common& c = P.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
   const int pair = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int hk = h / P.c.group;  // the K/V head of query head h (grouped K/V heads)
   const int qt0 = 2 * pair;
 
   if (warp == kWarpMma) {
@@ -193,11 +241,14 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   if (tid == 0) {
     mbar_init(&bars[kBarQRaw], 1);
     mbar_init(&bars[kBarQFull], kProlWarps * 32);
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars[kBarKRaw + s], 1);
       mbar_init(&bars[kBarKFull + s], kProlWarps * 32);
+      mbar_init(&bars[kBarKEmpty + s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       mbar_init(&bars[kBarVFull + s], 1);
-      mbar_init(&bars[kBarKVEmpty + s], 1);
+      mbar_init(&bars[kBarVEmpty + s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars[kBarSFull + t], 1);
@@ -209,6 +260,20 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
   float* sW = reinterpret_cast<float*>(sm + kOffW);  // [wq | wk]
   if (tid < 2 * kD) sW[tid] = tid < kD ? c_wq(P.c, tid) : c_wk(P.c, tid - kD);
+  PairFlags fl{nullptr, nullptr, nullptr, qt0 + 1 < c.nQt};
+  if constexpr (MK == kMaskBool) {
+    const uint8_t* row = c.flags + b * c.f_sb + h * c.f_sh;
+    fl.g0 = row + qt0 * c.f_sq;
+    fl.g1 = fl.has1 ? row + (qt0 + 1) * c.f_sq : fl.g0;
+    if (c.nKt <= kMaxFlagTiles) {
+      uint8_t* sf = sm + kOffFlags;
+      for (int e = tid; e < 2 * c.nKt; e += kFwdThreads) {
+        const int ti = e >= c.nKt, kt = e - ti * c.nKt;
+        sf[ti * kMaxFlagTiles + kt] = (ti ? fl.g1 : fl.g0)[kt];
+      }
+      fl.sm = sf;
+    }
+  }
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
     if constexpr (QKT) {
@@ -240,8 +305,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0, useful = 0;
     bool ok = true;
-    for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); kt < kt_end; kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
-      const uint8_t flag = tile_flag<MK>(c, b, h, qt0 + ti, kt);
+    for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end; kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+      const uint8_t flag = tile_flag<MK>(fl, ti, kt);
       useful += (flag != kTileAllFalse && (!CAUSAL || kt <= qt0 + ti)) ? 1 : 0;
       const int j0 = kt * kTile;
       // plain tiles: no mask values, no causal diagonal, no key bound inside
@@ -264,19 +329,30 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       tc_fence_after();
       // pass 1: row max (raw scores on plain tiles; the scale is positive)
       float mt = -INFINITY;
+      if (plain) {
+        // each 16-column load is issued before the previous one is reduced
+        uint32_t ra[16], rb[16];
+        float m0 = -INFINITY, m1 = -INFINITY;
+        tmem_ld16_issue(tS, ra);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t raw[32];
-        tmem_ld32(tS + 32 * q4, raw);
-        if (plain) {
-          float m0 = __uint_as_float(raw[0]), m1 = __uint_as_float(raw[1]);
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t(&cur)[16] = (q8 & 1) ? rb : ra;
+          uint32_t(&nxt)[16] = (q8 & 1) ? ra : rb;
+          tmem_ld_wait16(cur);
+          if (q8 < 7) tmem_ld16_issue(tS + 16 * (q8 + 1), nxt);
 #pragma unroll
-          for (int t = 2; t < 32; t += 2) {
-            m0 = fmaxf(m0, __uint_as_float(raw[t]));
-            m1 = fmaxf(m1, __uint_as_float(raw[t + 1]));
+          for (int t = 0; t < 16; t += 4) {
+            m0 = fmax3(m0, __uint_as_float(cur[t]), __uint_as_float(cur[t + 1]));
+            m1 = fmax3(m1, __uint_as_float(cur[t + 2]), __uint_as_float(cur[t + 3]));
           }
-          mt = fmaxf(mt, fmaxf(m0, m1) * sc);
-        } else {
+        }
+        mt = fmaxf(m0, m1) * sc;
+      }
+      if (!plain) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t raw[32];
+          tmem_ld32(tS + 32 * q4, raw);
           // scaled and masked once; pass 2 reads them back instead of the mask
           float sv[32];
           masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv, mask_vec, scratch);
@@ -288,39 +364,56 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           }
           tmem_st32(tS + 32 * q4, w32);
         }
+        tmem_st_wait();
       }
-      if (!plain) tmem_st_wait();
       float corr = 1.f;
       if (mt > m_run + kRescaleThreshold || (m_run == -INFINITY && mt > -INFINITY)) {
         corr = ex2(m_run - mt);  // 0 when m_run is -inf
         m_run = mt;
       }
       const float m_use = (m_run == -INFINITY) ? 0.f : m_run;
-      // pass 2: P = exp2(s - m) (bf16 into the first 64 S columns), row sum
+      // pass 2: P = exp2(s - m) (bf16 into the first 64 S columns), row sum.
+      // Step q8 of P lands in columns [8 q8, 8 q8 + 8), which the loads of
+      // steps <= q8 have already read.
       float ls0 = 0.f, ls1 = 0.f;
+      if (plain) {
+        uint32_t ra[16], rb[16];
+        const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m_use, -m_use);
+        float2 ls = make_float2(0.f, 0.f);
+        tmem_ld16_issue(tS, ra);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t raw[32], pw[16];
-        tmem_ld32(tS + 32 * q4, raw);
-        if (plain) {
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t(&cur)[16] = (q8 & 1) ? rb : ra;
+          uint32_t(&nxt)[16] = (q8 & 1) ? ra : rb;
+          tmem_ld_wait16(cur);
+          if (q8 < 7) tmem_ld16_issue(tS + 16 * (q8 + 1), nxt);
+          uint32_t pw[8];
 #pragma unroll
-          for (int t = 0; t < 16; ++t) {
-            const float p0 = ex2(fmaf(__uint_as_float(raw[2 * t]), sc, -m_use));
-            const float p1 = ex2(fmaf(__uint_as_float(raw[2 * t + 1]), sc, -m_use));
-            ls0 += p0;
-            ls1 += p1;
-            pw[t] = pack_bf16(p0, p1);
+          for (int t = 0; t < 8; ++t) {
+            const float2 x = __ffma2_rn(make_float2(__uint_as_float(cur[2 * t]), __uint_as_float(cur[2 * t + 1])), sc2, nm2);
+            const float p0 = ex2(x.x), p1 = ex2(x.y);
+            ls = __fadd2_rn(ls, make_float2(p0, p1));
+            pw[t] = pack16<F16>(p0, p1);
           }
-        } else {
+          tmem_st8(tS + 8 * q8, pw);
+        }
+        ls0 = ls.x;
+        ls1 = ls.y;
+      }
+      if (!plain) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t raw[32], pw[16];
+          tmem_ld32(tS + 32 * q4, raw);
 #pragma unroll
           for (int t = 0; t < 16; ++t) {
             const float p0 = ex2(__uint_as_float(raw[2 * t]) - m_use), p1 = ex2(__uint_as_float(raw[2 * t + 1]) - m_use);
             ls0 += p0;
             ls1 += p1;
-            pw[t] = pack_bf16(p0, p1);
+            pw[t] = pack16<F16>(p0, p1);
           }
+          tmem_st16(tS + 16 * q4, pw);
         }
-        tmem_st16(tS + 16 * q4, pw);
       }
       l_run = l_run * corr + (ls0 + ls1);
       if (n > 0 && __any_sync(0xffffffffu, corr != 1.f)) {  // warp-uniform: tcgen05.ld/st are collective
@@ -355,7 +448,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         float y[32];
 #pragma unroll
         for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r32[t]) * inv;
-        if (i < c.Sq) store_chunk32(P.o, ooff, P.o_f32, q4, y);
+        if (i < c.Sq) store_chunk32(P.o, ooff, P.o_dt, q4, y);
       }
       if (i < c.Sq)
         P.lse[((int64_t)b * c.H + h) * c.Sq + i] = (l_run > 0.f) ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
@@ -376,7 +469,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         uint8_t* tile = sm + kOffQ + ti * kTileBytes;
         if constexpr (QKT) {
           const int i = (qt0 + ti) * kTile + prow;  // rows past S_q stay TMA zeros
-          HalfRowPrologue hp;
+          HalfRowPrologue<F16> hp;
           if (i < c.Sq) {
             const __half2* t16 = c.tab16_q + b * c.tab_q_sb + (int64_t)i * kPairs;
             hp.prefetch(t16, hh);
@@ -386,7 +479,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
         } else if (p < kTile) {
           const int i = (qt0 + ti) * kTile + p;
           if (i < c.Sq)
-            rope_norm_global(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.is_f32, c.wq, c.eps,
+            rope_norm_global<F16>(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.dt, c.wq, c.eps,
                              c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, tile, p);
           else
             zero_row(tile, p);
@@ -396,26 +489,26 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars[kBarQFull]);
     }
     int n = 0;
-    for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); ok && kt < kt_end;
-         kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
-      const int slot = n % kStages;
+    for (int kt = next_tile<MK>(fl, 0, kt_end); ok && kt < kt_end;
+         kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+      const int slot = n % kKStages;
       uint8_t* tile = sm + kOffK + slot * kTileBytes;
       if constexpr (QKT) {
         const int j = kt * kTile + prow;
-        HalfRowPrologue hp;
+        HalfRowPrologue<F16> hp;
         if (j < c.Skv) {
           const __half2* t16 = c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs;
           hp.prefetch(t16, hh);
           hp.prefetch2(t16, hh);
         }
-        if (!wait_bar_warp(&bars[kBarKRaw + slot], (n / kStages) & 1, abort_flag, budget)) break;
+        if (!wait_bar_warp(&bars[kBarKRaw + slot], (n / kKStages) & 1, abort_flag, budget)) break;
         hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
       } else {
-        if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
+        if (n >= kKStages && !wait_bar(&bars[kBarKEmpty + slot], ((n / kKStages) - 1) & 1, abort_flag, budget)) break;
         if (p < kTile) {
           const int j = kt * kTile + p;
           if (j < c.Skv)
-            rope_norm_global(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + h * c.k.sh, c.k.is_f32, c.wk, c.eps,
+            rope_norm_global<F16>(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
                              c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs, tile, p);
           else
             zero_row(tile, p);
@@ -425,7 +518,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars[kBarKFull + slot]);
     }
   } else if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA: raw Q, raw K, V
+    // ------------------------------------------------------------ TMA: raw Q, raw K (lane 0), V (lane 1)
     if (lane_id == 0) {
       if constexpr (QKT) {
         mbar_arrive_expect_tx(&bars[kBarQRaw], 2 * kTileBytes);
@@ -437,87 +530,86 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tma_load_4d(tile, &P.tmap_q, &bars[kBarQRaw], 0, y, z, b);
           tma_load_4d(tile + kHalfBytes, &P.tmap_q, &bars[kBarQRaw], 64, y, z, b);
         }
-      }
-      int n = 0;
-      for (int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end); kt < kt_end;
-           kt = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end), ++n) {
-        const int slot = n % kStages;
-        if (n >= kStages && !wait_bar(&bars[kBarKVEmpty + slot], ((n / kStages) - 1) & 1, abort_flag, budget)) break;
-        if constexpr (QKT) {
+        int n = 0;
+        for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end;
+             kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+          const int slot = n % kKStages;
+          if (n >= kKStages && !wait_bar(&bars[kBarKEmpty + slot], ((n / kKStages) - 1) & 1, abort_flag, budget))
+            break;
           uint8_t* ktile = sm + kOffK + slot * kTileBytes;
-          const int y = P.k_s_first ? kt * kTile : h, z = P.k_s_first ? h : kt * kTile;
+          const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
           mbar_arrive_expect_tx(&bars[kBarKRaw + slot], kTileBytes);
           tma_load_4d(ktile, &P.tmap_k, &bars[kBarKRaw + slot], 0, y, z, b);
           tma_load_4d(ktile + kHalfBytes, &P.tmap_k, &bars[kBarKRaw + slot], 64, y, z, b);
         }
+        // every issued load lands before the CTA exits (these waits do not
+        // give up on abort; each is bounded)
+        mbar_wait(&bars[kBarQRaw], 0, budget);
+        for (int m = max(0, n - kKStages); m < n; ++m)
+          mbar_wait(&bars[kBarKRaw + m % kKStages], (m / kKStages) & 1, budget);
+      }
+    } else if (lane_id == 1) {
+      int n = 0;
+      for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end;
+           kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+        const int slot = n % kVStages;
+        if (n >= kVStages && !wait_bar(&bars[kBarVEmpty + slot], ((n / kVStages) - 1) & 1, abort_flag, budget)) break;
         uint8_t* tile = sm + kOffV + slot * kTileBytes;
-        const int y = P.v_s_first ? kt * kTile : h, z = P.v_s_first ? h : kt * kTile;
+        const int y = P.v_s_first ? kt * kTile : hk, z = P.v_s_first ? hk : kt * kTile;
         mbar_arrive_expect_tx(&bars[kBarVFull + slot], kTileBytes);
         tma_load_4d(tile, &P.tmap_v, &bars[kBarVFull + slot], 0, y, z, b);
         tma_load_4d(tile + kHalfBytes, &P.tmap_v, &bars[kBarVFull + slot], 64, y, z, b);
       }
-      // every issued load lands before the CTA exits
-      // (these waits do not give up on abort; each is bounded)
-      if constexpr (QKT) mbar_wait(&bars[kBarQRaw], 0, budget);
-      for (int m = max(0, n - kStages); m < n; ++m) {
-        mbar_wait(&bars[kBarVFull + m % kStages], (m / kStages) & 1, budget);
-        if constexpr (QKT) mbar_wait(&bars[kBarKRaw + m % kStages], (m / kStages) & 1, budget);
-      }
+      for (int m = max(0, n - kVStages); m < n; ++m)
+        mbar_wait(&bars[kBarVFull + m % kVStages], (m / kVStages) & 1, budget);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     if (lane_id == 0) {
-      const uint32_t idesc_qk = idesc_bf16(128, 128, 0, 0);
-      const uint32_t idesc_pv = idesc_bf16(128, 128, 0, 1);
-      const uint32_t aQ0 = smem_u32(sm + kOffQ), aQ1 = aQ0 + kTileBytes;
+      const uint64_t dQ0 = sdesc_sw128(smem_u32(sm + kOffQ), 16, 1024), dQ1 = sdesc_add(dQ0, kTileBytes);
+      const uint64_t dK0 = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_u32(sm + kOffV), kHalfBytes, 1024);
       const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
       bool ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
-      int kt = next_tile<MK>(c, b, h, qt0, 0, kt_end);
+      int kt = next_tile<MK>(fl, 0, kt_end);
       int n = 0;
       bool issued = false;
       if (ok && kt < kt_end) {
         ok = wait_bar(&bars[kBarKFull + 0], 0, abort_flag, budget);
         if (ok) {
           tc_fence_after();
-          const uint32_t aK = smem_u32(sm + kOffK);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, kmajor_desc(aQ0, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          issue_s<F16>(tS0, dQ0, dK0);
           mma_commit(&bars[kBarSFull + 0]);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, kmajor_desc(aQ1, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          issue_s<F16>(tS1, dQ1, dK0);
           mma_commit(&bars[kBarSFull + 1]);
+          mma_commit(&bars[kBarKEmpty + 0]);
           issued = true;
         }
       }
       while (ok && kt < kt_end) {
-        const int slot = n % kStages;
-        const int kt_next = next_tile<MK>(c, b, h, qt0, kt + 1, kt_end);
+        const int vslot = n % kVStages;
+        const int kt_next = next_tile<MK>(fl, kt + 1, kt_end);
         const bool has_next = kt_next < kt_end;
-        const int nslot = (n + 1) % kStages;
-        const uint32_t aV = smem_u32(sm + kOffV + slot * kTileBytes);
-        if (!(ok = wait_bar(&bars[kBarVFull + slot], (n / kStages) & 1, abort_flag, budget))) break;
+        const int nslot = (n + 1) % kKStages;
+        const uint64_t dV = sdesc_add(dV0, vslot * kTileBytes), dK = sdesc_add(dK0, nslot * kTileBytes);
+        if (!(ok = wait_bar(&bars[kBarVFull + vslot], (n / kVStages) & 1, abort_flag, budget))) break;
         if (!(ok = wait_bar(&bars[kBarPFull + 0], n & 1, abort_flag, budget))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(tO0, tS0 + kk * 8, mnmajor_desc(aV, kk), idesc_pv, (n > 0 || kk > 0));
+        issue_pv<F16>(tO0, tS0, dV, n > 0);
         if (has_next) {
-          if (!(ok = wait_bar(&bars[kBarKFull + nslot], ((n + 1) / kStages) & 1, abort_flag, budget))) break;
+          if (!(ok = wait_bar(&bars[kBarKFull + nslot], ((n + 1) / kKStages) & 1, abort_flag, budget))) break;
           tc_fence_after();
-          const uint32_t aK = smem_u32(sm + kOffK + nslot * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tS0, kmajor_desc(aQ0, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          issue_s<F16>(tS0, dQ0, dK);
           mma_commit(&bars[kBarSFull + 0]);
         }
         if (!(ok = wait_bar(&bars[kBarPFull + 1], n & 1, abort_flag, budget))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) mma_ts(tO1, tS1 + kk * 8, mnmajor_desc(aV, kk), idesc_pv, (n > 0 || kk > 0));
-        mma_commit(&bars[kBarKVEmpty + slot]);
+        issue_pv<F16>(tO1, tS1, dV, n > 0);
+        mma_commit(&bars[kBarVEmpty + vslot]);
         if (has_next) {
-          const uint32_t aK = smem_u32(sm + kOffK + nslot * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) mma_ss(tS1, kmajor_desc(aQ1, kk), kmajor_desc(aK, kk), idesc_qk, kk > 0);
+          issue_s<F16>(tS1, dQ1, dK);
           mma_commit(&bars[kBarSFull + 1]);
+          mma_commit(&bars[kBarKEmpty + nslot]);
         }
         kt = kt_next;
         ++n;
@@ -545,37 +637,37 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
 }  // namespace
 
-template <int MK, bool CAUSAL, bool QKT>
+template <int MK, bool CAUSAL, bool QKT, bool F16>
 cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
-  auto kern = fwd_kernel<MK, CAUSAL, QKT>;
-  static unsigned configured = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured & (1u << (dev & 31)))) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kFwdSmem);
-    if (e != cudaSuccess) return e;
-    configured |= 1u << (dev & 31);
-  }
+  auto kern = fwd_kernel<MK, CAUSAL, QKT, F16>;
+  static std::atomic<uint64_t> configured{0};
+  cudaError_t e = opt_in_smem(kern, kFwdSmem, configured);
+  if (e != cudaSuccess) return e;
   dim3 grid((p.c.nQt + 1) / 2, p.c.H, p.c.B);
   kern<<<grid, kFwdThreads, kFwdSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <bool QKT>
+template <bool QKT, bool F16>
 cudaError_t launch_fwd_q(const FwdParams& p, cudaStream_t stream) {
-  if (p.c.causal) return launch_fwd_t<kMaskNone, true, QKT>(p, stream);  // masks and causal never combine
+  if (p.c.causal) return launch_fwd_t<kMaskNone, true, QKT, F16>(p, stream);  // masks and causal never combine
   switch (p.c.mask_kind) {
-    case kMaskBool: return launch_fwd_t<kMaskBool, false, QKT>(p, stream);
-    case kMaskF32: return launch_fwd_t<kMaskF32, false, QKT>(p, stream);
-    case kMaskBF16: return launch_fwd_t<kMaskBF16, false, QKT>(p, stream);
-    default: return launch_fwd_t<kMaskNone, false, QKT>(p, stream);
+    case kMaskBool: return launch_fwd_t<kMaskBool, false, QKT, F16>(p, stream);
+    case kMaskF32: return launch_fwd_t<kMaskF32, false, QKT, F16>(p, stream);
+    case kMaskBF16: return launch_fwd_t<kMaskBF16, false, QKT, F16>(p, stream);
+    default: return launch_fwd_t<kMaskNone, false, QKT, F16>(p, stream);
   }
 }
 
-// Kernels are specialised on the mask kind, causal masking and whether q/k
-// are staged by TMA, so that each carries only its own code.
-cudaError_t launch_fwd(const FwdParams& p, cudaStream_t stream) {
-  return p.qk_tma ? launch_fwd_q<true>(p, stream) : launch_fwd_q<false>(p, stream);
+// Kernels are specialised on the mask kind, causal masking, whether q/k are
+// staged by TMA and the 16-bit operand type, so that each carries only its
+// own code. This translation unit holds one operand type (ST_OPERAND_F16).
+#if ST_OPERAND_F16
+cudaError_t launch_fwd_f16(const FwdParams& p, cudaStream_t stream) {
+#else
+cudaError_t launch_fwd_bf16(const FwdParams& p, cudaStream_t stream) {
+#endif
+  return p.qk_tma ? launch_fwd_q<true, ST_OPERAND_F16>(p, stream) : launch_fwd_q<false, ST_OPERAND_F16>(p, stream);
 }
 
 }  // namespace st

@@ -1,86 +1,13 @@
-// Warp-cooperative operand prologue: RMSNorm (fp32) + interleaved-pair RoPE of
-// one 128-row tile of q or k, rounded to bf16 and written as a K-major,
-// 128B-swizzled UMMA operand tile. One warp handles one row at a time; lane l
-// owns head dims 4l..4l+3 (two rotation pairs), so every global load (the raw
-// row, its (cos, sin) table row) is one coalesced request per row, the norm
-// weights stay in registers, and the row's sum of squares is a shuffle
-// reduction.
+// Operand prologues: RMSNorm (fp32) + interleaved-pair RoPE of q or k rows,
+// rounded to the 16-bit MMA operand type (bf16, or fp16 with F16) and written
+// as K-major, 128B-swizzled UMMA operand tiles. The in-place forms work on raw
+// rows that TMA has already landed in the operand layout (raw rows of the
+// operand type); the global forms read bf16, fp16 or fp32 rows from global
+// memory.
 #pragma once
 #include "st_common.cuh"
 
 namespace st {
-
-struct RowPrologue {
-  float w0, w1, w2, w3;  // this lane's four norm weights
-  float eps;
-  uint32_t dst;          // this lane's byte offset inside a row (half, chunk, 8-byte sub-chunk)
-  int lane;
-
-  __device__ __forceinline__ RowPrologue(const float* __restrict__ w, float eps_, int lane_)
-      : eps(eps_), lane(lane_) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(w) + lane_);
-    w0 = v.x; w1 = v.y; w2 = v.z; w3 = v.w;
-    dst = (lane_ >> 4) * kHalfBytes;
-  }
-
-  // Rows [row0, row0 + 128) of x (head h, batch b) into `tile`; rows at or
-  // beyond nrows are written as zeros. tab: the (cos, sin) table of batch b,
-  // indexed by row. Warp `wi` of `nw` handles rows wi, wi + nw, ...
-  __device__ __forceinline__ void tile(const RowTensor& x, int b, int h, int row0, int nrows,
-                                       const float2* __restrict__ tab, uint8_t* tile_base, int wi, int nw) const {
-    constexpr int U = 4;  // rows in flight per warp
-    const int64_t base = b * x.sb + h * x.sh + 4 * lane;
-    const uint32_t chunk = (lane & 15) >> 1, sub = (lane & 1) * 8;
-#pragma unroll 1
-    for (int rr = wi; rr < kTile; rr += nw * U) {
-      float v[U][4], cs[U][4];
-      bool valid[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int row = row0 + rr + u * nw;
-        valid[u] = (rr + u * nw < kTile) && row < nrows;
-        if (valid[u]) {
-          const int64_t off = base + (int64_t)row * x.ss;
-          if (x.is_f32) {
-            const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(x.p) + off));
-            v[u][0] = a.x; v[u][1] = a.y; v[u][2] = a.z; v[u][3] = a.w;
-          } else {
-            const uint2 a = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(x.p) + off));
-            v[u][0] = bf16_lo(a.x); v[u][1] = bf16_hi(a.x); v[u][2] = bf16_lo(a.y); v[u][3] = bf16_hi(a.y);
-          }
-          const float4 t = __ldg(reinterpret_cast<const float4*>(tab + (int64_t)row * kPairs) + lane);
-          cs[u][0] = t.x; cs[u][1] = t.y; cs[u][2] = t.z; cs[u][3] = t.w;
-        } else {
-          v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0.f;
-          cs[u][0] = 1.f; cs[u][1] = 0.f; cs[u][2] = 1.f; cs[u][3] = 0.f;
-        }
-      }
-      float ss[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        ss[u] = fmaf(v[u][0], v[u][0], fmaf(v[u][1], v[u][1], fmaf(v[u][2], v[u][2], v[u][3] * v[u][3])));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (rr + u * nw >= kTile) continue;
-        const int trow = rr + u * nw;
-        uint32_t lo = 0u, hi = 0u;
-        if (valid[u]) {
-          const float r = rsqrtf(ss[u] * (1.0f / kD) + eps);
-          const float n0 = v[u][0] * w0 * r, n1 = v[u][1] * w1 * r;
-          const float n2 = v[u][2] * w2 * r, n3 = v[u][3] * w3 * r;
-          lo = pack_bf16(n0 * cs[u][0] - n1 * cs[u][1], n0 * cs[u][1] + n1 * cs[u][0]);
-          hi = pack_bf16(n2 * cs[u][2] - n3 * cs[u][3], n2 * cs[u][3] + n3 * cs[u][2]);
-        }
-        *reinterpret_cast<uint2*>(tile_base + dst + sw128_off(trow, chunk) + sub) = make_uint2(lo, hi);
-      }
-    }
-  }
-};
 
 // Thread-per-row prologue on a tile that TMA has already filled with the raw
 // bf16 rows (128B-swizzled, the operand layout): the thread reads its row,
@@ -89,6 +16,7 @@ struct RowPrologue {
 // the 16-byte accesses are conflict-free. tab16: the row's 64 (cos, sin) in
 // fp16 (16 loads of 16 bytes, all issued before the arithmetic); w: the norm
 // weights in shared memory.
+template <bool F16>
 struct RowInplace {
   uint4 cs[kD / 8];  // (cos, sin) of pairs 4c .. 4c+3, fp16
   // Issues the row's table loads; finish() consumes them.
@@ -105,7 +33,7 @@ struct RowInplace {
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
+        const float lo = lo16<F16>(u[e]), hi = hi16<F16>(u[e]);
         a0 = fmaf(lo, lo, a0);
         a1 = fmaf(hi, hi, a1);
       }
@@ -124,17 +52,18 @@ struct RowInplace {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {  // pair 4c + e
         const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
-        const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
-        out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
+        const float n0 = lo16<F16>(u[e]) * wv[2 * e] * r, n1 = hi16<F16>(u[e]) * wv[2 * e + 1] * r;
+        out[e] = pack16<F16>(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
       }
       *p16 = make_uint4(out[0], out[1], out[2], out[3]);
     }
   }
 };
 
+template <bool F16>
 __device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const float* w, float eps,
                                                   const __half2* __restrict__ tab16) {
-  RowInplace rp;
+  RowInplace<F16> rp;
   rp.prefetch(tab16);
   rp.finish(tile, row, w, eps);
 }
@@ -146,6 +75,7 @@ __device__ __forceinline__ void rope_norm_inplace(uint8_t* tile, int row, const 
 // lines) instead of one line per lane, and the swizzled tile accesses of four
 // consecutive rows are conflict-free. The row's sum of squares is reduced
 // over the eight lanes with shuffles, so all 32 lanes call finish().
+template <bool F16>
 struct OctRow {
   uint4 cs0, cs1;  // (cos, sin) fp16 of this lane's pairs in half 0 and half 1
   // Folds the loaded words into `acc`: a use that the compiler cannot move the
@@ -167,8 +97,8 @@ struct OctRow {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
-      const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
-      out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
+      const float n0 = lo16<F16>(u[e]) * wv[2 * e] * r, n1 = hi16<F16>(u[e]) * wv[2 * e + 1] * r;
+      out[e] = pack16<F16>(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
     }
     v = make_uint4(out[0], out[1], out[2], out[3]);
   }
@@ -189,8 +119,8 @@ struct OctRow {
     float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float2 xa = make_float2(bf16_lo(ua[e]), bf16_hi(ua[e]));
-      const float2 xb = make_float2(bf16_lo(ub[e]), bf16_hi(ub[e]));
+      const float2 xa = make_float2(lo16<F16>(ua[e]), hi16<F16>(ua[e]));
+      const float2 xb = make_float2(lo16<F16>(ub[e]), hi16<F16>(ub[e]));
       sa = __ffma2_rn(xa, xa, sa);
       sb = __ffma2_rn(xb, xb, sb);
     }
@@ -228,7 +158,7 @@ struct OctRow {
     const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-      const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
+      const float lo = lo16<F16>(u[e]), hi = hi16<F16>(u[e]);
       a0 = fmaf(lo, lo, a0);
       a1 = fmaf(hi, hi, a1);
     }
@@ -249,6 +179,7 @@ struct OctRow {
 // half `hh` owns head dims [64*hh, 64*hh + 64) = the 64-column half `hh` of the
 // swizzled tile. The (cos, sin) loads are issued by prefetch() before the raw
 // rows are known to have landed; finish() waits for nothing itself.
+template <bool F16>
 struct HalfRowPrologue {
   uint4 cs[4];  // (cos, sin) fp16 of this lane's 32 pairs
   __device__ __forceinline__ void prefetch(const __half2* __restrict__ tab16_row, int hh) {
@@ -272,7 +203,7 @@ struct HalfRowPrologue {
       const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float lo = bf16_lo(u[e]), hi = bf16_hi(u[e]);
+        const float lo = lo16<F16>(u[e]), hi = hi16<F16>(u[e]);
         a0 = fmaf(lo, lo, a0);
         a1 = fmaf(hi, hi, a1);
       }
@@ -295,8 +226,8 @@ struct HalfRowPrologue {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 sc = __half22float2(*reinterpret_cast<const __half2*>(&t[e]));  // (cos, sin)
-        const float n0 = bf16_lo(u[e]) * wv[2 * e] * r, n1 = bf16_hi(u[e]) * wv[2 * e + 1] * r;
-        out[e] = pack_bf16(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
+        const float n0 = lo16<F16>(u[e]) * wv[2 * e] * r, n1 = hi16<F16>(u[e]) * wv[2 * e + 1] * r;
+        out[e] = pack16<F16>(n0 * sc.x - n1 * sc.y, n0 * sc.y + n1 * sc.x);
       }
       *p16 = make_uint4(out[0], out[1], out[2], out[3]);
     }
@@ -307,7 +238,8 @@ struct HalfRowPrologue {
 // memory; used when q/k are fp32 (no in-place TMA staging) and for rows that
 // a TMA load does not cover. The raw row is read twice (sum of squares, then
 // transform), the second time from L1.
-__device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, int is_f32,
+template <bool F16>
+__device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, int dt,
                                                  const float* __restrict__ w, float eps,
                                                  const float2* __restrict__ tab, uint8_t* tile, int row,
                                                  uint32_t half = kHalfBytes) {
@@ -315,7 +247,7 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c) {
     float x[8];
-    load_chunk8(base, off, is_f32, c, x);
+    load_chunk8(base, off, dt, c, x);
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
       ss0 = fmaf(x[e], x[e], ss0);
@@ -328,7 +260,7 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
 #pragma unroll
   for (int c = 0; c < kD / 8; ++c) {
     float x[8];
-    load_chunk8(base, off, is_f32, c, x);
+    load_chunk8(base, off, dt, c, x);
     uint32_t packed[4];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -336,8 +268,8 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
       const float4 ww = __ldg(w4 + 2 * c + hh);
       const float n0 = x[4 * hh] * ww.x * r, n1 = x[4 * hh + 1] * ww.y * r;
       const float n2 = x[4 * hh + 2] * ww.z * r, n3 = x[4 * hh + 3] * ww.w * r;
-      packed[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
-      packed[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+      packed[2 * hh] = pack16<F16>(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+      packed[2 * hh + 1] = pack16<F16>(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
     }
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) =
         make_uint4(packed[0], packed[1], packed[2], packed[3]);
@@ -349,7 +281,8 @@ __device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, 
 // 4 quarter .. 4 quarter + 3); the row's sum of squares is reduced over the four
 // lanes with shuffles, so every lane of the warp calls it (valid: the row
 // exists; the four lanes of a row agree; an invalid row is written as zeros).
-__device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t off, int is_f32,
+template <bool F16>
+__device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t off, int dt,
                                                       const float* __restrict__ w, float eps,
                                                       const float2* __restrict__ tab, uint8_t* tile, int row,
                                                       int quarter, bool valid, uint32_t half) {
@@ -357,7 +290,7 @@ __device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t 
   float ss = 0.f;
   if (valid) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) load_chunk8(base, off, is_f32, 4 * quarter + i, x[i]);
+    for (int i = 0; i < 4; ++i) load_chunk8(base, off, dt, 4 * quarter + i, x[i]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -380,8 +313,8 @@ __device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t 
         const float4 ww = __ldg(w4 + 2 * c + hh);
         const float n0 = x[i][4 * hh] * ww.x * r, n1 = x[i][4 * hh + 1] * ww.y * r;
         const float n2 = x[i][4 * hh + 2] * ww.z * r, n3 = x[i][4 * hh + 3] * ww.w * r;
-        packed[2 * hh] = pack_bf16(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
-        packed[2 * hh + 1] = pack_bf16(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
+        packed[2 * hh] = pack16<F16>(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
+        packed[2 * hh + 1] = pack16<F16>(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
       }
     }
     *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) =

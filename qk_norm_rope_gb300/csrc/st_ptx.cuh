@@ -86,6 +86,13 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
 
 // ----------------------------------------------------------------- cluster
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -180,11 +187,13 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
-//   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
-//   15 A major (0 = K-major, 1 = MN-major), 16 B major, 17-22 N>>3, 24-28 M>>4.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn_major, int b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
+// Instruction descriptor for kind::f16 with fp32 D and A/B both bf16
+// (f16 = false) or both fp16 (f16 = true).
+//   bits 4-5 D format (1 = f32), 7-9 A format (0 = f16, 1 = bf16), 10-12 B
+//   format, 15 A major (0 = K-major, 1 = MN-major), 16 B major, 17-22 N>>3,
+//   24-28 M>>4.
+__host__ __device__ constexpr uint32_t idesc16(bool f16, int M, int N, int a_mn_major, int b_mn_major) {
+  return (1u << 4) | ((f16 ? 0u : 1u) << 7) | ((f16 ? 0u : 1u) << 10) | (static_cast<uint32_t>(a_mn_major) << 15) |
          (static_cast<uint32_t>(b_mn_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);
 }
@@ -248,7 +257,23 @@ __device__ __forceinline__ void tmem_ld_wait32(uint32_t (&r)[32]) {
 }
 #undef ST_RW8
 
-// Stores 32 (resp. 16) 32-bit columns of the thread's lane. Completion is
+// 16-column forms of the split load, for double buffering under a tight
+// register budget.
+__device__ __forceinline__ void tmem_ld16_issue(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : ST_R8(0), ST_R8(8)
+      : "r"(taddr)
+      : "memory");
+}
+#define ST_RW8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]), \
+                  "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : ST_RW8(0), ST_RW8(8) : : "memory");
+}
+#undef ST_RW8
+
+// Stores 32 (resp. 16, 8) 32-bit columns of the thread's lane. Completion is
 // awaited with tmem_st_wait() before the data is consumed by an MMA.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
@@ -263,6 +288,10 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
           taddr),
       ST_W8(0), ST_W8(8)
       : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), ST_W8(0)
+               : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

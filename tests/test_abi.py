@@ -119,19 +119,31 @@ def test_valid_call_without_gpu_reports_cuda_error():
 def test_null_and_shape_errors():
     c = Call(); c.q = None; expect(c, api.ST_ERR_INVALID_ARG)
     c = Call(D=64); c.wq = T([64], api.ST_F32); c.wk = T([64], api.ST_F32); expect(c, api.ST_ERR_UNSUPPORTED)
-    c = Call(); c.k = T([1, 256, 3, 128]); expect(c, api.ST_ERR_SHAPE, "k has shape")
+    c = Call(); c.k = T([1, 256, 3, 128]); expect(c, api.ST_ERR_SHAPE, "must divide")
     c = Call(); c.o = T([1, 255, 2, 128]); expect(c, api.ST_ERR_SHAPE, "o has shape")
     c = Call(); c.lse = T([1, 2, 255], api.ST_F32); expect(c, api.ST_ERR_SHAPE, "lse")
     c = Call(); c.wq = T([64], api.ST_F32); expect(c, api.ST_ERR_SHAPE, "q_norm_w")
 
 
 def test_dtype_errors():
-    c = Call(); c.q.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "q")
+    c = Call(); c.q.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "q and k must have the same dtype")
+    c = Call(); c.q.dtype = c.k.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "v's dtype")
+    c = Call(); c.q.dtype = c.k.dtype = api.ST_I32; expect(c, api.ST_ERR_DTYPE, "q")
     c = Call(); c.v.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "v")
     c = Call(); c.o.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "o")
     c = Call(); c.wk.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "k_norm_w")
     c = Call(); c.ids.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "ids")
     c = Call(); c.mask = T([1, 1, 1, 256], api.ST_I32); expect(c, api.ST_ERR_DTYPE, "mask")
+
+
+def test_operand_types_accepted():
+    """bf16 throughout, fp16 throughout, and fp32 q/k with either 16-bit v."""
+    for qk, v in ((api.ST_BF16, api.ST_BF16), (api.ST_F16, api.ST_F16), (api.ST_F32, api.ST_BF16),
+                  (api.ST_F32, api.ST_F16)):
+        c = Call()
+        c.q.dtype = c.k.dtype = qk
+        c.v.dtype = c.o.dtype = v
+        assert c.ws_size(0) > 0 and c.ws_size(1) > 0, (qk, v, api.lib().st_last_error())
 
 
 def test_alignment_errors():
@@ -212,3 +224,14 @@ def test_python_rope_tables_marshalling():
         api.RopeTables(cpu, None)
     with pytest.raises(api.StError):
         api._require_cuda(api.RopeTables(cpu, cpu))
+
+
+def test_grouped_kv_heads_validation():
+    """k and v may carry fewer heads than q when their count divides H (grouped
+    K/V heads); dk and dv then have the K/V head count."""
+    c = Call(H=4); c.k = T([1, 256, 2, 128]); c.v = T([1, 256, 2, 128])
+    assert c.ws_size(1) > 0 and c.ws_size(0) == Call(H=4).ws_size(0)
+    c = Call(H=4); c.k = T([1, 256, 1, 128]); c.v = T([1, 256, 1, 128])
+    assert c.ws_size(1) > 0
+    c = Call(H=4); c.k = T([1, 256, 3, 128]); c.v = T([1, 256, 3, 128]); expect(c, api.ST_ERR_SHAPE, "must divide")
+    c = Call(H=4); c.k = T([1, 256, 2, 128]); c.v = T([1, 256, 4, 128]); expect(c, api.ST_ERR_SHAPE, "v has shape")

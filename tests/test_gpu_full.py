@@ -1,8 +1,9 @@
 """Full-size parity: each workload at its real size, run through the same C-ABI
-calls the benchmark times, checked against the oracle on sampled heads (the
-oracle recomputes those (b, h) heads one by one; heads are independent).
-The norm-weight gradients sum over every head, so at full size they are
-checked by the smaller parity tests only."""
+calls, with the same shared workspace and table reuse, that the benchmark
+times, checked against the oracle on sampled heads (the oracle recomputes those
+(b, h) heads one by one; heads are independent). The norm-weight gradients sum
+over every head: the Flux1 1024px case checks them against the oracle's sums
+over all 24 heads."""
 import numpy as np
 import pytest
 import torch
@@ -36,13 +37,16 @@ def run_full(api, inp, heads, mask_dev=None, mask_heads=None):
     q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.do))
     wq, wk, ids = inp.wq.to(dev), inp.wk.to(dev), inp.ids.to(dev)
     mask = mask_dev if mask_dev is not None else (None if inp.mask is None else inp.mask.to(dev))
-    o, lse = api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal)
+    ws = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal,
+                                                     for_backward=True), dtype=torch.uint8, device=dev)
+    o, lse = api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal,
+                                  workspace=ws)
     dq, dk, dv, dwq, dwk = api.st_rope_attn_bwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o, lse, do,
-                                                mask=mask, causal=inp.causal)
+                                                mask=mask, causal=inp.causal, workspace=ws, reuse_tables=True)
     api.st_check_status()
     torch.cuda.synchronize()
     assert torch.isfinite(dwq).all() and torch.isfinite(dwk).all()
-    got = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv)
+    got = dict(o=o, lse=lse, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk)
     for (b, h) in heads:
         ref = head_oracle(inp, b, h, None if mask_heads is None else mask_heads[(b, h)])
         print(f"head ({b},{h})")
@@ -56,8 +60,17 @@ def run_full(api, inp, heads, mask_dev=None, mask_heads=None):
 def test_flux1_1024_all_true_mask(cuda_lib):
     inp = wl.make("flux1_1024")
     cuda_lib.st_reset_stats()
-    run_full(cuda_lib, inp, heads=[(0, 0), (0, 23)])
-    assert cuda_lib.st_get_stats()["mask_all_true_skipped"] == 2
+    got = run_full(cuda_lib, inp, heads=[(0, 0), (0, 23)])
+    # the forward detects the all-True mask; the backward reuses its tile classes
+    assert cuda_lib.st_get_stats()["mask_all_true_skipped"] == 1
+    # the norm-weight gradients sum over all 24 heads: the oracle's full sums
+    # (an all-True mask is the same as none, which the oracle's pins establish)
+    args = (f64(inp.q), f64(inp.k), f64(inp.v), f64(inp.wq), f64(inp.wk), inp.eps, inp.ids.numpy(), inp.axes,
+            inp.theta)
+    _, _, _, dwq, dwk = oracle.bwd(*args, f64(inp.do))
+    for key, ref in (("dwq", dwq), ("dwk", dwk)):
+        ma, rf = compare(key, got[key], ref, check_max=False)
+        print(f"  {key:4s} max_abs={ma:.3e} rel_fro={rf:.3e}")
 
 
 def test_flux1_padded_batch_mixed_dtype(cuda_lib):

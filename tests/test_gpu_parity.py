@@ -187,6 +187,33 @@ def test_deterministic_dk_dv_dw(cuda_lib):
         assert torch.equal(a[k], b[k]), k
 
 
+@pytest.mark.parametrize("mask", ["none", "bool", "additive"])
+def test_backward_reusing_forward_tables(cuda_lib, mask):
+    """A backward that reuses the forward's tables and mask tile classes from a
+    shared workspace gives the same results as one that rebuilds them."""
+    kw = dict(mask_shape=(2, 1, 1, 300)) if mask == "bool" else dict(mask_shape=(2, 3, 300, 300))
+    inp = wl.make_custom(2, 3, 128, 300, axes=(16, 56, 56), seed=43, mask={"none": "none", "bool": "bool_random",
+                                                                           "additive": "additive"}[mask],
+                         ids=torch.randint(0, 40, (2, 300, 3), dtype=torch.int32), **kw)
+    d = to_dev(inp)
+    ref = gpu_fwd_bwd(cuda_lib, inp, d=d)
+    ws = torch.empty(cuda_lib.st_rope_attn_workspace_size(d["q"], d["k"], d["v"], d["ids"], inp.axes, inp.theta,
+                                                          d["mask"], False, for_backward=True),
+                     dtype=torch.uint8, device="cuda")
+    ws.fill_(0xAB)
+    o, lse = cuda_lib.st_rope_attn_fwd(d["q"], d["k"], d["v"], d["wq"], d["wk"], inp.eps, d["ids"], inp.axes,
+                                       inp.theta, mask=d["mask"], workspace=ws)
+    got = dict(o=o, lse=lse)
+    got["dq"], got["dk"], got["dv"], got["dwq"], got["dwk"] = cuda_lib.st_rope_attn_bwd(
+        d["q"], d["k"], d["v"], d["wq"], d["wk"], inp.eps, d["ids"], inp.axes, inp.theta, o, lse, d["do"],
+        mask=d["mask"], workspace=ws, reuse_tables=True)
+    cuda_lib.st_check_status()
+    for k in ("o", "lse", "dk", "dv", "dwk"):
+        assert torch.equal(got[k], ref[k]), k
+    compare("dq", got["dq"], ref["dq"].double().cpu().numpy(), atol=1e-2, rel_fro=1e-3)
+    compare("dwq", got["dwq"], ref["dwq"].double().cpu().numpy(), check_max=False, rel_fro=1e-5)
+
+
 def test_empty_inputs(cuda_lib):
     inp = wl.make_custom(1, 2, 128, 0, 0, axes=(128,), seed=39)
     d = to_dev(inp)
