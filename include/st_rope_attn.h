@@ -168,9 +168,20 @@ ST_API size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k
                                    const st_tensor* mask, int causal, const st_rope* rope, int for_backward);
 
 /* Forward.
- *  q, k:   [B, S_q, H, D] / [B, S_kv, H_kv, D], bf16 or fp32 (fp32 is rounded
- *          to bf16 after the norm and rotation, as an autocast SDPA would).
- *  v:      [B, S_kv, H_kv, D] bf16.
+ *  q, k:   [B, S_q, H, D] / [B, S_kv, H_kv, D], bf16, fp16 or fp32 (q and k
+ *          of one dtype).
+ *  v:      [B, S_kv, H_kv, D], bf16, fp16 or fp32.
+ *          Dtype combinations ("Metal Flash Attention", section
+ *          "Requirements": FP32 runs natively, FP16/BF16 on low-precision
+ *          kernels):
+ *          - bf16 (or fp16) q, k, v: tensor-core MMAs on bf16 (fp16)
+ *            operands with fp32 accumulation, softmax and norm arithmetic;
+ *          - fp32 q, k with bf16 or fp16 v (the autocast mix): q and k are
+ *            normalised and rotated in fp32, then rounded to v's type for the
+ *            MMAs, as an autocast SDPA would;
+ *          - fp32 q, k, v: every product and sum in fp32 on the CUDA cores
+ *            (exact-fp32 kernels, far slower than the tensor cores).
+ *          16-bit q/k of a type other than v's are rejected (ST_ERR_DTYPE).
  *          H_kv divides H (grouped K/V heads; H_kv = H is plain multi-head
  *          attention): query head h attends with K/V head h / (H / H_kv), and
  *          k is normalised and rotated at the K/V head count ("Metal Flash

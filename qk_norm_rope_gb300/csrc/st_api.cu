@@ -15,6 +15,7 @@
 
 #include "st_rope_attn.h"
 #include "st_aux.h"
+#include "st_f32.h"
 #include "st_kernels.h"
 
 namespace st {
@@ -237,6 +238,7 @@ struct Plan {
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
          off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
   int n_dwq = 0, n_dwk = 0;
+  bool f32 = false;  // q, k, v all fp32: the exact-fp32 kernels
 };
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -256,7 +258,8 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     return fail(ST_ERR_SHAPE, "sizes out of range");
   if (s.D != kD) return fail(ST_ERR_UNSUPPORTED, "head dimension %d is not supported (this build handles D=128)", s.D);
   st_status st;
-  const unsigned qk_types = bit(ST_BF16) | bit(ST_F16) | bit(ST_F32), v_types = bit(ST_BF16) | bit(ST_F16);
+  const unsigned qk_types = bit(ST_BF16) | bit(ST_F16) | bit(ST_F32);
+  const unsigned v_types = bit(ST_BF16) | bit(ST_F16) | bit(ST_F32);
   if ((st = check_bshd(q, "q", s.B, s.Sq, s.H, s.D, qk_types, &P->q)) != ST_OK) return st;
   // grouped K/V heads: k and v carry H_kv heads, H a multiple of H_kv
   s.Hkv = static_cast<int>(k->shape[2]);
@@ -265,10 +268,12 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
   if ((st = check_bshd(k, "k", s.B, s.Skv, s.Hkv, s.D, qk_types, &P->k)) != ST_OK) return st;
   if ((st = check_bshd(v, "v", s.B, s.Skv, s.Hkv, s.D, v_types, &P->v)) != ST_OK) return st;
   // the MMA operands take v's 16-bit type; 16-bit q/k must have it already
-  // (they are staged as raw operand rows), fp32 q/k are cast to it on load
+  // (they are staged as raw operand rows), fp32 q/k are cast to it on load;
+  // fp32 v (with fp32 q/k) selects the exact-fp32 kernels
   if (q->dtype != k->dtype) return fail(ST_ERR_DTYPE, "q and k must have the same dtype");
   if (q->dtype != ST_F32 && q->dtype != v->dtype)
     return fail(ST_ERR_DTYPE, "16-bit q/k must have v's dtype (or be fp32, cast on load)");
+  P->f32 = v->dtype == ST_F32;
   if (!rope) return fail(ST_ERR_INVALID_ARG, "rope is NULL");
   if (rope->cos || rope->sin) {  // the pages' table form
     if (rope->ids || rope->ids_k) return fail(ST_ERR_INVALID_ARG, "rope: give either ids or cos/sin tables, not both");
@@ -350,11 +355,13 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     P->off_delta = off;
     off = align_up(off + (size_t)s.B * s.H * s.Sq * sizeof(float), 256);
     P->off_dqacc = off;
-    off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * sizeof(float), 256);
-    P->n_dwk = s.B * s.Hkv * P->nKt;  // one partial per backward CTA (key tile, K/V head, batch)
+    if (!P->f32) off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * sizeof(float), 256);
+    P->n_dwk = s.B * s.Hkv * P->nKt * 4;  // per backward CTA (key tile, K/V head, batch) and 32-row quarter
+    if (P->f32) P->n_dwk = s.B * s.Hkv * ((s.Skv + kF32Tile - 1) / kF32Tile);  // per fp32 key tile
     P->off_dwk = off;
     off = align_up(off + (size_t)P->n_dwk * kD * sizeof(float), 256);
     P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kTile - 1) / kTile);
+    if (P->f32) P->n_dwq = s.B * s.H * ((s.Sq + kF32Tile - 1) / kF32Tile);  // per fp32 query tile
     P->off_dwq = off;
     off = align_up(off + (size_t)P->n_dwq * kD * sizeof(float), 256);
     P->off_dwscratch = off;
@@ -586,6 +593,47 @@ st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* ma
   return ST_OK;
 }
 
+// The forward's launches (tables, mask tile classes, attention) on a
+// validated call, with `ws` the workspace (or the built-in scratch).
+st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k, const st_tensor* v,
+                          const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps, const st_rope* rope,
+                          const st_tensor* mask, int causal, float scale, st_tensor* o, const RowTensor& ro,
+                          st_tensor* lse, uint8_t* ws, cudaStream_t stream) {
+  st_status st;
+  Dev dev;
+  if ((st = device_globals(&dev)) != ST_OK) return st;
+  if (P.f32) {
+    F32Params fp;
+    memset(&fp, 0, sizeof(fp));
+    fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
+    fp.c.mask = mask ? mask->data : nullptr;
+    fp.o = static_cast<float*>(o->data);
+    fp.o_sb = ro.sb; fp.o_ss = ro.ss; fp.o_sh = ro.sh;
+    fp.lse = static_cast<float*>(lse->data);
+    if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+    return cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_f32_fwd(fp, stream); }),
+                      "fp32 forward kernel launch");
+  }
+  FwdParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
+  fp.c.mask = mask ? mask->data : nullptr;
+  fp.o = o->data;
+  fp.o_sb = ro.sb;
+  fp.o_ss = ro.ss;
+  fp.o_sh = ro.sh;
+  fp.o_dt = ro.dt;
+  fp.lse = static_cast<float*>(lse->data);
+  if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
+  fp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
+  if (fp.qk_tma) {
+    if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
+    if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
+  }
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  return cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -623,30 +671,12 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
     ++h_fwd_calls;
     return ST_OK;
   }
-  Dev dev;
-  if ((st = device_globals(&dev)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  FwdParams fp;
-  memset(&fp, 0, sizeof(fp));
-  fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
-  fp.c.mask = mask ? mask->data : nullptr;
-  fp.o = o->data;
-  fp.o_sb = ro.sb;
-  fp.o_ss = ro.ss;
-  fp.o_sh = ro.sh;
-  fp.o_dt = ro.dt;
-  fp.lse = static_cast<float*>(lse->data);
-  if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
-  fp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
-  if (fp.qk_tma) {
-    if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
-    if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
-  }
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
-  if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch")) != ST_OK) return st;
+  if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
+                            static_cast<uint8_t*>(workspace), stream)) != ST_OK)
+    return st;
   ++h_fwd_calls;
-  if (q->dtype == ST_F32) ++h_mixed;
+  if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
   return ST_OK;
 }
 
@@ -689,7 +719,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   BwdParams bp;
   memset(&bp, 0, sizeof(bp));
-  if (P.nKt > 0) {
+  if (P.nKt > 0 && !P.f32) {
     if ((st = encode_rows_map(v, &bp.tmap_v, &bp.v_s_first)) != ST_OK) return st;
     if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first, kTile / 2)) != ST_OK)
       return st;
@@ -711,7 +741,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   if (!reuse && (st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
 
   float* delta = reinterpret_cast<float*>(ws + P.off_delta);
-  float* dq_acc = reinterpret_cast<float*>(ws + P.off_dqacc);
+  float* dq_acc = P.f32 ? nullptr : reinterpret_cast<float*>(ws + P.off_dqacc);  // the fp32 path needs none
   if ((int64_t)s.B * s.Sq * s.H > 0) {
     PreParams pp;
     memset(&pp, 0, sizeof(pp));
@@ -725,7 +755,30 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     pp.B = s.B; pp.H = s.H; pp.Sq = s.Sq;
     if ((st = cuda_check(launch_counted(ST_K_BWD_PRE, stream, [&] { return launch_bwd_pre(pp, stream); }), "backward pre launch")) != ST_OK) return st;
   }
-  if (P.nKt > 0) {
+  if (P.f32) {
+    // exact fp32: a kernel over key tiles (dk, dv), one over query tiles (dq)
+    F32Params fp;
+    memset(&fp, 0, sizeof(fp));
+    fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
+    fp.c.mask = mask ? mask->data : nullptr;
+    fp.lse_in = static_cast<const float*>(lse->data);
+    fp.delta = delta;
+    fp.dout = static_cast<const float*>(d_o->data);
+    fp.do_sb = rdo.sb; fp.do_ss = rdo.ss; fp.do_sh = rdo.sh;
+    fp.dq = static_cast<float*>(dq->data); fp.dq_sb = rdq.sb; fp.dq_ss = rdq.ss; fp.dq_sh = rdq.sh;
+    fp.dk = static_cast<float*>(dk->data); fp.dk_sb = rdk.sb; fp.dk_ss = rdk.ss; fp.dk_sh = rdk.sh;
+    fp.dv = static_cast<float*>(dv->data); fp.dv_sb = rdv.sb; fp.dv_ss = rdv.ss; fp.dv_sh = rdv.sh;
+    fp.dwq_part = reinterpret_cast<float*>(ws + P.off_dwq);
+    fp.dwk_part = reinterpret_cast<float*>(ws + P.off_dwk);
+    if (s.Skv > 0 && (st = cuda_check(launch_counted(ST_K_BWD, stream, [&] { return launch_f32_bwd_kv(fp, stream); }),
+                                      "fp32 backward (keys) launch")) != ST_OK)
+      return st;
+    if ((int64_t)s.B * s.Sq * s.H > 0 &&
+        (st = cuda_check(launch_counted(ST_K_DQ_POST, stream, [&] { return launch_f32_bwd_q(fp, stream); }),
+                         "fp32 backward (queries) launch")) != ST_OK)
+      return st;
+  }
+  if (P.nKt > 0 && !P.f32) {
     fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &bp.c);
     bp.c.mask = mask ? mask->data : nullptr;
     bp.dout = d_o->data;
@@ -737,10 +790,13 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
       return st;
     bp.dv = dv->data; bp.dv_sb = rdv.sb; bp.dv_ss = rdv.ss; bp.dv_sh = rdv.sh; bp.dv_dt = rdv.dt;
     bp.dk = dk->data; bp.dk_sb = rdk.sb; bp.dk_ss = rdk.ss; bp.dk_sh = rdk.sh; bp.dk_dt = rdk.dt;
+    // the epilogue stores dv (and 16-bit dk) rows by TMA
+    if ((st = encode_rows_map(dv, &bp.tmap_dv, &bp.dv_s_first)) != ST_OK) return st;
+    if (bp.qk_tma && (st = encode_rows_map(dk, &bp.tmap_dk, &bp.dk_s_first)) != ST_OK) return st;
     bp.dwk_part = reinterpret_cast<float*>(ws + P.off_dwk);
     if ((st = cuda_check(launch_counted(ST_K_BWD, stream, [&] { return launch_bwd(bp, stream); }), "backward kernel launch")) != ST_OK) return st;
   }
-  if ((int64_t)s.B * s.Sq * s.H > 0) {
+  if ((int64_t)s.B * s.Sq * s.H > 0 && !P.f32) {
     PostParams pq;
     memset(&pq, 0, sizeof(pq));
     pq.dq_acc = dq_acc;
@@ -766,7 +822,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   dp.dwk = static_cast<float*>(d_k_norm_w->data);
   if ((st = cuda_check(launch_counted(ST_K_DW, stream, [&] { return launch_dw_reduce(dp, stream); }), "weight-gradient reduce launch")) != ST_OK) return st;
   ++h_bwd_calls;
-  if (q->dtype == ST_F32) ++h_mixed;
+  if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
   return ST_OK;
 }
 
@@ -839,32 +895,12 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   }
   void* scratch = nullptr;
   if ((st = noalloc_scratch_address(&scratch)) != ST_OK) return st;
-  Dev dev;
-  if ((st = device_globals(&dev)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-  uint8_t* ws = static_cast<uint8_t*>(scratch);
-  FwdParams fp;
-  memset(&fp, 0, sizeof(fp));
-  fill_common(P, q_norm_w, k_norm_w, eps, causal, scale, ws, dev, &fp.c);
-  fp.c.mask = mask ? mask->data : nullptr;
-  fp.o = o->data;
-  fp.o_sb = ro.sb;
-  fp.o_ss = ro.ss;
-  fp.o_sh = ro.sh;
-  fp.o_dt = ro.dt;
-  fp.lse = static_cast<float*>(lse->data);
-  if (P.nKt > 0 && (st = encode_rows_map(v, &fp.tmap_v, &fp.v_s_first)) != ST_OK) return st;
-  fp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
-  if (fp.qk_tma) {
-    if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
-    if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
-  }
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
-  if ((st = cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }),
-                       "forward kernel launch")) != ST_OK)
+  if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
+                            static_cast<uint8_t*>(scratch), stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
-  if (q->dtype == ST_F32) ++h_mixed;
+  if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
   return ST_OK;
 }
 

@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Pr
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
     const int64_t row = row0 + u;
-    if (row < nrows) reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (row < nrows && p.dq_acc) reinterpret_cast<float4*>(p.dq_acc + row * kD)[lane] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   float acc[kPreRows];
 #pragma unroll

@@ -54,7 +54,7 @@ struct PreParams {
   const void* dout;
   int64_t do_sb, do_ss, do_sh;
   float* delta;   // [B, H, Sq]
-  float* dq_acc;  // [B, Sq, H, D]
+  float* dq_acc;  // [B, Sq, H, D], zeroed (nullptr: none to zero)
   unsigned* ctrl; // control words: the weight-gradient counters are cleared
   int B, H, Sq;
 };

@@ -83,6 +83,7 @@ constexpr uint32_t kOffW = kOffBar + kBarBytes;                 // q norm weight
 constexpr uint32_t kBwdSmem = kOffW + kD * 4;                   // the base must be 1024-byte aligned
 static_assert(kBwdSmem <= 232448, "backward shared memory exceeds the per-block limit");
 static_assert(kProlThreads >= kSub, "one prologue thread per stat row");
+static_assert(kQStages * 2 * kSub >= 4 * kTile, "the epilogue's row-sum exchange fits in the stat area");
 
 enum {
   kBarKRaw = 0,                          // raw k rows landed (TMA)
@@ -226,12 +227,17 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
 // boxes over kOffK..kOffV) and the row's fp32 (cos, sin) (four 32-float boxes
 // at kOffQ) were staged by TMA, 128B-swizzled. The two row sums (x.x, x.g')
 // are completed through `ex` in shared memory, between named barriers of the
-// eight epilogue warps. colsum[q] receives, in lane l, the sum of dy x r at
-// column 64 hh + 32 q + l over the warp's 32 rows.
+// eight epilogue warps; sWk holds the k norm weights. A 16-bit dk row goes to
+// `stage` (the operand-tile layout, stored by TMA afterwards); an fp32 one is
+// stored directly. Returns, in lane l, the sums of dy x r at columns 64 hh + l
+// (x) and 64 hh + 32 + l (y) over the warp's 32 rows.
+// Out of line: it runs once per CTA, and inlined it would spread the roles'
+// hot loops over more instruction-cache lines.
 template <bool QKT, bool F16>
-__device__ __forceinline__ void dk_half_rows(const BwdParams& P, const uint8_t* sm, uint32_t tacc, bool have, int b,
-                                             int hk, int j, int r, int hh, bool key_ok, int lane, float* ex,
-                                             float (&colsum)[2]) {
+__device__ __noinline__ float2 dk_half_rows(const BwdParams& P, const uint8_t* sm, uint32_t tacc, bool have, int b,
+                                               int hk, int j, int r, int hh, bool key_ok, int lane, float* ex,
+                                               const float* sWk, uint8_t* stage) {
+  float colsum[2];
   const Common& c = P.c;
   // the chunk (16 bytes) of this thread's half row holding dims 64 hh + 4 t .. +3 (fp32)
   // or 64 hh + 8 t .. +7 (bf16)
@@ -275,7 +281,7 @@ __device__ __forceinline__ void dk_half_rows(const BwdParams& P, const uint8_t* 
   named_bar(kBarIdEpi, kEpiThreads);
   const float rr = rsqrtf((ex[r] + ex[kTile + r]) * (1.0f / kD) + c.eps);
   const float sc = c.scale;
-  const float4* w4 = reinterpret_cast<const float4*>(c.wk + 64 * hh);
+  const float4* w4 = reinterpret_cast<const float4*>(sWk + 64 * hh);
   float xg = 0.f;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
@@ -302,7 +308,7 @@ __device__ __forceinline__ void dk_half_rows(const BwdParams& P, const uint8_t* 
         load_x8(d0, x8);
         const float4 t0 = tab_chunk(d0 >> 2), t1 = tab_chunk((d0 >> 2) + 1);
         const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-        const float4 wa = __ldg(w4 + (d0 >> 2)), wb = __ldg(w4 + (d0 >> 2) + 1);
+        const float4 wa = w4[d0 >> 2], wb = w4[(d0 >> 2) + 1];
         const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -323,11 +329,47 @@ __device__ __forceinline__ void dk_half_rows(const BwdParams& P, const uint8_t* 
       }
       if (pass == 0) {
         colsum[q] = warp_reduce_scatter32(u, lane);
+      } else if (QKT) {
+        // 16-bit dk: chunks 4q .. 4q+3 of the row's half hh in the staging tile
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(stage + hh * kHalfBytes + sw128_off(r, 4 * q + c4)) =
+              make_uint4(pack16<F16>(u[8 * c4], u[8 * c4 + 1]), pack16<F16>(u[8 * c4 + 2], u[8 * c4 + 3]),
+                         pack16<F16>(u[8 * c4 + 4], u[8 * c4 + 5]), pack16<F16>(u[8 * c4 + 6], u[8 * c4 + 7]));
       } else if (key_ok) {
         store_chunk32(P.dk, b * P.dk_sb + (int64_t)j * P.dk_ss + hk * P.dk_sh, P.dk_dt, 2 * hh + q, u);
       }
     }
   }
+  return make_float2(colsum[0], colsum[1]);
+}
+
+// P^T of this thread's key against 32 queries iq0 .. iq0 + 31 on a sub-tile
+// that needs masking (a bool tile with False elements, an additive mask
+// broadcast over the queries, the causal diagonal, rows past S_q). Out of
+// line: sub-tiles without masking never run it, and inlined it would spread
+// the compute warps' hot loop over more instruction-cache lines.
+// It reads the warp's 32 S^T columns at TMEM address tS and writes P^T (16-bit
+// pairs) over the first 16 of them itself, so that no array crosses the call.
+template <int MK, bool CAUSAL, bool F16>
+__device__ __noinline__ void p_masked(const Common& c, uint32_t tS, float key_term, int b, int h, int iq0, int j,
+                                      bool key_ok, uint8_t flag, bool mask_bcast_q, const float* lse) {
+  uint32_t sv[32], pw[16];
+  tmem_ld32(tS, sv);
+#pragma unroll
+  for (int t2 = 0; t2 < 16; ++t2) {
+    float p2[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = 2 * t2 + e;
+      const float s2 = score2<MK, CAUSAL>(c, __uint_as_float(sv[t]), key_term, b, h, iq0 + t, j, key_ok, flag,
+                                          mask_bcast_q);
+      p2[e] = ex2(s2 - lse[t]);  // LSE = +inf for rows without keys or past S_q: P = 0
+    }
+    pw[t2] = pack16<F16>(p2[0], p2[1]);
+  }
+  tmem_st16(tS, pw);
+  tmem_st_wait();
 }
 
 // ELEM: the mask varies along the queries (per-element terms); a mask that is
@@ -456,7 +498,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
                            (!CAUSAL || iq0 >= kt * kTile + kTile - 1);
         // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), bf16 into TMEM
         uint32_t pw[16];
-        {
+        if (!plain && !ELEM) {
+          // masked sub-tile, out of line; P^T comes back from TMEM for dS^T
+          p_masked<MK, CAUSAL, F16>(c, tS + q0, key_term, b, h, iq0 + q0, j, key_ok, flag, mask_bcast_q, st_lse + q0);
+          tmem_ld16_issue(tS + q0, pw);
+          tmem_ld_wait16(pw);
+        } else {
           uint32_t sv[32];
           tmem_ld32(tS + q0, sv);
           if (plain) {
@@ -471,20 +518,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
               pw[2 * v4] = pack16<F16>(ex2(x01.x), ex2(x01.y));
               pw[2 * v4 + 1] = pack16<F16>(ex2(x23.x), ex2(x23.y));
             }
-          } else if constexpr (!ELEM) {
-#pragma unroll
-            for (int t2 = 0; t2 < 16; ++t2) {
-              float p2[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int t = 2 * t2 + e;
-                const float s2 = score2<MK, CAUSAL>(c, __uint_as_float(sv[t]), key_term, b, h, iq0 + q0 + t, j, key_ok,
-                                                    flag, mask_bcast_q);
-                p2[e] = ex2(s2 - st_lse[q0 + t]);  // LSE = +inf for rows without keys or past S_q: P = 0
-              }
-              pw[t2] = pack16<F16>(p2[0], p2[1]);
-            }
-          } else {
+          } else if constexpr (ELEM) {
             // per-element mask terms of the 32 queries, 16 at a time (loads pinned)
             const bool elem_mask = key_ok && flag != kTileAllFalse && !(MK == kMaskBool && flag == kTileAllTrue);
 #pragma unroll
@@ -520,8 +554,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
               }
             }
           }
+          tmem_st16(tS + q0, pw);  // the first 16 of the warp's own 32 S^T columns
         }
-        tmem_st16(tS + q0, pw);  // the first 16 of the warp's own 32 S^T columns
         // ---- dS^T = P^T (dP^T - Delta), bf16 into shared memory (row r, K-major)
         if (!(ok = wait_bar_warp(&bars[kBarDPFull + bf], (n >> 1) & 1, abort_flag, budget))) break;
         tc_fence_after();
@@ -554,32 +588,41 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     }
     // ---- epilogue of the eight compute warps: warp w holds key rows
     // 32 (w % 4) .. (its TMEM lanes) and head dims [64 hq, 64 hq + 64) of dV
-    // and dK'. Once every MMA has completed, the K tile and the Q' ring are
-    // free: the raw k rows and the tile's fp32 (cos, sin) rows are staged
-    // there by TMA while dV is written; then dk (inverse rotation + RMSNorm
-    // backward) and the CTA's partial sums of the k norm-weight gradient.
+    // and dK'. Once every MMA has completed, the K tile, the Q' ring and the
+    // dO ring are free: the raw k rows and the tile's fp32 (cos, sin) rows are
+    // staged by TMA (K tile, Q' ring) while dV is laid out in the dO ring and
+    // stored by TMA; then dk (inverse rotation + RMSNorm backward) is laid out
+    // in the dS buffers and stored by TMA (16-bit k; fp32 rows are stored
+    // directly), and each warp writes its partial sums of the k norm-weight
+    // gradient.
     if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
     // one decision for the eight warps (they share named barriers below)
-    if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok)) {
+    if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
       tc_fence_after();
-      if (tid == 0 && !phantom) {
+      float* ex = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed: row-sum exchange (2 KB)
+      float* sWk = reinterpret_cast<float*>(sm + kOffW);     // the Q' prologue is done with the q weights
+      const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
+      if (tid == 0) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars[kBarEpi], (QKT ? kTileBytes : 2 * kTileBytes) + 4 * kBoxBytes);
-        const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
         if constexpr (QKT) {
-          tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarEpi], 0, y, z, b);
-          tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarEpi], 64, y, z, b);
+          tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarEpi], 0, ty, tz, b);
+          tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarEpi], 64, ty, tz, b);
         } else {
 #pragma unroll
-          for (int x = 0; x < 4; ++x) tma_load_4d(sm + kOffK + x * kBoxBytes, &P.tmap_k, &bars[kBarEpi], 32 * x, y, z, b);
+          for (int x = 0; x < 4; ++x)
+            tma_load_4d(sm + kOffK + x * kBoxBytes, &P.tmap_k, &bars[kBarEpi], 32 * x, ty, tz, b);
         }
         const int trow = (c.tab_k_sb != 0 ? b * c.Skv : 0) + kt * kTile;
 #pragma unroll
         for (int x = 0; x < 4; ++x) tma_load_2d(sm + kOffQ + x * kBoxBytes, &P.tmap_tab_k, &bars[kBarEpi], 32 * x, trow);
       }
+      if (tid < kD) sWk[tid] = __ldg(c.wk + tid);
       {
+        // dV: this thread's 64 columns of row r, 16-bit, into the dO ring in
+        // the operand-tile layout
+        uint8_t* stage = sm + kOffDO + hq * kHalfBytes;
         const uint32_t tacc = tmem + 256 + lanebits + 64 * hq;
-        const int64_t off = b * P.dv_sb + (int64_t)j * P.dv_ss + hk * P.dv_sh;
 #pragma unroll 1
         for (int q = 0; q < 2; ++q) {
           uint32_t v[32];
@@ -589,26 +632,41 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 #pragma unroll
             for (int t = 0; t < 32; ++t) v[t] = 0u;
           }
-          float y[32];
 #pragma unroll
-          for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(v[t]);
-          if (key_ok) store_chunk32(P.dv, off, P.dv_dt, 2 * hq + q, y);
+          for (int c4 = 0; c4 < 4; ++c4)
+            *reinterpret_cast<uint4*>(stage + sw128_off(r, 4 * q + c4)) =
+                make_uint4(pack16<F16>(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
+                           pack16<F16>(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
+                           pack16<F16>(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
+                           pack16<F16>(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
         }
+        fence_proxy_async_smem();
       }
-      if (!phantom &&
-          !named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
-        float* ex = reinterpret_cast<float*>(sm + kOffDS);  // the dS buffers are idle: row-sum exchange
-        float* red = ex + 4 * kTile;                          // and the four row groups' column sums
-        float colsum[2];
-        dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq, key_ok, lane_id, ex,
-                          colsum);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) red[qd * kD + 64 * hq + 32 * q + lane_id] = colsum[q];
-        named_bar(kBarIdEpi, kEpiThreads);
-        if (tid < kD) {  // column tid, the row groups added in a fixed order
-          const float sum = ((red[tid] + red[kD + tid]) + red[2 * kD + tid]) + red[3 * kD + tid];
-          P.dwk_part[(((int64_t)b * c.Hkv + hk) * c.nKt + kt) * kD + tid] = sum;
+      if (!named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
+        if (tid == 0) {  // the staged dV rows (rows past S_kv are not written)
+          const int vy = P.dv_s_first ? kt * kTile : hk, vz = P.dv_s_first ? hk : kt * kTile;
+          tma_store_4d(&P.tmap_dv, sm + kOffDO, 0, vy, vz, b);
+          tma_store_4d(&P.tmap_dv, sm + kOffDO + kHalfBytes, 64, vy, vz, b);
+          bulk_commit_group();
         }
+        const float2 colsum = dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq,
+                                                     key_ok, lane_id, ex, sWk, sm + kOffDS);
+        // this warp's column sums over its 32 rows: one partial row per warp
+        // quarter (rows 32 qd ..), added in a fixed order by the reduction
+        float* part = P.dwk_part + ((((int64_t)b * c.Hkv + hk) * c.nKt + kt) * 4 + qd) * kD + 64 * hq;
+        part[lane_id] = colsum.x;
+        part[32 + lane_id] = colsum.y;
+        if constexpr (QKT) {
+          fence_proxy_async_smem();
+          named_bar(kBarIdEpi, kEpiThreads);
+          if (tid == 0) {
+            const int ky = P.dk_s_first ? kt * kTile : hk, kz = P.dk_s_first ? hk : kt * kTile;
+            tma_store_4d(&P.tmap_dk, sm + kOffDS, 0, ky, kz, b);
+            tma_store_4d(&P.tmap_dk, sm + kOffDS + kHalfBytes, 64, ky, kz, b);
+            bulk_commit_group();
+          }
+        }
+        if (tid == 0) bulk_wait_read_all();  // the staged rows are read before the CTA may exit
       }
     }
   } else if (warp < kWarpDrain0 + kDrainWarps) {

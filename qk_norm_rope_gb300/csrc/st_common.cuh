@@ -82,8 +82,10 @@ struct BwdParams {
   CUtensorMap tmap_q;   // raw q rows, 32-row boxes (16-bit only; see qk_tma)
   CUtensorMap tmap_k;   // raw k rows, 128-row boxes (16-bit: 64 columns; fp32: 32 columns, epilogue only)
   CUtensorMap tmap_tab_k;  // the fp32 (cos, sin) table of the keys as [Bt_k * Skv, 128] floats, 32 x 128 boxes
+  CUtensorMap tmap_dv;     // dv rows, 128-row boxes (TMA store of the epilogue)
+  CUtensorMap tmap_dk;     // dk rows, 128-row boxes (16-bit k only)
   CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 64 rows (reduce target)
-  int v_s_first, do_s_first, q_s_first, k_s_first;
+  int v_s_first, do_s_first, q_s_first, k_s_first, dv_s_first, dk_s_first;
   int qk_tma;
   const void* dout;
   int64_t do_sb, do_ss, do_sh;
@@ -97,7 +99,7 @@ struct BwdParams {
   void* dk;            // dk, finished in the kernel's epilogue (inverse rotation + RMSNorm backward)
   int64_t dk_sb, dk_ss, dk_sh;
   int dk_dt;
-  float* dwk_part;     // [B, Hkv, nKt, D]: per-CTA partial sums of the k norm-weight gradient
+  float* dwk_part;     // [B, Hkv, nKt, 4, D]: partial sums of the k norm-weight gradient per CTA and row quarter
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }

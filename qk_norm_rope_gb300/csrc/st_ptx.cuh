@@ -140,6 +140,15 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, const 
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
 }
+// Store of a shared-memory box into a global tensor through a tiled tensor
+// map, tracked by the issuing thread's bulk async-group. Rows outside the
+// tensor are not written.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, const void* src, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk group of this thread has finished reading
 // its shared-memory source.

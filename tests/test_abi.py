@@ -129,7 +129,8 @@ def test_dtype_errors():
     c = Call(); c.q.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "q and k must have the same dtype")
     c = Call(); c.q.dtype = c.k.dtype = api.ST_F16; expect(c, api.ST_ERR_DTYPE, "v's dtype")
     c = Call(); c.q.dtype = c.k.dtype = api.ST_I32; expect(c, api.ST_ERR_DTYPE, "q")
-    c = Call(); c.v.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "v")
+    c = Call(); c.v.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "v's dtype")
+    c = Call(); c.v.dtype = api.ST_I32; expect(c, api.ST_ERR_DTYPE, "v")
     c = Call(); c.o.dtype = api.ST_F32; expect(c, api.ST_ERR_DTYPE, "o")
     c = Call(); c.wk.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "k_norm_w")
     c = Call(); c.ids.dtype = api.ST_BF16; expect(c, api.ST_ERR_DTYPE, "ids")
@@ -137,9 +138,10 @@ def test_dtype_errors():
 
 
 def test_operand_types_accepted():
-    """bf16 throughout, fp16 throughout, and fp32 q/k with either 16-bit v."""
+    """bf16 throughout, fp16 throughout, fp32 q/k with either 16-bit v, and
+    fp32 throughout (the exact-fp32 kernels)."""
     for qk, v in ((api.ST_BF16, api.ST_BF16), (api.ST_F16, api.ST_F16), (api.ST_F32, api.ST_BF16),
-                  (api.ST_F32, api.ST_F16)):
+                  (api.ST_F32, api.ST_F16), (api.ST_F32, api.ST_F32)):
         c = Call()
         c.q.dtype = c.k.dtype = qk
         c.v.dtype = c.o.dtype = v
