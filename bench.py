@@ -166,6 +166,19 @@ def load_traffic(kernel: str):
     return None, None
 
 
+def device_mask(inp, name, dev):
+    """The workload's mask on the device; a per-head additive mask is built one
+    (b, h) slice at a time from the seeded generator the parity tests use."""
+    if not inp.meta.get("mask_per_head"):
+        return None if inp.mask is None else inp.mask.to(dev)
+    B, Sq, H, _ = inp.q.shape
+    mask = torch.empty(B, H, Sq, inp.k.shape[1], dtype=torch.float32, device=dev)
+    for b in range(B):
+        for h in range(H):
+            mask[b, h].copy_(wl.additive_mask_head(name, b, h))
+    return mask
+
+
 def run_ours(args, rank, world, dev):
     from qk_norm_rope_gb300 import api
 
@@ -175,12 +188,7 @@ def run_ours(args, rank, world, dev):
     step_flops = f_fwd + f_bwd
     g = lambda t: None if t is None else t.to(dev)
     q, k, v, do, wq, wk, ids = (g(t) for t in (inp.q, inp.k, inp.v, inp.do, inp.wq, inp.wk, inp.ids))
-    mask = g(inp.mask)
-    if inp.meta.get("mask_per_head"):
-        mask = torch.empty(B, H, Sq, inp.k.shape[1], dtype=torch.float32, device=dev)
-        for b in range(B):
-            for h in range(H):
-                mask[b, h].copy_(wl.additive_mask_head(args.workload, b, h))
+    mask = device_mask(inp, args.workload, dev)
     o = torch.empty(B, Sq, H, D, dtype=v.dtype, device=dev)
     lse = torch.empty(B, H, Sq, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -298,6 +306,12 @@ def run_ours(args, rank, world, dev):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(inp, args.workload, budget_s=args.cpu_seconds)
 
+    sweep = None
+    if world == 1 and not args.no_sweep and args.workload == "flux1_1024":
+        del q, k, v, do, dq, dk, dv, ws, o, lse, mask
+        torch.cuda.empty_cache()
+        sweep = workload_sweep(dev, flush)
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -313,7 +327,100 @@ def run_ours(args, rank, world, dev):
         "roofline": roof, "kernels": per_kernel, "gpu_launches": int(launches), "clocks": clk, "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if sweep is not None:
+        line["workloads"] = sweep
     return line
+
+
+# The other configurations and the pages' probe shapes, measured briefly after
+# the headline workload under the same rules (warm-up, L2 flush before every
+# timed step, CUDA events); the Z-Image DiT shape also runs the eager torch
+# composition the pages compare their fused entry point with.
+SWEEP = ["tiny_flux", "flux1_padded", "causal_8k", "causal_8k_additive", "flux2_long", "flux1_probe_6144",
+         "flux1_probe_24576", "zimage_dit"]
+
+
+def workload_sweep(dev, flush, steps=3, warmup=2):
+    from qk_norm_rope_gb300 import api
+    out = {}
+    for name in SWEEP:
+        inp = wl.make(name)
+        B, Sq, H, D = inp.q.shape
+        Skv = inp.k.shape[1]
+        f_fwd, f_bwd = nominal_flops(inp)
+        g = lambda t: None if t is None else t.to(dev)
+        q, k, v, do, wq, wk, ids = (g(t) for t in (inp.q, inp.k, inp.v, inp.do, inp.wq, inp.wk, inp.ids))
+        mask = device_mask(inp, name, dev)
+        ws = torch.empty(api.st_rope_attn_workspace_size(q, k, v, ids, inp.axes, inp.theta, mask, inp.causal,
+                                                         for_backward=True), dtype=torch.uint8, device=dev)
+        o = torch.empty(B, Sq, H, D, dtype=v.dtype, device=dev)
+        lse = torch.empty(B, H, Sq, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dwq, dwk = torch.empty_like(wq), torch.empty_like(wk)
+
+        def step():
+            api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal,
+                                 o=o, lse=lse, workspace=ws)
+            api.st_rope_attn_bwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o, lse, do, mask=mask,
+                                 causal=inp.causal, workspace=ws, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk,
+                                 reuse_tables=True)
+
+        def timed(fn, n):
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for a, b in evs:
+                flush.zero_()
+                a.record()
+                fn()
+                b.record()
+            torch.cuda.synchronize()
+            return sum(a.elapsed_time(b) for a, b in evs) / n
+
+        for _ in range(warmup):
+            step()
+        api.st_check_status()
+        ms = timed(step, steps)
+        api.st_timing_enable(True)
+        api.st_timing_read()
+        timed(step, steps)
+        kt = api.st_timing_read()
+        api.st_timing_enable(False)
+        api.st_check_status()
+        fwd_us = kt["fwd"][1] / max(kt["fwd"][0], 1) * 1e3
+        bwd_us = kt["bwd"][1] / max(kt["bwd"][0], 1) * 1e3
+        rec = {"shape": [B, Sq, H, D], "causal": inp.causal, "ms_per_step": round(ms, 4),
+               "tflops": round((f_fwd + f_bwd) / (ms * 1e-3) / 1e12, 2),
+               "fwd_kernel_us": round(fwd_us, 1), "bwd_kernel_us": round(bwd_us, 1),
+               "fwd_tflops": round(f_fwd / (fwd_us * 1e-6) / 1e12, 2) if fwd_us else None,
+               "bwd_tflops": round(f_bwd / (bwd_us * 1e-6) / 1e12, 2) if bwd_us else None,
+               "pct_of_dense_bf16_peak": round(100 * (f_fwd + f_bwd) / (ms * 1e-3) / 1e12 / DENSE_BF16_PEAK_TFLOPS, 2),
+               "q_dtype": str(inp.q.dtype)[6:], "mask": None if inp.mask is None and not inp.meta.get("mask_per_head")
+               else list(mask.shape)}
+        if name == "zimage_dit":
+            cos, sin = rope_tables_torch(ids, inp.axes, inp.theta)
+            leaves = [t.detach().requires_grad_() for t in (q, k, v, wq, wk)]
+
+            def eager_step():
+                oo = eager_attention(*leaves, inp.eps, cos, sin, mask=mask, causal=inp.causal)
+                torch.autograd.grad(oo, leaves, do)
+
+            def fused_fwd():
+                api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o=o, lse=lse, workspace=ws)
+
+            def eager_fwd():
+                with torch.no_grad():
+                    eager_attention(q, k, v, wq, wk, inp.eps, cos, sin)
+
+            for _ in range(warmup):
+                eager_step()
+                eager_fwd()
+            rec["eager_ms_per_step"] = round(timed(eager_step, steps), 4)
+            rec["fused_fwd_ms"] = round(timed(fused_fwd, steps), 4)
+            rec["eager_fwd_ms"] = round(timed(eager_fwd, steps), 4)
+            rec["eager"] = "torch rms_norm + table rotation (fp32) + scaled_dot_product_attention, autograd"
+        out[name] = rec
+        del q, k, v, do, mask, ws, o, lse, dq, dk, dv
+        torch.cuda.empty_cache()
+    return out
 
 
 def rope_tables_torch(ids, axes, theta):
@@ -352,12 +459,7 @@ def run_eager(args, rank, world, dev):
     f_fwd, f_bwd = nominal_flops(inp)
     g = lambda t: None if t is None else t.to(dev)
     q, k, v, do, wq, wk, ids = (g(t) for t in (inp.q, inp.k, inp.v, inp.do, inp.wq, inp.wk, inp.ids))
-    mask = g(inp.mask)
-    if inp.meta.get("mask_per_head"):
-        mask = torch.empty(B, H, Sq, inp.k.shape[1], dtype=torch.float32, device=dev)
-        for b in range(B):
-            for h in range(H):
-                mask[b, h].copy_(wl.additive_mask_head(args.workload, b, h))
+    mask = device_mask(inp, args.workload, dev)
     cos, sin = rope_tables_torch(ids, inp.axes, inp.theta)   # built once, as a model caches them
     leaves = [t.detach().requires_grad_() for t in (q, k, v, wq, wk)]
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -536,6 +638,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the other workloads measured after the headline one")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 

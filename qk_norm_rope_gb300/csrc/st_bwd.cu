@@ -372,6 +372,112 @@ __device__ __noinline__ void p_masked(const Common& c, uint32_t tS, float key_te
   tmem_st_wait();
 }
 
+// ---- epilogue of the eight compute warps, once the walk is over (n
+// sub-tiles; `ok` is false after an abort). Warp w holds key rows 32 (w % 4)
+// .. (its TMEM lanes) and head dims [64 hq, 64 hq + 64) of dV and dK'. Once
+// every MMA has completed, the K tile, the Q' ring and the dO ring are free:
+// the raw k rows and the tile's fp32 (cos, sin) rows are staged by TMA (K
+// tile, Q' ring) while dV is laid out in the dO ring and stored by TMA; then
+// dk (inverse rotation + RMSNorm backward) is laid out in the dS buffers and
+// stored by TMA (16-bit k; fp32 rows are stored directly), and each warp
+// writes its partial sums of the k norm-weight gradient.
+// Out of line, with every index derived again from the thread and block
+// coordinates, so that nothing it needs stays live in registers through the
+// main loop: with its values held across the loop (inlined, or called with
+// them as arguments) the whole kernel took 12% longer at the 96-register cap
+// (Flux1 1024px backward: 1039 us against 924 us).
+template <bool QKT, bool F16>
+__device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n, bool ok) {
+  const Common& c = P.c;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  const uint32_t* tslot = reinterpret_cast<const uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(const_cast<uint32_t*>(tslot) + 1);
+  const uint32_t tmem = *tslot;
+  const long long budget = c.wait_budget;
+  const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
+  const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const bool phantom = kt >= c.nKt;
+  const int qd = warp & 3, hq = warp >> 2;
+  const int r = qd * 32 + lane_id;
+  const int j = kt * kTile + r;
+  const bool key_ok = j < c.Skv;
+  const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
+  if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
+  // one decision for the eight warps (they share named barriers below)
+  if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
+    tc_fence_after();
+    float* ex = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed: row-sum exchange (2 KB)
+    float* sWk = reinterpret_cast<float*>(sm + kOffW);     // the Q' prologue is done with the q weights
+    const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
+    if (tid == 0) {
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&bars[kBarEpi], (QKT ? kTileBytes : 2 * kTileBytes) + 4 * kBoxBytes);
+      if constexpr (QKT) {
+        tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarEpi], 0, ty, tz, b);
+        tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarEpi], 64, ty, tz, b);
+      } else {
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          tma_load_4d(sm + kOffK + x * kBoxBytes, &P.tmap_k, &bars[kBarEpi], 32 * x, ty, tz, b);
+      }
+      const int trow = (c.tab_k_sb != 0 ? b * c.Skv : 0) + kt * kTile;
+#pragma unroll
+      for (int x = 0; x < 4; ++x) tma_load_2d(sm + kOffQ + x * kBoxBytes, &P.tmap_tab_k, &bars[kBarEpi], 32 * x, trow);
+    }
+    if (tid < kD) sWk[tid] = __ldg(c.wk + tid);
+    {
+      // dV: this thread's 64 columns of row r, 16-bit, into the dO ring in
+      // the operand-tile layout
+      uint8_t* stage = sm + kOffDO + hq * kHalfBytes;
+      const uint32_t tacc = tmem + 256 + lanebits + 64 * hq;
+#pragma unroll 1
+      for (int q = 0; q < 2; ++q) {
+        uint32_t v[32];
+        if (n > 0) {
+          tmem_ld32(tacc + 32 * q, v);
+        } else {
+#pragma unroll
+          for (int t = 0; t < 32; ++t) v[t] = 0u;
+        }
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          *reinterpret_cast<uint4*>(stage + sw128_off(r, 4 * q + c4)) =
+              make_uint4(pack16<F16>(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
+                         pack16<F16>(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
+                         pack16<F16>(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
+                         pack16<F16>(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
+      }
+      fence_proxy_async_smem();
+    }
+    if (!named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
+      if (tid == 0) {  // the staged dV rows (rows past S_kv are not written)
+        const int vy = P.dv_s_first ? kt * kTile : hk, vz = P.dv_s_first ? hk : kt * kTile;
+        tma_store_4d(&P.tmap_dv, sm + kOffDO, 0, vy, vz, b);
+        tma_store_4d(&P.tmap_dv, sm + kOffDO + kHalfBytes, 64, vy, vz, b);
+        bulk_commit_group();
+      }
+      const float2 colsum = dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq,
+                                                   key_ok, lane_id, ex, sWk, sm + kOffDS);
+      // this warp's column sums over its 32 rows: one partial row per warp
+      // quarter (rows 32 qd ..), added in a fixed order by the reduction
+      float* part = P.dwk_part + ((((int64_t)b * c.Hkv + hk) * c.nKt + kt) * 4 + qd) * kD + 64 * hq;
+      part[lane_id] = colsum.x;
+      part[32 + lane_id] = colsum.y;
+      if constexpr (QKT) {
+        fence_proxy_async_smem();
+        named_bar(kBarIdEpi, kEpiThreads);
+        if (tid == 0) {
+          const int ky = P.dk_s_first ? kt * kTile : hk, kz = P.dk_s_first ? hk : kt * kTile;
+          tma_store_4d(&P.tmap_dk, sm + kOffDS, 0, ky, kz, b);
+          tma_store_4d(&P.tmap_dk, sm + kOffDS + kHalfBytes, 64, ky, kz, b);
+          bulk_commit_group();
+        }
+      }
+      if (tid == 0) bulk_wait_read_all();  // the staged rows are read before the CTA may exit
+    }
+  }
+}
+
 // ELEM: the mask varies along the queries (per-element terms); a mask that is
 // broadcast over the queries reduces to one term per key.
 template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
@@ -586,89 +692,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         mbar_arrive(&bars[kBarCDone + bf]);
       }
     }
-    // ---- epilogue of the eight compute warps: warp w holds key rows
-    // 32 (w % 4) .. (its TMEM lanes) and head dims [64 hq, 64 hq + 64) of dV
-    // and dK'. Once every MMA has completed, the K tile, the Q' ring and the
-    // dO ring are free: the raw k rows and the tile's fp32 (cos, sin) rows are
-    // staged by TMA (K tile, Q' ring) while dV is laid out in the dO ring and
-    // stored by TMA; then dk (inverse rotation + RMSNorm backward) is laid out
-    // in the dS buffers and stored by TMA (16-bit k; fp32 rows are stored
-    // directly), and each warp writes its partial sums of the k norm-weight
-    // gradient.
-    if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
-    // one decision for the eight warps (they share named barriers below)
-    if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
-      tc_fence_after();
-      float* ex = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed: row-sum exchange (2 KB)
-      float* sWk = reinterpret_cast<float*>(sm + kOffW);     // the Q' prologue is done with the q weights
-      const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
-      if (tid == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars[kBarEpi], (QKT ? kTileBytes : 2 * kTileBytes) + 4 * kBoxBytes);
-        if constexpr (QKT) {
-          tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarEpi], 0, ty, tz, b);
-          tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarEpi], 64, ty, tz, b);
-        } else {
-#pragma unroll
-          for (int x = 0; x < 4; ++x)
-            tma_load_4d(sm + kOffK + x * kBoxBytes, &P.tmap_k, &bars[kBarEpi], 32 * x, ty, tz, b);
-        }
-        const int trow = (c.tab_k_sb != 0 ? b * c.Skv : 0) + kt * kTile;
-#pragma unroll
-        for (int x = 0; x < 4; ++x) tma_load_2d(sm + kOffQ + x * kBoxBytes, &P.tmap_tab_k, &bars[kBarEpi], 32 * x, trow);
-      }
-      if (tid < kD) sWk[tid] = __ldg(c.wk + tid);
-      {
-        // dV: this thread's 64 columns of row r, 16-bit, into the dO ring in
-        // the operand-tile layout
-        uint8_t* stage = sm + kOffDO + hq * kHalfBytes;
-        const uint32_t tacc = tmem + 256 + lanebits + 64 * hq;
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-          uint32_t v[32];
-          if (n > 0) {
-            tmem_ld32(tacc + 32 * q, v);
-          } else {
-#pragma unroll
-            for (int t = 0; t < 32; ++t) v[t] = 0u;
-          }
-#pragma unroll
-          for (int c4 = 0; c4 < 4; ++c4)
-            *reinterpret_cast<uint4*>(stage + sw128_off(r, 4 * q + c4)) =
-                make_uint4(pack16<F16>(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
-                           pack16<F16>(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
-                           pack16<F16>(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
-                           pack16<F16>(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
-        }
-        fence_proxy_async_smem();
-      }
-      if (!named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
-        if (tid == 0) {  // the staged dV rows (rows past S_kv are not written)
-          const int vy = P.dv_s_first ? kt * kTile : hk, vz = P.dv_s_first ? hk : kt * kTile;
-          tma_store_4d(&P.tmap_dv, sm + kOffDO, 0, vy, vz, b);
-          tma_store_4d(&P.tmap_dv, sm + kOffDO + kHalfBytes, 64, vy, vz, b);
-          bulk_commit_group();
-        }
-        const float2 colsum = dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq,
-                                                     key_ok, lane_id, ex, sWk, sm + kOffDS);
-        // this warp's column sums over its 32 rows: one partial row per warp
-        // quarter (rows 32 qd ..), added in a fixed order by the reduction
-        float* part = P.dwk_part + ((((int64_t)b * c.Hkv + hk) * c.nKt + kt) * 4 + qd) * kD + 64 * hq;
-        part[lane_id] = colsum.x;
-        part[32 + lane_id] = colsum.y;
-        if constexpr (QKT) {
-          fence_proxy_async_smem();
-          named_bar(kBarIdEpi, kEpiThreads);
-          if (tid == 0) {
-            const int ky = P.dk_s_first ? kt * kTile : hk, kz = P.dk_s_first ? hk : kt * kTile;
-            tma_store_4d(&P.tmap_dk, sm + kOffDS, 0, ky, kz, b);
-            tma_store_4d(&P.tmap_dk, sm + kOffDS + kHalfBytes, 64, ky, kz, b);
-            bulk_commit_group();
-          }
-        }
-        if (tid == 0) bulk_wait_read_all();  // the staged rows are read before the CTA may exit
-      }
-    }
+    bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp < kWarpDrain0 + kDrainWarps) {
     // ------------------------------------------------------------ dQ drain
     // A sub-tile's dQ'^T (128 head dims x 64 queries, fp32) leaves TMEM at once

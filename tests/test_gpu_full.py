@@ -111,3 +111,12 @@ def test_causal_8k_additive_mask(cuda_lib):
 def test_flux2_long(cuda_lib):
     inp = wl.make("flux2_long")
     run_full(cuda_lib, inp, heads=[(0, 31)])
+
+
+@pytest.mark.parametrize("name,head", [("flux1_probe_6144", (0, 7)), ("flux1_probe_24576", (0, 11))])
+def test_flux1_probe_shapes(cuda_lib, name, head):
+    # the pages' probe shapes (1024px and 2048px images, no text tokens): the
+    # whole problem runs on the GPU, one head is recomputed by the oracle
+    # (at S = 24576 that is about a minute of host time)
+    inp = wl.make(name)
+    run_full(cuda_lib, inp, heads=[head])
