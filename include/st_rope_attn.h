@@ -109,12 +109,13 @@ typedef struct {
  *        [B, S_kv, D]); NULL means "same as cos/sin" and requires S_q == S_kv.
  * reuse_tables: read by st_rope_attn_bwd only. 1 states that the workspace
  *        passed to the backward already holds the device tables of exactly
- *        this rotation and the tile classes of exactly this mask, written by
- *        an st_rope_attn_fwd call on the same workspace pointer that is stream-
- *        ordered before the backward (a backward-sized workspace serves both
- *        calls: its first bytes have the forward's layout); the backward then
- *        skips rebuilding them. Anything else is undefined results (not a
- *        fault). 0: the backward rebuilds them. */
+ *        this rotation, the tile classes of exactly this mask and the
+ *        normalised, rotated q rows (Q') of exactly these inputs, written by an
+ *        st_rope_attn_fwd call on the same workspace pointer with a backward-
+ *        sized workspace_bytes, stream-ordered before the backward (its first
+ *        bytes have the forward's layout); the backward then skips rebuilding
+ *        them. Anything else is undefined results (not a fault). 0: the
+ *        backward rebuilds them. */
 typedef struct {
   const st_tensor* ids;
   const st_tensor* ids_k;
@@ -151,8 +152,9 @@ enum {
                          backward in its epilogue), dQ' accumulation */
   ST_K_DQ_POST = 5,   /* dQ: inverse rotation + RMSNorm backward */
   ST_K_DW = 6,        /* norm-weight gradient reduction */
-  ST_K_PROBE = 7,     /* bounded-wait self-test */
-  ST_K_COUNT = 8
+  ST_K_QPRIME = 7,    /* Q' rows for a backward without a forward's workspace */
+  ST_K_PROBE = 8,     /* bounded-wait self-test */
+  ST_K_COUNT = 9
 };
 
 /* Per-kernel device time between two st_timing_read calls. */
@@ -196,7 +198,12 @@ ST_API size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k
  *  o:      [B, S_q, H, D] output, dtype of v.  lse: [B, H, S_q] fp32 output,
  *          natural-log log-sum-exp of each row (contiguous).
  *  workspace: device buffer of at least st_rope_attn_workspace_size(..., 0)
- *          bytes, 256-byte aligned; its contents need no initialisation.
+ *          bytes, 256-byte aligned; its contents need no initialisation. When
+ *          workspace_bytes also covers st_rope_attn_workspace_size(..., 1)
+ *          (and q, k, v are not all fp32), the forward leaves its Q' rows
+ *          ([B, S_q, H, D] in the 16-bit operand type, the bf16 or fp16 values
+ *          its attention kernel multiplies) in the backward's part of the
+ *          workspace, for a backward with rope->reuse_tables = 1.
  *  stream: cudaStream_t. */
 ST_API st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* q_norm_w,
                            const st_tensor* k_norm_w, float eps, const st_rope* rope, const st_tensor* mask,

@@ -68,7 +68,7 @@ class st_stats(ctypes.Structure):
                                                 "kernel_launches")]
 
 
-KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce", "probe"]
+KERNEL_KINDS = ["table", "classify", "fwd", "bwd_pre", "bwd", "dq_post", "dw_reduce", "qprime", "probe"]
 
 
 class st_kernel_times(ctypes.Structure):

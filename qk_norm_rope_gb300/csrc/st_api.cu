@@ -236,7 +236,7 @@ struct Plan {
   // workspace offsets
   size_t off_tab16_q = 0, off_tab16_k = 0;
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
-         off_dwk = 0, off_dwq = 0, off_dwscratch = 0, total = 0;
+         off_dwk = 0, off_dwq = 0, off_dwscratch = 0, off_qp = 0, total = 0;
   int n_dwq = 0, n_dwk = 0;
   bool f32 = false;  // q, k, v all fp32: the exact-fp32 kernels
 };
@@ -366,6 +366,10 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     off = align_up(off + (size_t)P->n_dwq * kD * sizeof(float), 256);
     P->off_dwscratch = off;
     off = align_up(off + (size_t)2 * dw_reduce_blocks(P->n_dwq, P->n_dwk) * kD * sizeof(float), 256);
+    if (!P->f32) {  // Q' rows [B, S_q, H, D] in the 16-bit operand type, left by the forward
+      P->off_qp = off;
+      off = align_up(off + (size_t)s.B * s.Sq * s.H * kD * 2, 256);
+    }
   }
   P->total = off;
   return ST_OK;
@@ -593,12 +597,31 @@ st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* ma
   return ST_OK;
 }
 
+// 4-D tiled map over the workspace's Q' rows [B, S_q, H, D] (contiguous, the
+// 16-bit operand type) as (d, h, s, b), for 64-column x box_rows boxes with
+// 128-byte swizzle: the forward stores its Q' tiles through it, the backward
+// loads its sub-tiles.
+st_status encode_qp_map(uint8_t* qp, const Shape& s, bool f16, int box_rows, CUtensorMap* map) {
+  st_tensor t;
+  memset(&t, 0, sizeof(t));
+  t.data = qp;
+  t.dtype = f16 ? ST_F16 : ST_BF16;
+  t.ndim = 4;
+  t.shape[0] = s.B; t.shape[1] = s.Sq; t.shape[2] = s.H; t.shape[3] = kD;
+  t.stride[3] = 1; t.stride[2] = kD; t.stride[1] = (int64_t)s.H * kD; t.stride[0] = (int64_t)s.Sq * s.H * kD;
+  int s_first = 0;
+  st_status st = encode_rows_map(&t, map, &s_first, box_rows);
+  if (st == ST_OK && s_first) return fail(ST_ERR_UNSUPPORTED, "unexpected Q' map order");
+  return st;
+}
+
 // The forward's launches (tables, mask tile classes, attention) on a
-// validated call, with `ws` the workspace (or the built-in scratch).
+// validated call, with `ws` the workspace (or the built-in scratch). With
+// `qp` non-null the attention kernel also stores its Q' tiles there.
 st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k, const st_tensor* v,
                           const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps, const st_rope* rope,
                           const st_tensor* mask, int causal, float scale, st_tensor* o, const RowTensor& ro,
-                          st_tensor* lse, uint8_t* ws, cudaStream_t stream) {
+                          st_tensor* lse, uint8_t* ws, uint8_t* qp, cudaStream_t stream) {
   st_status st;
   Dev dev;
   if ((st = device_globals(&dev)) != ST_OK) return st;
@@ -629,6 +652,10 @@ st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k,
   if (fp.qk_tma) {
     if ((st = encode_rows_map(q, &fp.tmap_q, &fp.q_s_first)) != ST_OK) return st;
     if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
+  }
+  if (qp) {
+    if ((st = encode_qp_map(qp, P.sh, v->dtype == ST_F16, kTile, &fp.tmap_qp)) != ST_OK) return st;
+    fp.save_qp = 1;
   }
   if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
   return cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch");
@@ -672,8 +699,16 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
     return ST_OK;
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // a workspace that can also serve the backward receives the Q' rows, which
+  // a backward reusing it reads instead of normalising and rotating q again
+  uint8_t* qp = nullptr;
+  if (!P.f32) {
+    Plan PB;
+    if (plan_call(q, k, v, mask, causal, rope, 1, &PB) == ST_OK && workspace_bytes >= PB.total)
+      qp = static_cast<uint8_t*>(workspace) + PB.off_qp;
+  }
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(workspace), stream)) != ST_OK)
+                            static_cast<uint8_t*>(workspace), qp, stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
@@ -726,10 +761,10 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     bp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
     // raw k rows: the prologue's TMA source (bf16) and the epilogue's (both dtypes)
     if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
-    if (bp.qk_tma) {
-      if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(q, &bp.tmap_q, &bp.q_s_first, kTile / 4)) != ST_OK)
-        return st;
-    }
+    // the Q' rows of the workspace, 32-row boxes (each CTA of a pair loads half a sub-tile)
+    if ((int64_t)s.B * s.Sq * s.H > 0 &&
+        (st = encode_qp_map(ws + P.off_qp, s, v->dtype == ST_F16, kTile / 4, &bp.tmap_q)) != ST_OK)
+      return st;
     if ((st = encode_table_map(reinterpret_cast<const float2*>(ws + P.off_tab_k), (int64_t)P.ids_k.Bt * s.Skv,
                                &bp.tmap_tab_k)) != ST_OK)
       return st;
@@ -739,6 +774,23 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   // the table kernel would have cleared)
   const bool reuse = rope->reuse_tables != 0 && (int64_t)s.B * s.Sq * s.H > 0;
   if (!reuse && (st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  if (!reuse && !P.f32 && P.nKt > 0 && (int64_t)s.B * s.Sq * s.H > 0) {
+    // no forward left its Q' rows in this workspace: build them
+    QPrimeParams qpp;
+    memset(&qpp, 0, sizeof(qpp));
+    qpp.q = P.q;
+    qpp.tab = reinterpret_cast<const float2*>(ws + P.off_tab_q);
+    qpp.tab16 = reinterpret_cast<const __half2*>(ws + P.off_tab16_q);
+    qpp.tab_sb = P.ids_q.Bt > 1 ? (int64_t)s.Sq * kPairs : 0;
+    qpp.w = static_cast<const float*>(q_norm_w->data);
+    qpp.eps = eps;
+    qpp.out = ws + P.off_qp;
+    qpp.f16 = v->dtype == ST_F16 ? 1 : 0;
+    qpp.B = s.B; qpp.H = s.H; qpp.Sq = s.Sq;
+    if ((st = cuda_check(launch_counted(ST_K_QPRIME, stream, [&] { return launch_qprime(qpp, stream); }),
+                         "Q' row kernel launch")) != ST_OK)
+      return st;
+  }
 
   float* delta = reinterpret_cast<float*>(ws + P.off_delta);
   float* dq_acc = P.f32 ? nullptr : reinterpret_cast<float*>(ws + P.off_dqacc);  // the fp32 path needs none
@@ -897,7 +949,7 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   if ((st = noalloc_scratch_address(&scratch)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(scratch), stream)) != ST_OK)
+                            static_cast<uint8_t*>(scratch), nullptr, stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;

@@ -367,6 +367,99 @@ cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
+// One thread per row, with the forward prologues' arithmetic in their order,
+// so that the rows equal the ones a forward leaves in the workspace:
+// r = 1/sqrt(mean x^2 + eps) (16-bit q: the sum of squares of each 64-dim half
+// with separate even/odd accumulators, as the two lanes of a row do; fp32 q:
+// even/odd accumulators over the whole row), n = x w r,
+// y = (n0 cos - n1 sin, n0 sin + n1 cos) with the fp16 (16-bit q) or fp32
+// (fp32 q) table, rounded once to the operand type.
+__global__ void __launch_bounds__(128) qprime_kernel(const __grid_constant__ QPrimeParams p) {
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= nrows) return;
+  const RowIdx x = row_idx(row, p.Sq, p.H, nrows < (int64_t(1) << 31));
+  const int64_t off = x.b * p.q.sb + (int64_t)x.i * p.q.ss + x.h * p.q.sh;
+  const int64_t trow = x.b * p.tab_sb + (int64_t)x.i * kPairs;
+  uint4* out = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * kD);
+  const float4* w4 = reinterpret_cast<const float4*>(p.w);
+  if (p.q.dt != kDtF32) {
+    const bool f16 = p.q.dt == kDtF16;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q.p) + off);
+    float half_ss[2];
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = __ldg(src + 8 * hh + c);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = f16 ? f16_lo(u[e]) : bf16_lo(u[e]), hi = f16 ? f16_hi(u[e]) : bf16_hi(u[e]);
+          a0 = fmaf(lo, lo, a0);
+          a1 = fmaf(hi, hi, a1);
+        }
+      }
+      half_ss[hh] = a0 + a1;
+    }
+    const float r = rsqrtf((half_ss[0] + half_ss[1]) * (1.0f / kD) + p.eps);
+#pragma unroll 1
+    for (int c = 0; c < 16; ++c) {  // dims 8c .. 8c + 7
+      const uint4 v = __ldg(src + c);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+      const float4 wa = __ldg(w4 + 2 * c), wb = __ldg(w4 + 2 * c + 1);
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+      uint32_t o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 sc = __half22float2(p.tab16[trow + 4 * c + e]);
+        const float lo = f16 ? f16_lo(u[e]) : bf16_lo(u[e]), hi = f16 ? f16_hi(u[e]) : bf16_hi(u[e]);
+        const float n0 = lo * wv[2 * e] * r, n1 = hi * wv[2 * e + 1] * r;
+        const float y0 = n0 * sc.x - n1 * sc.y, y1 = n0 * sc.y + n1 * sc.x;
+        o4[e] = p.f16 ? pack16<true>(y0, y1) : pack16<false>(y0, y1);
+      }
+      out[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+  } else {
+    const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q.p) + off);
+    float ss0 = 0.f, ss1 = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < kD / 4; ++c) {
+      const float4 v = __ldg(src + c);
+      ss0 = fmaf(v.x, v.x, ss0);
+      ss1 = fmaf(v.y, v.y, ss1);
+      ss0 = fmaf(v.z, v.z, ss0);
+      ss1 = fmaf(v.w, v.w, ss1);
+    }
+    const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + p.eps);
+    const float4* t4 = reinterpret_cast<const float4*>(p.tab + trow);
+#pragma unroll 1
+    for (int c = 0; c < kD / 8; ++c) {
+      uint32_t o4[4];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const float4 v = __ldg(src + 2 * c + hh);
+        const float4 cs = __ldg(t4 + 2 * c + hh);
+        const float4 ww = __ldg(w4 + 2 * c + hh);
+        const float n0 = v.x * ww.x * r, n1 = v.y * ww.y * r, n2 = v.z * ww.z * r, n3 = v.w * ww.w * r;
+        const float y0 = n0 * cs.x - n1 * cs.y, y1 = n0 * cs.y + n1 * cs.x;
+        const float y2 = n2 * cs.z - n3 * cs.w, y3 = n2 * cs.w + n3 * cs.z;
+        o4[2 * hh] = p.f16 ? pack16<true>(y0, y1) : pack16<false>(y0, y1);
+        o4[2 * hh + 1] = p.f16 ? pack16<true>(y2, y3) : pack16<false>(y2, y3);
+      }
+      out[c] = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+    }
+  }
+}
+
+cudaError_t launch_qprime(const QPrimeParams& p, cudaStream_t stream) {
+  const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
+  const int64_t blocks = (nrows + 127) / 128;
+  qprime_kernel<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream) {
   dim3 grid(dw_reduce_blocks(p.n_q, p.n_k), 2);
   dw_reduce_kernel<<<grid, kD, 0, stream>>>(p);

@@ -73,6 +73,21 @@ struct PostParams {
   int B, H, Sq;
 };
 
+// Q' rows for a backward that does not reuse a forward's workspace: the
+// forward kernel's q prologue (RMSNorm with the q weights, rotation, rounding
+// to the 16-bit operand type) as a row kernel into [B, Sq, H, D].
+struct QPrimeParams {
+  RowTensor q;
+  const float2* tab;      // fp32 (cos, sin) rows: fp32 q, as the forward's fp32 prologue
+  const __half2* tab16;   // fp16 (cos, sin) rows: 16-bit q, as the forward's TMA-staged prologue
+  int64_t tab_sb;         // pairs between the tables of two samples (0: shared)
+  const float* w;
+  float eps;
+  void* out;              // [B, Sq, H, D] contiguous, 16-bit operand type
+  int f16;                // operand type: 1 fp16, 0 bf16
+  int B, H, Sq;
+};
+
 struct DwParams {
   const float* dwq_part;
   const float* dwk_part;
@@ -88,6 +103,7 @@ cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream);
 cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream);
+cudaError_t launch_qprime(const QPrimeParams& p, cudaStream_t stream);
 cudaError_t launch_wait_probe(unsigned* status, unsigned long long* counters, long long budget, cudaStream_t stream);
 
 }  // namespace st

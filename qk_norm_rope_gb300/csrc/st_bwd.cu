@@ -10,7 +10,10 @@
 //   dS^T = P^T (dP^T - Delta)
 //   dV += P^T dO, dK' += dS^T Q', dQ'^T = K'^T dS^T    (tensor core, TMEM)
 // dQ'^T (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
-// bulk reduces. The two CTAs of a cluster share the Q' operand prologue.
+// bulk reduces. Q' comes from the workspace, where the forward kernel left
+// the tiles it normalised and rotated (a standalone row kernel fills it when
+// the forward did not run on this workspace); each CTA of a cluster loads half
+// of a sub-tile's rows by TMA multicast into both CTAs' stage.
 //
 // Warp roles (608 threads; 96 registers per thread):
 //   warps 0-7    compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and
@@ -21,14 +24,12 @@
 //                out at once and its columns released; each warp then stages
 //                its 32 head dims in its own shared-memory box and adds the box
 //                into global memory with a TMA bulk reduce of its own
-//   warps 12-15  Q' prologue: each CTA of the cluster normalises and rotates
-//                32 of a sub-tile's 64 rows (eight lanes per row) and copies
-//                them into the peer's stage as well (DSMEM bulk copy); the
-//                sub-tile's LSE and Delta; K' once
+//   warps 12-15  prologue: K' once (normalised and rotated in place); then
+//                each sub-tile's LSE and Delta
 //   warp 16      TMEM allocation + tcgen05.mma issue (one thread)
-//   warp 17      TMA: raw K, V once; this CTA's 32 raw Q rows per sub-tile
-//                (4-stage ring, a stage reused once both CTAs' MMAs released
-//                it)
+//   warp 17      TMA: raw K, V once; this CTA's 32 Q' rows per sub-tile,
+//                multicast to both CTAs (4-stage ring, a stage reused once both
+//                CTAs' MMAs released it)
 //   warp 18      TMA: dO sub-tiles (2-stage ring), so that the Q' ring never
 //                waits behind a dO stage
 // TMEM (512 columns): two sub-tile buffers of 128 columns, dV, dK'. A buffer
@@ -79,7 +80,7 @@ constexpr uint32_t kOffR = kOffDS + 2 * kSubBytes;              // dQ'^T staging
 constexpr uint32_t kOffStat = kOffR + kDrainWarps * kRBoxBytes; // [stage][LSE*log2e | Delta][64] fp32
 constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kSub * 4;
 constexpr uint32_t kBarBytes = 512;
-constexpr uint32_t kOffW = kOffBar + kBarBytes;                 // q norm weights, fp32
+constexpr uint32_t kOffW = kOffBar + kBarBytes;                 // k norm weights for the epilogue, fp32
 constexpr uint32_t kBwdSmem = kOffW + kD * 4;                   // the base must be 1024-byte aligned
 static_assert(kBwdSmem <= 232448, "backward shared memory exceeds the per-block limit");
 static_assert(kProlThreads >= kSub, "one prologue thread per stat row");
@@ -89,8 +90,8 @@ enum {
   kBarKRaw = 0,                          // raw k rows landed (TMA)
   kBarKFull,                             // K' ready (and V, for a CTA past the last key tile)
   kBarVFull,
-  kBarQRaw,                              // + stage: raw q rows landed (TMA)
-  kBarQFull = kBarQRaw + kQStages,       // + stage: Q' + stats ready (prologue threads + the peer's rows)
+  kBarQRaw,                              // + stage: Q' rows landed (both CTAs' multicast loads)
+  kBarQFull = kBarQRaw + kQStages,       // + stage: the stage's LSE/Delta written (prologue threads)
   kBarQFree = kBarQFull + kQStages,      // + stage: both CTAs' MMAs done with the stage
   kBarDOFull = kBarQFree + kQStages,     // + stage: dO rows landed
   kBarDOFree = kBarDOFull + kDOStages,   // + stage: MMAs done with the dO rows
@@ -407,7 +408,7 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
   if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
     tc_fence_after();
     float* ex = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed: row-sum exchange (2 KB)
-    float* sWk = reinterpret_cast<float*>(sm + kOffW);     // the Q' prologue is done with the q weights
+    float* sWk = reinterpret_cast<float*>(sm + kOffW);     // k norm weights
     const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
     if (tid == 0) {
       fence_proxy_async_smem();
@@ -529,22 +530,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     *abort_flag = 0;
     fence_mbar_init();
   }
-  float* sWq = reinterpret_cast<float*>(sm + kOffW);
-  if (tid < kD) sWq[tid] = __ldg(P.c.wq + tid);
   if (warp == kWarpTma && lane_id == 0 && P.c.nQt > 0) {  // the maps exist only when there is work
     tma_prefetch_desc(&P.tmap_v);
     tma_prefetch_desc(&P.tmap_do);
     tma_prefetch_desc(&P.tmap_dq);
     tma_prefetch_desc(&P.tmap_k);
     tma_prefetch_desc(&P.tmap_tab_k);
-    if constexpr (QKT) tma_prefetch_desc(&P.tmap_q);
+    tma_prefetch_desc(&P.tmap_q);
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers exist before any remote copy or arrival
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t crank = cluster_rank(), peer = crank ^ 1u;
+  const uint32_t crank = cluster_rank();
   const long long budget = c.wait_budget;
   const bool phantom = kt >= c.nKt;  // pads the cluster when the key-tile count is odd
   QWalk W;
@@ -769,21 +768,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     // barrier could differ between threads if another role aborts meanwhile,
     // and the loop below has named barriers of its own
     ok = !named_bar_any(3, kProlThreads, *abort_flag != 0);
-    const uint32_t peer_q = mapa_shared(smem_u32(sm + kOffQ), peer);
-    const uint32_t peer_qfull = mapa_shared(smem_u32(&bars[kBarQFull]), peer);
-    // Q' rows: eight lanes per row (see OctRow), four rows per warp and pass;
-    // pass k (0, 1) of warp pw handles row 16k + 4pw + (lane & 3) of this
-    // CTA's 32 rows of a sub-tile. The (cos, sin) rows of the next sub-tile
-    // are loaded while this one is finished and pinned before it starts.
-    // Chunk (part) order over the lanes: the eight lanes of a quarter warp
-    // hold chunks c and c + 4 of four consecutive rows, eight distinct 16-byte
-    // slots of the swizzled rows, so their shared-memory accesses do not
-    // conflict.
-    const int part = (((lane_id >> 2) & 1) << 2) | (lane_id >> 3), pw = warp - kWarpProl0;
-    const int ra = kPeerRows * static_cast<int>(crank) + 4 * pw + (lane_id & 3), rb = ra + 16;
-    const __half2* tab16 = c.tab16_q + b * c.tab_q_sb;
-    OctRow<F16> rp[2];
-    // LSE and Delta of row p of the current sub-tile, loaded one sub-tile ahead
+    // Q' rows arrive by TMA from the workspace (the forward's normalised,
+    // rotated q rows); these threads stage each sub-tile's LSE (base 2; +inf
+    // for rows without keys or past S_q, so that P = 0) and Delta, loaded one
+    // sub-tile ahead. A stage's values are rewritten once both CTAs' MMAs have
+    // released the stage (the compute warps have read them by then).
     float lse_c = -INFINITY, dl_c = 0.f;
     auto load_stats = [&](int iq0, int h) {
       lse_c = -INFINITY;
@@ -797,67 +786,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     WPos m = next_pos<MK>(c, b, W, W.start(), kt0);
     int s = 0;
     if (W.more(m)) load_stats(W.qt(m) * kTile, W.head(m));
-    if constexpr (QKT) {
-      if (W.more(m)) {
-        const int i0 = W.qt(m) * kTile;
-        if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
-        if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
-      }
-    }
     for (int n = 0; ok && W.more(m); ++n) {
-      const int qt = W.qt(m), h = W.head(m);
-      // the next sub-tile of the walk
       const WPos m_next = s == 0 ? m : next_pos<MK>(c, b, W, W.step(m), kt0);
       const int s_next = s ^ 1;
       const int sq = n % kQStages;
-      uint8_t* stage = sm + kOffQ + sq * kSubBytes;
-      const int iq0 = qt * kTile + kSub * s;
-      if constexpr (QKT) pin_loads(rp[1].fold(rp[0].fold(__float_as_uint(lse_c) ^ __float_as_uint(dl_c))), scratch);
-      // LSE (base 2; +inf for rows without keys or past S_q, so P = 0) and
-      // Delta of the sub-tile's 64 rows (every CTA keeps all of them)
       const float l2 = (lse_c == -INFINITY) ? INFINITY : lse_c * kLog2e, dl = dl_c;
-      // a failed wait skips the work but not the named barrier below
-      if constexpr (QKT) {
-        if (wait_bar_warp(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) {
-          // rows past S_q stay TMA zeros
-          OctRow<F16>::finish2(rp[0], rp[1], stage, ra, rb, part, sWq, c.eps, iq0 + ra < c.Sq, iq0 + rb < c.Sq, kSubHalf);
-          if (W.more(m_next)) {
-            const int i0 = W.qt(m_next) * kTile + kSub * s_next;
-            if (i0 + ra < c.Sq) rp[0].prefetch(tab16 + (int64_t)(i0 + ra) * kPairs, part);
-            if (i0 + rb < c.Sq) rp[1].prefetch(tab16 + (int64_t)(i0 + rb) * kPairs, part);
-          }
-        }
-      } else {
-        static_assert(kProlThreads == 4 * kPeerRows, "four lanes per Q' row");
-        if (n < kQStages ||
-            wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
-          // this CTA's 32 rows, four lanes per row (rows past S_q become zeros)
-          const int row = kPeerRows * static_cast<int>(crank) + (p >> 2);
-          const bool valid = iq0 + row < c.Sq;
-          const int i = valid ? iq0 + row : 0;
-          rope_norm_global_quad<F16>(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.dt, c.wq, c.eps,
-                                c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, stage, row, p & 3, valid, kSubHalf);
-        }
-      }
+      if (n >= kQStages &&
+          !wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget))
+        break;
       if (p < kSub) {
         stat[sq * 2 * kSub + p] = l2;
         stat[sq * 2 * kSub + kSub + p] = dl;
       }
       if (W.more(m_next)) load_stats(W.qt(m_next) * kTile + kSub * s_next, W.head(m_next));
-      // this CTA's 32 rows are final: one bulk copy per column half to the
-      // same offsets of the peer's stage, completing on its Q' barrier
-      fence_proxy_async_smem();
-      if (named_bar_any(3, kProlThreads, *abort_flag != 0)) break;
-      if (p == 0) {
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const uint32_t off = sq * kSubBytes + hh * kSubHalf + kPeerRowsBytes * crank;
-          bulk_copy_to_peer(peer_q + off, sm + kOffQ + off, kPeerRowsBytes, peer_qfull + 8u * sq);
-        }
-        mbar_arrive_expect_tx(&bars[kBarQFull + sq], 2 * kPeerRowsBytes);  // the peer's rows
-      } else {
-        mbar_arrive(&bars[kBarQFull + sq]);
-      }
+      mbar_arrive(&bars[kBarQFull + sq]);
       m = m_next;
       s = s_next;
     }
@@ -880,24 +822,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       }
       int n = 0, q_issued = 0;
       bool stop = false;
-      if constexpr (QKT) {
-        for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
-          const int qt = W.qt(m), h = W.head(m);
-          for (int s = 0; s < 2; ++s, ++n) {  // this CTA's 32 raw rows of the sub-tile
-            const int sq = n % kQStages;
-            if (n >= kQStages &&
-                !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
-              stop = true;
-              break;
-            }
-            uint8_t* qrows = sm + kOffQ + sq * kSubBytes + kPeerRowsBytes * crank;
-            const int row = qt * kTile + kSub * s + kPeerRows * static_cast<int>(crank);
-            const int y = P.q_s_first ? row : h, z = P.q_s_first ? h : row;
-            mbar_arrive_expect_tx(&bars[kBarQRaw + sq], 2 * kPeerRowsBytes);
-            tma_load_4d(qrows, &P.tmap_q, &bars[kBarQRaw + sq], 0, y, z, b);
-            tma_load_4d(qrows + kSubHalf, &P.tmap_q, &bars[kBarQRaw + sq], 64, y, z, b);
-            ++q_issued;
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+        const int qt = W.qt(m), h = W.head(m);
+        for (int s = 0; s < 2; ++s, ++n) {
+          // this CTA's 32 Q' rows of the sub-tile, into both CTAs' stage; the
+          // stage holds the peer's 32 rows as well once kSubBytes have landed
+          const int sq = n % kQStages;
+          if (n >= kQStages &&
+              !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
+            stop = true;
+            break;
           }
+          uint8_t* qrows = sm + kOffQ + sq * kSubBytes + kPeerRowsBytes * crank;
+          const int row = qt * kTile + kSub * s + kPeerRows * static_cast<int>(crank);
+          mbar_arrive_expect_tx(&bars[kBarQRaw + sq], kSubBytes);
+          tma_load_4d_mc(qrows, &P.tmap_q, &bars[kBarQRaw + sq], 0, h, row, b, 0x3);
+          tma_load_4d_mc(qrows + kSubHalf, &P.tmap_q, &bars[kBarQRaw + sq], 64, h, row, b, 0x3);
+          ++q_issued;
         }
       }
       // drain: every issued load lands before the CTA exits (these waits do not
@@ -954,7 +895,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) nsub += 2;
       auto issue_s = [&](int n) -> bool {  // S^T(n) into its half of buffer n % 2
         const int sq = n % kQStages;
-        if (!wait_bar(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
+        if (!wait_bar(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
         tc_fence_after();
         const uint64_t dQk = sdesc_add(dQk0, sq * kSubBytes);
 #pragma unroll

@@ -69,6 +69,8 @@ struct FwdParams {
   int v_s_first;       // map dims are (d, s, h, b) instead of (d, h, s, b)
   int q_s_first, k_s_first;
   int qk_tma;          // 1: q and k are 16-bit and staged by TMA, normalised in place
+  CUtensorMap tmap_qp; // the workspace's Q' rows ([B, Sq, H, D], operand type), 128-row boxes (TMA store)
+  int save_qp;         // 1: the CTA stores its Q' tiles there for the backward
   void* o;
   int64_t o_sb, o_ss, o_sh;
   int o_dt;
@@ -79,7 +81,7 @@ struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
   CUtensorMap tmap_do;  // dO rows, 64-row boxes
-  CUtensorMap tmap_q;   // raw q rows, 32-row boxes (16-bit only; see qk_tma)
+  CUtensorMap tmap_q;   // Q' rows of the workspace ([B, Sq, H, D], operand type), 32-row boxes
   CUtensorMap tmap_k;   // raw k rows, 128-row boxes (16-bit: 64 columns; fp32: 32 columns, epilogue only)
   CUtensorMap tmap_tab_k;  // the fp32 (cos, sin) table of the keys as [Bt_k * Skv, 128] floats, 32 x 128 boxes
   CUtensorMap tmap_dv;     // dv rows, 128-row boxes (TMA store of the epilogue)

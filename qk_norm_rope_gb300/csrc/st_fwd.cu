@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
+    if (P.save_qp) tma_prefetch_desc(&P.tmap_qp);
     if constexpr (QKT) {
       tma_prefetch_desc(&P.tmap_q);
       tma_prefetch_desc(&P.tmap_k);
@@ -562,6 +563,21 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       for (int m = max(0, n - kVStages); m < n; ++m)
         mbar_wait(&bars[kBarVFull + m % kVStages], (m / kVStages) & 1, budget);
+    } else if (lane_id == 2 && P.save_qp) {
+      // the finished Q' tiles go to the workspace for the backward (rows past
+      // S_q are clipped by the map); the tiles stay in place for the whole CTA
+      if (wait_bar(&bars[kBarQFull], 0, abort_flag, budget)) {
+#pragma unroll 1
+        for (int ti = 0; ti < 2; ++ti) {
+          const int row = (qt0 + ti) * kTile;
+          if (row >= c.Sq) break;
+          const uint8_t* tile = sm + kOffQ + ti * kTileBytes;
+          tma_store_4d(&P.tmap_qp, tile, 0, h, row, b);
+          tma_store_4d(&P.tmap_qp, tile + kHalfBytes, 64, h, row, b);
+        }
+        bulk_commit_group();
+        bulk_wait_read_all();  // the source tiles are read before the CTA may exit
+      }
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
