@@ -237,6 +237,9 @@ struct Plan {
   size_t off_tab16_q = 0, off_tab16_k = 0;
   size_t off_ctrl = 0, off_tab_q = 0, off_tab_k = 0, off_flags = 0, off_delta = 0, off_dqacc = 0,
          off_dwk = 0, off_dwq = 0, off_dwscratch = 0, off_qp = 0, total = 0;
+  size_t off_kflags = 0, off_kcache = 0;
+  size_t fwd_base = 0;  // the forward's bytes without the K' tile cache
+  bool kcache = false;  // the forward part ends with the K' tile cache
   int n_dwq = 0, n_dwk = 0;
   bool f32 = false;  // q, k, v all fp32: the exact-fp32 kernels
 };
@@ -351,6 +354,16 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     P->off_flags = off;
     off = align_up(off + (size_t)P->Bm * P->Hm * P->nQtm * P->nKt, 256);
   }
+  P->fwd_base = off;
+  if (!P->f32 && P->nKt > 0) {
+    // K' tiles shared between the forward's CTAs: publication flags
+    // [B, H_kv, nKt] and the tiles [B, S_kv, H_kv, D] in the operand type
+    P->kcache = true;
+    P->off_kflags = off;
+    off = align_up(off + (size_t)s.B * s.Hkv * P->nKt * sizeof(uint32_t), 256);
+    P->off_kcache = off;
+    off = align_up(off + (size_t)s.B * s.Skv * s.Hkv * kD * 2, 256);
+  }
   if (for_backward) {
     P->off_delta = off;
     off = align_up(off + (size_t)s.B * s.H * s.Sq * sizeof(float), 256);
@@ -461,11 +474,15 @@ st_status cuda_check(cudaError_t e, const char* what) {
 
 // Rotary tables and mask tile classes: the first launches of a call.
 st_status launch_prelude(const Plan& P, const st_rope* rope, const st_tensor* mask, uint8_t* ws, const Dev& dev,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool zero_kflags = false) {
   unsigned* ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
   TableParams t;
   fill_table(P.ids_q, rope, reinterpret_cast<float2*>(ws + P.off_tab_q), reinterpret_cast<__half2*>(ws + P.off_tab16_q),
              ctrl, &t);
+  if (zero_kflags) {  // the forward's K' publication flags start lowered
+    t.zero = reinterpret_cast<unsigned*>(ws + P.off_kflags);
+    t.n_zero = (int64_t)P.sh.B * P.sh.Hkv * P.nKt;
+  }
   st_status st = cuda_check(launch_counted(ST_K_TABLE, stream, [&] { return launch_table(t, stream); }), "table kernel launch");
   if (st != ST_OK) return st;
   if (P.separate_k_table) {
@@ -597,21 +614,21 @@ st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* ma
   return ST_OK;
 }
 
-// 4-D tiled map over the workspace's Q' rows [B, S_q, H, D] (contiguous, the
+// 4-D tiled map over contiguous operand rows [B, S, H, D] of the workspace (the
 // 16-bit operand type) as (d, h, s, b), for 64-column x box_rows boxes with
-// 128-byte swizzle: the forward stores its Q' tiles through it, the backward
-// loads its sub-tiles.
-st_status encode_qp_map(uint8_t* qp, const Shape& s, bool f16, int box_rows, CUtensorMap* map) {
+// 128-byte swizzle: the Q' rows (the forward stores its tiles, the backward
+// loads sub-tiles) and the forward's shared K' tiles.
+st_status encode_operand_rows_map(uint8_t* base, int B, int S, int H, bool f16, int box_rows, CUtensorMap* map) {
   st_tensor t;
   memset(&t, 0, sizeof(t));
-  t.data = qp;
+  t.data = base;
   t.dtype = f16 ? ST_F16 : ST_BF16;
   t.ndim = 4;
-  t.shape[0] = s.B; t.shape[1] = s.Sq; t.shape[2] = s.H; t.shape[3] = kD;
-  t.stride[3] = 1; t.stride[2] = kD; t.stride[1] = (int64_t)s.H * kD; t.stride[0] = (int64_t)s.Sq * s.H * kD;
+  t.shape[0] = B; t.shape[1] = S; t.shape[2] = H; t.shape[3] = kD;
+  t.stride[3] = 1; t.stride[2] = kD; t.stride[1] = (int64_t)H * kD; t.stride[0] = (int64_t)S * H * kD;
   int s_first = 0;
   st_status st = encode_rows_map(&t, map, &s_first, box_rows);
-  if (st == ST_OK && s_first) return fail(ST_ERR_UNSUPPORTED, "unexpected Q' map order");
+  if (st == ST_OK && s_first) return fail(ST_ERR_UNSUPPORTED, "unexpected operand-row map order");
   return st;
 }
 
@@ -621,7 +638,7 @@ st_status encode_qp_map(uint8_t* qp, const Shape& s, bool f16, int box_rows, CUt
 st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k, const st_tensor* v,
                           const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps, const st_rope* rope,
                           const st_tensor* mask, int causal, float scale, st_tensor* o, const RowTensor& ro,
-                          st_tensor* lse, uint8_t* ws, uint8_t* qp, cudaStream_t stream) {
+                          st_tensor* lse, uint8_t* ws, uint8_t* qp, bool kcache, cudaStream_t stream) {
   st_status st;
   Dev dev;
   if ((st = device_globals(&dev)) != ST_OK) return st;
@@ -654,10 +671,18 @@ st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k,
     if (P.nKt > 0 && (st = encode_rows_map(k, &fp.tmap_k, &fp.k_s_first)) != ST_OK) return st;
   }
   if (qp) {
-    if ((st = encode_qp_map(qp, P.sh, v->dtype == ST_F16, kTile, &fp.tmap_qp)) != ST_OK) return st;
+    if ((st = encode_operand_rows_map(qp, P.sh.B, P.sh.Sq, P.sh.H, v->dtype == ST_F16, kTile, &fp.tmap_qp)) != ST_OK) return st;
     fp.save_qp = 1;
   }
-  if ((st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  kcache = kcache && P.kcache;
+  if (kcache) {
+    if ((st = encode_operand_rows_map(ws + P.off_kcache, P.sh.B, P.sh.Skv, P.sh.Hkv, v->dtype == ST_F16, kTile,
+                                      &fp.tmap_kc)) != ST_OK)
+      return st;
+    fp.kflags = reinterpret_cast<uint32_t*>(ws + P.off_kflags);
+    fp.kcache = 1;
+  }
+  if ((st = launch_prelude(P, rope, mask, ws, dev, stream, kcache)) != ST_OK) return st;
   return cuda_check(launch_counted(ST_K_FWD, stream, [&] { return launch_fwd(fp, stream); }), "forward kernel launch");
 }
 
@@ -708,7 +733,7 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
       qp = static_cast<uint8_t*>(workspace) + PB.off_qp;
   }
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(workspace), qp, stream)) != ST_OK)
+                            static_cast<uint8_t*>(workspace), qp, true, stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
@@ -763,7 +788,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
     // the Q' rows of the workspace, 32-row boxes (each CTA of a pair loads half a sub-tile)
     if ((int64_t)s.B * s.Sq * s.H > 0 &&
-        (st = encode_qp_map(ws + P.off_qp, s, v->dtype == ST_F16, kTile / 4, &bp.tmap_q)) != ST_OK)
+        (st = encode_operand_rows_map(ws + P.off_qp, s.B, s.Sq, s.H, v->dtype == ST_F16, kTile / 4, &bp.tmap_q)) != ST_OK)
       return st;
     if ((st = encode_table_map(reinterpret_cast<const float2*>(ws + P.off_tab_k), (int64_t)P.ids_k.Bt * s.Skv,
                                &bp.tmap_tab_k)) != ST_OK)
@@ -923,11 +948,12 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   Plan P;
   st_status st = plan_call(q, k, v, mask, causal, rope, 0, &P);
   if (st != ST_OK) return st;
-  if (P.total > ST_NOALLOC_SCRATCH_BYTES)
+  // the K' tile cache is used only when it fits as well
+  if (P.fwd_base > ST_NOALLOC_SCRATCH_BYTES)
     return fail(ST_ERR_WORKSPACE,
                 "this call needs %zu bytes of scratch; the built-in scratch holds %u bytes "
                 "(use st_rope_attn_fwd with a caller workspace)",
-                P.total, (unsigned)ST_NOALLOC_SCRATCH_BYTES);
+                P.fwd_base, (unsigned)ST_NOALLOC_SCRATCH_BYTES);
   const Shape& s = P.sh;
   if ((st = check_vec(q_norm_w, "q_norm_w", kD)) != ST_OK) return st;
   if ((st = check_vec(k_norm_w, "k_norm_w", kD)) != ST_OK) return st;
@@ -949,7 +975,7 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   if ((st = noalloc_scratch_address(&scratch)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(scratch), nullptr, stream)) != ST_OK)
+                            static_cast<uint8_t*>(scratch), nullptr, P.total <= ST_NOALLOC_SCRATCH_BYTES, stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;

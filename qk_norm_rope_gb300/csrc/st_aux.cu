@@ -48,6 +48,8 @@ __device__ __forceinline__ float table_elem(const void* t, int dtype, int64_t e)
 // form, entry 2p of the caller's pair-duplicated cos/sin rows.
 __global__ void table_kernel(const __grid_constant__ TableParams p) {
   if (blockIdx.x == 0 && threadIdx.x < kCtrlWords && p.ctrl) p.ctrl[threadIdx.x] = 0u;
+  for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.n_zero; e += (int64_t)gridDim.x * blockDim.x)
+    p.zero[e] = 0u;
   const int64_t n = (int64_t)p.Bt * p.S * kPairs;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
     const int pr = static_cast<int>(e & (kPairs - 1));

@@ -36,6 +36,8 @@ struct TableParams {
   float2* out;               // [Bt, S, 64] (cos, sin) fp32
   __half2* out16;            // [Bt, S, 64] (cos, sin) fp16, read by the operand prologues
   unsigned* ctrl;            // zeroed when non-null
+  unsigned* zero;            // n_zero further words zeroed (the forward's K' publication flags), or null
+  int64_t n_zero;
 };
 
 struct ClassifyParams {

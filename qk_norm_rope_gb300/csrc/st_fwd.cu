@@ -70,7 +70,8 @@ enum {
   kBarOFull = kBarPFull + 2,
   kNumBars = kBarOFull + 1
 };
-static_assert(kNumBars * 8 + 16 <= 256, "barrier area");
+static_assert(kNumBars * 8 + 32 <= 256, "barrier area");  // + TMEM slot, abort flag, sink, K stage modes
+constexpr int kBarIdProl = 1;  // named barrier of the prologue warps
 
 // Byte offsets of K-step kk (16 elements) inside a K-major tile (two 64-column
 // halves) and inside an MN-major tile (16 rows of 128 B per step); the MMA
@@ -118,14 +119,26 @@ __device__ __forceinline__ uint8_t tile_flag(const PairFlags& f, int ti, int kt)
 __device__ __forceinline__ float c_wq(const Common& c, int d) { return __ldg(c.wq + d); }
 __device__ __forceinline__ float c_wk(const Common& c, int d) { return __ldg(c.wk + d); }
 
-// Next key tile at or after kt that at least one of the two query tiles needs.
+// The CTA's walk over its key tiles [0, L): position u visits tile
+// (u + rot) mod L. The CTAs of a head start at evenly spread tiles, so that a
+// K' tile one of them publishes is usually in place before the others reach
+// it (the online softmax does not depend on the order).
+struct KWalk {
+  int L, rot;
+  __device__ __forceinline__ int tile(int u) const { return u + rot >= L ? u + rot - L : u + rot; }
+};
+
+// Next walk position at or after u whose tile at least one of the two query
+// tiles needs.
 template <int MK>
-__device__ __forceinline__ int next_tile(const PairFlags& f, int kt, int kt_end) {
+__device__ __forceinline__ int next_tile(const PairFlags& f, const KWalk& w, int u) {
   if constexpr (MK == kMaskBool) {
-    for (; kt < kt_end; ++kt)
+    for (; u < w.L; ++u) {
+      const int kt = w.tile(u);
       if (tile_flag<MK>(f, 0, kt) != kTileAllFalse || tile_flag<MK>(f, 1, kt) != kTileAllFalse) break;
+    }
   }
-  return kt;
+  return u;
 }
 
 // Base-2 scores of 32 key columns [j0, j0 + 32) of query row i from their raw
@@ -227,6 +240,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  // per K stage: 1 when the stage received a finished K' tile from the
+  // workspace (another CTA published it), 0 when the prologue builds it
+  volatile uint32_t* kmode = tslot + 4;
 
   const Common& c = P.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
@@ -277,6 +293,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   if (warp == kWarpTma && lane_id == 0) {
     tma_prefetch_desc(&P.tmap_v);
     if (P.save_qp) tma_prefetch_desc(&P.tmap_qp);
+    if (P.kcache) tma_prefetch_desc(&P.tmap_kc);
     if constexpr (QKT) {
       tma_prefetch_desc(&P.tmap_q);
       tma_prefetch_desc(&P.tmap_k);
@@ -289,6 +306,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
 
   int kt_end = c.nKt;
   if (CAUSAL) kt_end = min(c.nKt, (qt0 * kTile + 2 * kTile - 1) / kTile + 1);
+  KWalk kw;
+  kw.L = kt_end;
+  kw.rot = kt_end > 0 ? static_cast<int>((static_cast<int64_t>(pair) * kt_end) / gridDim.x) : 0;
   const long long budget = c.wait_budget;
 
   if (warp < kSoftWarps) {
@@ -306,7 +326,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     float m_run = -INFINITY, l_run = 0.f;
     int n = 0, useful = 0;
     bool ok = true;
-    for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end; kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+    for (int u = next_tile<MK>(fl, kw, 0); u < kw.L; u = next_tile<MK>(fl, kw, u + 1), ++n) {
+      const int kt = kw.tile(u);
       const uint8_t flag = tile_flag<MK>(fl, ti, kt);
       useful += (flag != kTileAllFalse && (!CAUSAL || kt <= qt0 + ti)) ? 1 : 0;
       const int j0 = kt * kTile;
@@ -489,24 +510,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       fence_proxy_async_smem();
       mbar_arrive(&bars[kBarQFull]);
     }
+    // one decision for the prologue warps, which share a named barrier below
+    ok = !named_bar_any(kBarIdProl, kProlWarps * 32, !ok);
+    // K' tiles: built here unless another CTA of the same head already
+    // published the tile in the workspace (the TMA warp then loaded it
+    // finished). A tile built here is published in turn: thread 0 stores it by
+    // TMA and, once the store has completed, raises the tile's flag (release);
+    // the flag of one tile is raised when the next one is published or at the
+    // end, so the wait for completion never stalls a tile.
+    const uint32_t* flag_row = P.kflags + ((int64_t)b * c.Hkv + hk) * c.nKt;
+    int pend_kt = -1;  // thread 0: the tile whose store is in flight
+    auto raise_pending = [&]() {
+      if (pend_kt < 0) return;
+      bulk_wait_all();
+      fence_proxy_async_global();
+      st_release_gpu(const_cast<uint32_t*>(flag_row) + pend_kt, 1u);
+      pend_kt = -1;
+    };
     int n = 0;
-    for (int kt = next_tile<MK>(fl, 0, kt_end); ok && kt < kt_end;
-         kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+    for (int u = next_tile<MK>(fl, kw, 0); ok && u < kw.L; u = next_tile<MK>(fl, kw, u + 1), ++n) {
+      const int kt = kw.tile(u);
       const int slot = n % kKStages;
       uint8_t* tile = sm + kOffK + slot * kTileBytes;
-      if constexpr (QKT) {
-        const int j = kt * kTile + prow;
-        HalfRowPrologue<F16> hp;
-        if (j < c.Skv) {
-          const __half2* t16 = c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs;
-          hp.prefetch(t16, hh);
-          hp.prefetch2(t16, hh);
-        }
-        if (!wait_bar_warp(&bars[kBarKRaw + slot], (n / kKStages) & 1, abort_flag, budget)) break;
-        hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
-      } else {
-        if (n >= kKStages && !wait_bar(&bars[kBarKEmpty + slot], ((n / kKStages) - 1) & 1, abort_flag, budget)) break;
-        if (p < kTile) {
+      // the stage is free and its rows (raw, or a published K' tile) have
+      // landed; fp32 rows are read from global memory below
+      const bool got = wait_bar_warp(&bars[kBarKRaw + slot], (n / kKStages) & 1, abort_flag, budget);
+      const bool cached = got && kmode[slot] != 0u;
+      if (got && !cached) {
+        if constexpr (QKT) {
+          const int j = kt * kTile + prow;
+          HalfRowPrologue<F16> hp;
+          if (j < c.Skv) {
+            const __half2* t16 = c.tab16_k + b * c.tab_k_sb + (int64_t)j * kPairs;
+            hp.prefetch(t16, hh);
+            hp.prefetch2(t16, hh);
+          }
+          hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
+        } else if (p < kTile) {
           const int j = kt * kTile + p;
           if (j < c.Skv)
             rope_norm_global<F16>(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
@@ -514,10 +554,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           else
             zero_row(tile, p);
         }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
+      if (P.kcache) {
+        if (named_bar_any(kBarIdProl, kProlWarps * 32, !got)) break;  // the tile's rows are final
+        if (!cached && p == 0) {
+          raise_pending();
+          tma_store_4d(&P.tmap_kc, tile, 0, hk, kt * kTile, b);  // rows past S_kv are clipped
+          tma_store_4d(&P.tmap_kc, tile + kHalfBytes, 64, hk, kt * kTile, b);
+          bulk_commit_group();
+          bulk_wait_read_all();  // read before the stage can be released and refilled
+          pend_kt = kt;
+        }
+      } else if (!got) {
+        break;
+      }
       mbar_arrive(&bars[kBarKFull + slot]);
     }
+    if (p == 0) raise_pending();
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: raw Q, raw K (lane 0), V (lane 1)
     if (lane_id == 0) {
@@ -531,28 +585,43 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           tma_load_4d(tile, &P.tmap_q, &bars[kBarQRaw], 0, y, z, b);
           tma_load_4d(tile + kHalfBytes, &P.tmap_q, &bars[kBarQRaw], 64, y, z, b);
         }
-        int n = 0;
-        for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end;
-             kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
-          const int slot = n % kKStages;
-          if (n >= kKStages && !wait_bar(&bars[kBarKEmpty + slot], ((n / kKStages) - 1) & 1, abort_flag, budget))
-            break;
-          uint8_t* ktile = sm + kOffK + slot * kTileBytes;
+      }
+      // the K ring: a published K' tile (finished, from the workspace), else
+      // the raw 16-bit rows (normalised in place by the prologue), else (fp32
+      // rows, which the prologue reads itself) a plain arrival
+      const uint32_t* flag_row = P.kflags + ((int64_t)b * c.Hkv + hk) * c.nKt;
+      int n = 0;
+      for (int u = next_tile<MK>(fl, kw, 0); u < kw.L; u = next_tile<MK>(fl, kw, u + 1), ++n) {
+        const int kt = kw.tile(u);
+        const int slot = n % kKStages;
+        if (n >= kKStages && !wait_bar(&bars[kBarKEmpty + slot], ((n / kKStages) - 1) & 1, abort_flag, budget))
+          break;
+        uint8_t* ktile = sm + kOffK + slot * kTileBytes;
+        const bool cached = P.kcache && ld_acquire_gpu(flag_row + kt) != 0u;
+        kmode[slot] = cached ? 1u : 0u;
+        if (cached) {
+          fence_proxy_async_global();  // the TMA read is ordered after the flag
+          mbar_arrive_expect_tx(&bars[kBarKRaw + slot], kTileBytes);
+          tma_load_4d(ktile, &P.tmap_kc, &bars[kBarKRaw + slot], 0, hk, kt * kTile, b);
+          tma_load_4d(ktile + kHalfBytes, &P.tmap_kc, &bars[kBarKRaw + slot], 64, hk, kt * kTile, b);
+        } else if constexpr (QKT) {
           const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
           mbar_arrive_expect_tx(&bars[kBarKRaw + slot], kTileBytes);
           tma_load_4d(ktile, &P.tmap_k, &bars[kBarKRaw + slot], 0, y, z, b);
           tma_load_4d(ktile + kHalfBytes, &P.tmap_k, &bars[kBarKRaw + slot], 64, y, z, b);
+        } else {
+          mbar_arrive(&bars[kBarKRaw + slot]);
         }
-        // every issued load lands before the CTA exits (these waits do not
-        // give up on abort; each is bounded)
-        mbar_wait(&bars[kBarQRaw], 0, budget);
-        for (int m = max(0, n - kKStages); m < n; ++m)
-          mbar_wait(&bars[kBarKRaw + m % kKStages], (m / kKStages) & 1, budget);
       }
+      // every issued load lands before the CTA exits (these waits do not
+      // give up on abort; each is bounded)
+      if constexpr (QKT) mbar_wait(&bars[kBarQRaw], 0, budget);
+      for (int m = max(0, n - kKStages); m < n; ++m)
+        mbar_wait(&bars[kBarKRaw + m % kKStages], (m / kKStages) & 1, budget);
     } else if (lane_id == 1) {
       int n = 0;
-      for (int kt = next_tile<MK>(fl, 0, kt_end); kt < kt_end;
-           kt = next_tile<MK>(fl, kt + 1, kt_end), ++n) {
+      for (int u = next_tile<MK>(fl, kw, 0); u < kw.L; u = next_tile<MK>(fl, kw, u + 1), ++n) {
+        const int kt = kw.tile(u);
         const int slot = n % kVStages;
         if (n >= kVStages && !wait_bar(&bars[kBarVEmpty + slot], ((n / kVStages) - 1) & 1, abort_flag, budget)) break;
         uint8_t* tile = sm + kOffV + slot * kTileBytes;
@@ -587,10 +656,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const uint64_t dV0 = sdesc_sw128(smem_u32(sm + kOffV), kHalfBytes, 1024);
       const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
       bool ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
-      int kt = next_tile<MK>(fl, 0, kt_end);
+      int u = next_tile<MK>(fl, kw, 0);  // walk position (the MMAs need no tile index)
       int n = 0;
       bool issued = false;
-      if (ok && kt < kt_end) {
+      if (ok && u < kw.L) {
         ok = wait_bar(&bars[kBarKFull + 0], 0, abort_flag, budget);
         if (ok) {
           tc_fence_after();
@@ -602,10 +671,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           issued = true;
         }
       }
-      while (ok && kt < kt_end) {
+      while (ok && u < kw.L) {
         const int vslot = n % kVStages;
-        const int kt_next = next_tile<MK>(fl, kt + 1, kt_end);
-        const bool has_next = kt_next < kt_end;
+        const int u_next = next_tile<MK>(fl, kw, u + 1);
+        const bool has_next = u_next < kw.L;
         const int nslot = (n + 1) % kKStages;
         const uint64_t dV = sdesc_add(dV0, vslot * kTileBytes), dK = sdesc_add(dK0, nslot * kTileBytes);
         if (!(ok = wait_bar(&bars[kBarVFull + vslot], (n / kVStages) & 1, abort_flag, budget))) break;
@@ -627,7 +696,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           mma_commit(&bars[kBarSFull + 1]);
           mma_commit(&bars[kBarKEmpty + nslot]);
         }
-        kt = kt_next;
+        u = u_next;
         ++n;
       }
       if (issued) {
