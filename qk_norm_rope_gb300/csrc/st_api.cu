@@ -799,6 +799,14 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   // the table kernel would have cleared)
   const bool reuse = rope->reuse_tables != 0 && (int64_t)s.B * s.Sq * s.H > 0;
   if (!reuse && (st = launch_prelude(P, rope, mask, ws, dev, stream)) != ST_OK) return st;
+  if (reuse && P.kcache && P.nKt > 0) {
+    // the forward on this workspace published every K' tile that a query tile needs
+    if ((st = encode_operand_rows_map(ws + P.off_kcache, s.B, s.Skv, s.Hkv, v->dtype == ST_F16, kTile,
+                                      &bp.tmap_kc)) != ST_OK)
+      return st;
+    bp.kp_ready = 1;
+    bp.kflags = reinterpret_cast<const uint32_t*>(ws + P.off_kflags);
+  }
   if (!reuse && !P.f32 && P.nKt > 0 && (int64_t)s.B * s.Sq * s.H > 0) {
     // no forward left its Q' rows in this workspace: build them
     QPrimeParams qpp;

@@ -104,7 +104,7 @@ enum {
   kBarEpi,                               // epilogue: raw k rows and (cos, sin) rows staged
   kNumBars
 };
-static_assert(kNumBars * 8 + 12 <= kBarBytes, "barrier area");
+static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");  // + TMEM slot, abort flag, sink, K tile mode
 
 __device__ __forceinline__ uint32_t kofs128(int kk) { return (kk >> 2) * kHalfBytes + (kk & 3) * 32; }  // K-major, 128 rows
 __device__ __forceinline__ uint32_t kofs64(int kk) { return (kk >> 2) * kSubHalf + (kk & 3) * 32; }     // K-major, 64 rows
@@ -494,7 +494,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   float* stat = reinterpret_cast<float*>(sm + kOffStat);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
-  uint32_t* scratch = tslot + 2;  // sink for pin_loads
+  uint32_t* scratch = tslot + 2;  // [0]: sink for pin_loads; [1]: 1 when the K' tile came finished from the forward
 
   const Common& c = P.c;
   const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
@@ -536,6 +536,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     tma_prefetch_desc(&P.tmap_dq);
     tma_prefetch_desc(&P.tmap_k);
     tma_prefetch_desc(&P.tmap_tab_k);
+    if (P.kp_ready) tma_prefetch_desc(&P.tmap_kc);
     tma_prefetch_desc(&P.tmap_q);
   }
   tc_fence_before();
@@ -746,8 +747,12 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         zero_row(sm + kOffV, row);
       }
     } else {
-      if constexpr (QKT) ok = wait_bar(&bars[kBarKRaw], 0, abort_flag, budget);
-      for (int row = p; ok && row < kTile; row += kProlThreads) {
+      // the tile's rows have landed: raw 16-bit rows, or the K' tile that the
+      // forward published (then nothing is left to do); fp32 rows are read
+      // from global memory below
+      ok = wait_bar(&bars[kBarKRaw], 0, abort_flag, budget);
+      const bool cached = *reinterpret_cast<volatile uint32_t*>(scratch + 1) != 0u;
+      for (int row = p; ok && !cached && row < kTile; row += kProlThreads) {
         const int jj = kt * kTile + row;
         if constexpr (QKT) {
           if (jj < c.Skv)  // rows past S_kv stay TMA zeros
@@ -807,11 +812,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     // ------------------------------------------------------------ TMA: raw K, V, raw Q
     if (lane_id == 0) {
       if (!phantom) {
-        if constexpr (QKT) {
+        // K' as the forward published it (rows past S_kv read as zeros), else
+        // the raw rows (16-bit), else a plain arrival (fp32 rows)
+        const bool cached = P.kp_ready && P.kflags[((int64_t)b * c.Hkv + hk) * c.nKt + kt] != 0u;
+        scratch[1] = cached ? 1u : 0u;
+        if (cached) {
+          mbar_arrive_expect_tx(&bars[kBarKRaw], kTileBytes);
+          tma_load_4d(sm + kOffK, &P.tmap_kc, &bars[kBarKRaw], 0, hk, kt * kTile, b);
+          tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_kc, &bars[kBarKRaw], 64, hk, kt * kTile, b);
+        } else if constexpr (QKT) {
           const int y = P.k_s_first ? kt * kTile : hk, z = P.k_s_first ? hk : kt * kTile;
           mbar_arrive_expect_tx(&bars[kBarKRaw], kTileBytes);
           tma_load_4d(sm + kOffK, &P.tmap_k, &bars[kBarKRaw], 0, y, z, b);
           tma_load_4d(sm + kOffK + kHalfBytes, &P.tmap_k, &bars[kBarKRaw], 64, y, z, b);
+        } else {
+          mbar_arrive(&bars[kBarKRaw]);
         }
         const int vy = P.v_s_first ? kt * kTile : hk, vz = P.v_s_first ? hk : kt * kTile;
         mbar_arrive_expect_tx(&bars[kBarVFull], kTileBytes);
@@ -845,7 +860,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       // give up on abort; each is bounded)
       if (!phantom) {
         mbar_wait(&bars[kBarVFull], 0, budget);
-        if constexpr (QKT) mbar_wait(&bars[kBarKRaw], 0, budget);
+        mbar_wait(&bars[kBarKRaw], 0, budget);
       }
       for (int x = max(0, q_issued - kQStages); x < q_issued; ++x)
         mbar_wait(&bars[kBarQRaw + x % kQStages], (x / kQStages) & 1, budget);

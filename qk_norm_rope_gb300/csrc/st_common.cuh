@@ -90,6 +90,9 @@ struct BwdParams {
   CUtensorMap tmap_dv;     // dv rows, 128-row boxes (TMA store of the epilogue)
   CUtensorMap tmap_dk;     // dk rows, 128-row boxes (16-bit k only)
   CUtensorMap tmap_dq;  // dq_acc as (d, h, s, b), fp32, 128B swizzle, box 32 x 64 rows (reduce target)
+  CUtensorMap tmap_kc;  // the forward's shared K' tiles, 128-row boxes (kp_ready)
+  int kp_ready;         // 1: the workspace holds the forward's K' tiles and their flags (a reusing backward)
+  const uint32_t* kflags;  // [B, Hkv, nKt]: 1 where the forward published the tile
   int v_s_first, do_s_first, q_s_first, k_s_first, dv_s_first, dk_s_first;
   int qk_tma;
   const void* dout;

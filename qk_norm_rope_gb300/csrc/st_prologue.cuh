@@ -25,20 +25,28 @@ struct RowInplace {
 #pragma unroll
     for (int c = 0; c < kD / 8; ++c) cs[c] = ldg_nc_v4(t16 + c);
   }
+  // The sum of squares is taken per 64-column half (even and odd columns
+  // apart) and the halves added, the order of HalfRowPrologue, so that a K'
+  // row built here equals the forward's bit for bit.
   __device__ __forceinline__ void finish(uint8_t* tile, int row, const float* w, float eps) const {
-    float a0 = 0.f, a1 = 0.f;
+    float half_ss[2];
 #pragma unroll
-    for (int c = 0; c < kD / 8; ++c) {
-      const uint4 v = *reinterpret_cast<const uint4*>(tile + (c >> 3) * kHalfBytes + sw128_off(row, c & 7));
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    for (int hh = 0; hh < 2; ++hh) {
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float lo = lo16<F16>(u[e]), hi = hi16<F16>(u[e]);
-        a0 = fmaf(lo, lo, a0);
-        a1 = fmaf(hi, hi, a1);
+      for (int c = 0; c < 8; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + hh * kHalfBytes + sw128_off(row, c));
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float lo = lo16<F16>(u[e]), hi = hi16<F16>(u[e]);
+          a0 = fmaf(lo, lo, a0);
+          a1 = fmaf(hi, hi, a1);
+        }
       }
+      half_ss[hh] = a0 + a1;
     }
-    const float r = rsqrtf((a0 + a1) * (1.0f / kD) + eps);
+    const float r = rsqrtf((half_ss[0] + half_ss[1]) * (1.0f / kD) + eps);
     const float4* w4 = reinterpret_cast<const float4*>(w);
 #pragma unroll
     for (int c = 0; c < kD / 8; ++c) {
