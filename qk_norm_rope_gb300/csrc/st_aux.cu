@@ -116,7 +116,7 @@ __global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
 // owns head dims 4l..4l+3 of each row. Block 0 also clears the weight-gradient
 // reduction counters (the table kernel, which clears them otherwise, may be
 // skipped by a backward that reuses the forward's tables).
-constexpr int kPreRows = 4;
+constexpr int kPreRows = 2;
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ PreParams p) {
   if (blockIdx.x == 0 && threadIdx.x < 2 && p.ctrl) p.ctrl[kCtrlDwDone + threadIdx.x] = 0u;
@@ -192,7 +192,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-constexpr int kPostRows = 4;  // rows per warp and pass, their loads issued together
+constexpr int kPostRows = 1;  // rows per warp and pass, their loads issued together
 
 __global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_constant__ PostParams p) {
   __shared__ float4 part[kPostWarps][32];

@@ -67,7 +67,10 @@ constexpr uint32_t kSubHalf = kSubBytes / 2;
 constexpr int kPeerRows = kSub / kCluster;                 // Q' rows produced per CTA per sub-tile
 constexpr uint32_t kPeerRowsBytes = kPeerRows * 128;       // those rows in one column half
 constexpr uint32_t kRBoxBytes = kSub * 32 * 4;             // one [64 queries][32 head dims] fp32 box
-constexpr int kBarIdEpi = 4, kEpiThreads = kComputeWarps * 32;  // named barrier of the epilogue warps
+// named barrier of the epilogue: the compute, drain and prologue warps (16)
+constexpr int kBarIdEpi = 4, kEpiThreads = (kComputeWarps + kDrainWarps + kProlWarps) * 32;
+static_assert(kComputeWarps + kDrainWarps + kProlWarps == 16 && kWarpProl0 + kProlWarps == kWarpMma,
+              "the epilogue warps are warps 0-15: four per TMEM lane quarter");
 constexpr uint32_t kBoxBytes = 128 * 128;                  // a [128 rows][128 bytes] TMA box
 
 // shared memory layout (offsets from the 1024-byte aligned dynamic base)
@@ -218,42 +221,33 @@ __device__ __forceinline__ float warp_reduce_scatter32(float (&v)[32], int lane)
   return v[0];
 }
 
-// dK of key row j, shared by two threads: the thread of warp w holds head
-// dims [64 hh, 64 hh + 64) (hh = w / 4) of the row in its TMEM lane (the dK'
-// accumulator, the gradient of the rotated, normed row divided by the softmax
-// scale). With x the raw k row, r = 1 / sqrt(mean x^2 + eps), g = scale dK',
-// dy = R^T g (the rotation with sin negated) and g' = w dy:
+// dK of key row j, shared by four threads: the thread of warp w (of the
+// sixteen epilogue warps) holds head dims [32 cq, 32 cq + 32) (cq = w / 4) of
+// the row in its TMEM lane (the dK' accumulator, the gradient of the rotated,
+// normed row divided by the softmax scale). With x the raw k row,
+// r = 1 / sqrt(mean x^2 + eps), g = scale dK', dy = R^T g (the rotation with
+// sin negated) and g' = w dy:
 //   dk = r g' - (r^3 / D) x (x . g'),   dW_k gathers dy x r.
 // The raw row (bf16: the two 64-column halves of kOffK; fp32: four 32-column
 // boxes over kOffK..kOffV) and the row's fp32 (cos, sin) (four 32-float boxes
 // at kOffQ) were staged by TMA, 128B-swizzled. The two row sums (x.x, x.g')
-// are completed through `ex` in shared memory, between named barriers of the
-// eight epilogue warps; sWk holds the k norm weights. A 16-bit dk row goes to
-// `stage` (the operand-tile layout, stored by TMA afterwards); an fp32 one is
-// stored directly. Returns, in lane l, the sums of dy x r at columns 64 hh + l
-// (x) and 64 hh + 32 + l (y) over the warp's 32 rows.
+// are completed through `ex_ss` and `ex_xg` in shared memory, between named
+// barriers of the epilogue warps; sWk holds the k norm weights. A 16-bit dk
+// row goes to `stage` (the operand-tile layout, stored by TMA afterwards); an
+// fp32 one is stored directly. Returns, in lane l, the sum of dy x r at column
+// 32 cq + l over the warp's 32 rows.
 // Out of line: it runs once per CTA, and inlined it would spread the roles'
 // hot loops over more instruction-cache lines.
 template <bool QKT, bool F16>
-__device__ __noinline__ float2 dk_half_rows(const BwdParams& P, const uint8_t* sm, uint32_t tacc, bool have, int b,
-                                               int hk, int j, int r, int hh, bool key_ok, int lane, float* ex,
-                                               const float* sWk, uint8_t* stage) {
-  float colsum[2];
+__device__ __noinline__ float dk_quarter_rows(const BwdParams& P, const uint8_t* sm, uint32_t tacc, bool have, int b,
+                                              int hk, int j, int r, int cq, bool key_ok, int lane, float* ex_ss,
+                                              float* ex_xg, const float* sWk, uint8_t* stage) {
   const Common& c = P.c;
-  // the chunk (16 bytes) of this thread's half row holding dims 64 hh + 4 t .. +3 (fp32)
-  // or 64 hh + 8 t .. +7 (bf16)
-  auto x_chunk = [&](int t) -> const uint4* {
-    if constexpr (QKT) return reinterpret_cast<const uint4*>(sm + kOffK + hh * kHalfBytes + sw128_off(r, t));
-    return reinterpret_cast<const uint4*>(sm + kOffK + (2 * hh + (t >> 3)) * kBoxBytes + sw128_off(r, t & 7));
-  };
-  // (cos, sin) of pairs 32 hh + 2 t, +1
-  auto tab_chunk = [&](int t) -> float4 {
-    return *reinterpret_cast<const float4*>(sm + kOffQ + (2 * hh + (t >> 3)) * kBoxBytes + sw128_off(r, t & 7));
-  };
-  // eight consecutive dims d0 .. d0 + 7 of the half (d0 a multiple of 8)
+  // eight consecutive dims d0 .. d0 + 7 of the quarter (d0 a multiple of 8)
   auto load_x8 = [&](int d0, float (&x8)[8]) {
     if constexpr (QKT) {
-      const uint4 u = *x_chunk(d0 >> 3);
+      const uint4 u = *reinterpret_cast<const uint4*>(sm + kOffK + (cq >> 1) * kHalfBytes +
+                                                      sw128_off(r, 4 * (cq & 1) + (d0 >> 3)));
       const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -261,15 +255,19 @@ __device__ __noinline__ float2 dk_half_rows(const BwdParams& P, const uint8_t* s
         x8[2 * e + 1] = hi16<F16>(w[e]);
       }
     } else {
-      const float4 a = *reinterpret_cast<const float4*>(x_chunk(d0 >> 2));
-      const float4 bq = *reinterpret_cast<const float4*>(x_chunk((d0 >> 2) + 1));
+      const uint8_t* box = sm + kOffK + cq * kBoxBytes;
+      const float4 a = *reinterpret_cast<const float4*>(box + sw128_off(r, d0 >> 2));
+      const float4 bq = *reinterpret_cast<const float4*>(box + sw128_off(r, (d0 >> 2) + 1));
       x8[0] = a.x; x8[1] = a.y; x8[2] = a.z; x8[3] = a.w; x8[4] = bq.x; x8[5] = bq.y; x8[6] = bq.z; x8[7] = bq.w;
     }
   };
-  // the half row's sum of squares, completed with the partner's half
+  // (cos, sin) of the quarter's pairs 2t, 2t + 1 (pairs 16 cq + 2t ..)
+  auto tab_chunk = [&](int t) -> float4 {
+    return *reinterpret_cast<const float4*>(sm + kOffQ + cq * kBoxBytes + sw128_off(r, t));
+  };
   float ss0 = 0.f, ss1 = 0.f;
 #pragma unroll
-  for (int d0 = 0; d0 < 64; d0 += 8) {
+  for (int d0 = 0; d0 < 32; d0 += 8) {
     float x8[8];
     load_x8(d0, x8);
 #pragma unroll
@@ -278,71 +276,69 @@ __device__ __noinline__ float2 dk_half_rows(const BwdParams& P, const uint8_t* s
       ss1 = fmaf(x8[e + 1], x8[e + 1], ss1);
     }
   }
-  ex[hh * kTile + r] = ss0 + ss1;
+  ex_ss[cq * kTile + r] = ss0 + ss1;
   named_bar(kBarIdEpi, kEpiThreads);
-  const float rr = rsqrtf((ex[r] + ex[kTile + r]) * (1.0f / kD) + c.eps);
+  const float rr =
+      rsqrtf((((ex_ss[r] + ex_ss[kTile + r]) + ex_ss[2 * kTile + r]) + ex_ss[3 * kTile + r]) * (1.0f / kD) + c.eps);
   const float sc = c.scale;
-  const float4* w4 = reinterpret_cast<const float4*>(sWk + 64 * hh);
-  float xg = 0.f;
+  const float4* w4 = reinterpret_cast<const float4*>(sWk + 32 * cq);
+  float xg = 0.f, colsum = 0.f;
 #pragma unroll 1
   for (int pass = 0; pass < 2; ++pass) {
     if (pass == 1) {  // x . g' over the whole row
-      ex[2 * kTile + hh * kTile + r] = xg;
+      ex_xg[cq * kTile + r] = xg;
       named_bar(kBarIdEpi, kEpiThreads);
-      xg = ex[2 * kTile + r] + ex[3 * kTile + r];
+      xg = ((ex_xg[r] + ex_xg[kTile + r]) + ex_xg[2 * kTile + r]) + ex_xg[3 * kTile + r];
     }
     const float c3 = rr * rr * rr * xg * (1.0f / kD);
-#pragma unroll 1
-    for (int q = 0; q < 2; ++q) {
-      uint32_t v[32];
-      if (have) {
-        tmem_ld32(tacc + 32 * q, v);
-      } else {
+    uint32_t v[32];
+    if (have) {
+      tmem_ld32(tacc, v);
+    } else {
 #pragma unroll
-        for (int t = 0; t < 32; ++t) v[t] = 0u;
-      }
-      float u[32];
+      for (int t = 0; t < 32; ++t) v[t] = 0u;
+    }
+    float u[32];
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
-        const int d0 = 32 * q + 8 * c8;  // dims d0 .. d0 + 7 of the half: pairs d0/2 .. d0/2 + 3
-        float x8[8];
-        load_x8(d0, x8);
-        const float4 t0 = tab_chunk(d0 >> 2), t1 = tab_chunk((d0 >> 2) + 1);
-        const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-        const float4 wa = w4[d0 >> 2], wb = w4[(d0 >> 2) + 1];
-        const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+    for (int c8 = 0; c8 < 4; ++c8) {
+      const int d0 = 8 * c8;  // dims d0 .. d0 + 7 of the quarter: pairs d0/2 .. d0/2 + 3
+      float x8[8];
+      load_x8(d0, x8);
+      const float4 t0 = tab_chunk(d0 >> 2), t1 = tab_chunk((d0 >> 2) + 1);
+      const float cs[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      const float4 wa = w4[d0 >> 2], wb = w4[(d0 >> 2) + 1];
+      const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int t = 8 * c8 + 2 * e;
-          const float g0 = __uint_as_float(v[t]) * sc, g1 = __uint_as_float(v[t + 1]) * sc;
-          const float cc = cs[2 * e], sn = cs[2 * e + 1];
-          const float dy0 = fmaf(g0, cc, g1 * sn), dy1 = fmaf(g1, cc, -g0 * sn);
-          const float gw0 = wv[2 * e] * dy0, gw1 = wv[2 * e + 1] * dy1;
-          if (pass == 0) {
-            xg = fmaf(x8[2 * e], gw0, fmaf(x8[2 * e + 1], gw1, xg));
-            u[t] = key_ok ? dy0 * x8[2 * e] * rr : 0.f;
-            u[t + 1] = key_ok ? dy1 * x8[2 * e + 1] * rr : 0.f;
-          } else {
-            u[t] = fmaf(rr, gw0, -c3 * x8[2 * e]);
-            u[t + 1] = fmaf(rr, gw1, -c3 * x8[2 * e + 1]);
-          }
+      for (int e = 0; e < 4; ++e) {
+        const int t = d0 + 2 * e;
+        const float g0 = __uint_as_float(v[t]) * sc, g1 = __uint_as_float(v[t + 1]) * sc;
+        const float cc = cs[2 * e], sn = cs[2 * e + 1];
+        const float dy0 = fmaf(g0, cc, g1 * sn), dy1 = fmaf(g1, cc, -g0 * sn);
+        const float gw0 = wv[2 * e] * dy0, gw1 = wv[2 * e + 1] * dy1;
+        if (pass == 0) {
+          xg = fmaf(x8[2 * e], gw0, fmaf(x8[2 * e + 1], gw1, xg));
+          u[t] = key_ok ? dy0 * x8[2 * e] * rr : 0.f;
+          u[t + 1] = key_ok ? dy1 * x8[2 * e + 1] * rr : 0.f;
+        } else {
+          u[t] = fmaf(rr, gw0, -c3 * x8[2 * e]);
+          u[t + 1] = fmaf(rr, gw1, -c3 * x8[2 * e + 1]);
         }
       }
-      if (pass == 0) {
-        colsum[q] = warp_reduce_scatter32(u, lane);
-      } else if (QKT) {
-        // 16-bit dk: chunks 4q .. 4q+3 of the row's half hh in the staging tile
+    }
+    if (pass == 0) {
+      colsum = warp_reduce_scatter32(u, lane);
+    } else if (QKT) {
+      // 16-bit dk: chunks 4 (cq % 2) .. + 3 of the row's half cq / 2 in the staging tile
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(stage + hh * kHalfBytes + sw128_off(r, 4 * q + c4)) =
-              make_uint4(pack16<F16>(u[8 * c4], u[8 * c4 + 1]), pack16<F16>(u[8 * c4 + 2], u[8 * c4 + 3]),
-                         pack16<F16>(u[8 * c4 + 4], u[8 * c4 + 5]), pack16<F16>(u[8 * c4 + 6], u[8 * c4 + 7]));
-      } else if (key_ok) {
-        store_chunk32(P.dk, b * P.dk_sb + (int64_t)j * P.dk_ss + hk * P.dk_sh, P.dk_dt, 2 * hh + q, u);
-      }
+      for (int c4 = 0; c4 < 4; ++c4)
+        *reinterpret_cast<uint4*>(stage + (cq >> 1) * kHalfBytes + sw128_off(r, 4 * (cq & 1) + c4)) =
+            make_uint4(pack16<F16>(u[8 * c4], u[8 * c4 + 1]), pack16<F16>(u[8 * c4 + 2], u[8 * c4 + 3]),
+                       pack16<F16>(u[8 * c4 + 4], u[8 * c4 + 5]), pack16<F16>(u[8 * c4 + 6], u[8 * c4 + 7]));
+    } else if (key_ok) {
+      store_chunk32(P.dk, b * P.dk_sb + (int64_t)j * P.dk_ss + hk * P.dk_sh, P.dk_dt, cq, u);
     }
   }
-  return make_float2(colsum[0], colsum[1]);
+  return colsum;
 }
 
 // P^T of this thread's key against 32 queries iq0 .. iq0 + 31 on a sub-tile
@@ -373,18 +369,20 @@ __device__ __noinline__ void p_masked(const Common& c, uint32_t tS, float key_te
   tmem_st_wait();
 }
 
-// ---- epilogue of the eight compute warps, once the walk is over (n
-// sub-tiles; `ok` is false after an abort). Warp w holds key rows 32 (w % 4)
-// .. (its TMEM lanes) and head dims [64 hq, 64 hq + 64) of dV and dK'. Once
-// every MMA has completed, the K tile, the Q' ring and the dO ring are free:
-// the raw k rows and the tile's fp32 (cos, sin) rows are staged by TMA (K
-// tile, Q' ring) while dV is laid out in the dO ring and stored by TMA; then
-// dk (inverse rotation + RMSNorm backward) is laid out in the dS buffers and
-// stored by TMA (16-bit k; fp32 rows are stored directly), and each warp
-// writes its partial sums of the k norm-weight gradient.
+// ---- epilogue of the sixteen compute, drain and prologue warps, once their
+// walks are over (n sub-tiles; `ok` is false after an abort). Warp w holds key
+// rows 32 (w % 4) .. (its TMEM lanes) and head dims [32 cq, 32 cq + 32)
+// (cq = w / 4) of dV and dK'. Once every MMA has completed, the K tile, the Q'
+// ring and the dO ring are free: the raw k rows and the tile's fp32 (cos, sin)
+// rows are staged by TMA (K tile, Q' ring) while dV is laid out in the dO ring
+// and stored by TMA; then dk (inverse rotation + RMSNorm backward) is laid out
+// in the dS buffers and stored by TMA (16-bit k; fp32 rows are stored
+// directly), and each warp writes its partial sums of the k norm-weight
+// gradient. The row sums are exchanged through the stat area and the drain's
+// staging boxes (free once the drain is done).
 // Out of line, with every index derived again from the thread and block
 // coordinates, so that nothing it needs stays live in registers through the
-// main loop: with its values held across the loop (inlined, or called with
+// main loops: with its values held across the loop (inlined, or called with
 // them as arguments) the whole kernel took 12% longer at the 96-register cap
 // (Flux1 1024px backward: 1039 us against 924 us).
 template <bool QKT, bool F16>
@@ -398,17 +396,21 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
   const int tid = threadIdx.x, warp = tid >> 5, lane_id = tid & 31;
   const int kt = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const bool phantom = kt >= c.nKt;
-  const int qd = warp & 3, hq = warp >> 2;
+  const int qd = warp & 3, cq = warp >> 2;
   const int r = qd * 32 + lane_id;
   const int j = kt * kTile + r;
   const bool key_ok = j < c.Skv;
   const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
-  if (ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
-  // one decision for the eight warps (they share named barriers below)
+  // the compute warps learn here that every MMA is done (the drain warps
+  // waited for the last dQ'^T themselves; the barrier below orders the rest)
+  if (warp < kComputeWarps && ok && n > 0)
+    ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
+  // one decision for the sixteen warps (they share named barriers below)
   if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
     tc_fence_after();
-    float* ex = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed: row-sum exchange (2 KB)
-    float* sWk = reinterpret_cast<float*>(sm + kOffW);     // k norm weights
+    float* ex_ss = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed (2 KB)
+    float* ex_xg = reinterpret_cast<float*>(sm + kOffR);     // the drain is done with its boxes
+    float* sWk = reinterpret_cast<float*>(sm + kOffW);       // k norm weights
     const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
     if (tid == 0) {
       fence_proxy_async_smem();
@@ -427,27 +429,23 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
     }
     if (tid < kD) sWk[tid] = __ldg(c.wk + tid);
     {
-      // dV: this thread's 64 columns of row r, 16-bit, into the dO ring in
-      // the operand-tile layout
-      uint8_t* stage = sm + kOffDO + hq * kHalfBytes;
-      const uint32_t tacc = tmem + 256 + lanebits + 64 * hq;
-#pragma unroll 1
-      for (int q = 0; q < 2; ++q) {
-        uint32_t v[32];
-        if (n > 0) {
-          tmem_ld32(tacc + 32 * q, v);
-        } else {
+      // dV: this thread's 32 columns of row r, 16-bit, into the dO ring in the
+      // operand-tile layout
+      uint8_t* stage = sm + kOffDO + (cq >> 1) * kHalfBytes;
+      uint32_t v[32];
+      if (n > 0) {
+        tmem_ld32(tmem + 256 + lanebits + 32 * cq, v);
+      } else {
 #pragma unroll
-          for (int t = 0; t < 32; ++t) v[t] = 0u;
-        }
-#pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4)
-          *reinterpret_cast<uint4*>(stage + sw128_off(r, 4 * q + c4)) =
-              make_uint4(pack16<F16>(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
-                         pack16<F16>(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
-                         pack16<F16>(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
-                         pack16<F16>(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
+        for (int t = 0; t < 32; ++t) v[t] = 0u;
       }
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4)
+        *reinterpret_cast<uint4*>(stage + sw128_off(r, 4 * (cq & 1) + c4)) =
+            make_uint4(pack16<F16>(__uint_as_float(v[8 * c4]), __uint_as_float(v[8 * c4 + 1])),
+                       pack16<F16>(__uint_as_float(v[8 * c4 + 2]), __uint_as_float(v[8 * c4 + 3])),
+                       pack16<F16>(__uint_as_float(v[8 * c4 + 4]), __uint_as_float(v[8 * c4 + 5])),
+                       pack16<F16>(__uint_as_float(v[8 * c4 + 6]), __uint_as_float(v[8 * c4 + 7])));
       fence_proxy_async_smem();
     }
     if (!named_bar_any(kBarIdEpi, kEpiThreads, !wait_bar_warp(&bars[kBarEpi], 0, abort_flag, budget))) {
@@ -457,13 +455,11 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
         tma_store_4d(&P.tmap_dv, sm + kOffDO + kHalfBytes, 64, vy, vz, b);
         bulk_commit_group();
       }
-      const float2 colsum = dk_half_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 64 * hq, n > 0, b, hk, j, r, hq,
-                                                   key_ok, lane_id, ex, sWk, sm + kOffDS);
+      const float colsum = dk_quarter_rows<QKT, F16>(P, sm, tmem + 384 + lanebits + 32 * cq, n > 0, b, hk, j, r,
+                                                     cq, key_ok, lane_id, ex_ss, ex_xg, sWk, sm + kOffDS);
       // this warp's column sums over its 32 rows: one partial row per warp
       // quarter (rows 32 qd ..), added in a fixed order by the reduction
-      float* part = P.dwk_part + ((((int64_t)b * c.Hkv + hk) * c.nKt + kt) * 4 + qd) * kD + 64 * hq;
-      part[lane_id] = colsum.x;
-      part[32 + lane_id] = colsum.y;
+      P.dwk_part[((((int64_t)b * c.Hkv + hk) * c.nKt + kt) * 4 + qd) * kD + 32 * cq + lane_id] = colsum;
       if constexpr (QKT) {
         fence_proxy_async_smem();
         named_bar(kBarIdEpi, kEpiThreads);
@@ -736,7 +732,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         }
       }
     }
-    if (leader) bulk_wait_all();
+    if (leader) bulk_wait_all();  // the boxes are free for the epilogue's exchange
+    bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp < kWarpProl0 + kProlWarps) {
     // ------------------------------------------------------------ Q' / K' prologue
     const int p = tid - kWarpProl0 * 32;  // 0 .. kProlThreads - 1
@@ -791,13 +788,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     WPos m = next_pos<MK>(c, b, W, W.start(), kt0);
     int s = 0;
     if (W.more(m)) load_stats(W.qt(m) * kTile, W.head(m));
-    for (int n = 0; ok && W.more(m); ++n) {
+    int n = 0;
+    for (; ok && W.more(m); ++n) {
       const WPos m_next = s == 0 ? m : next_pos<MK>(c, b, W, W.step(m), kt0);
       const int s_next = s ^ 1;
       const int sq = n % kQStages;
       const float l2 = (lse_c == -INFINITY) ? INFINITY : lse_c * kLog2e, dl = dl_c;
       if (n >= kQStages &&
-          !wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget))
+          !(ok = wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)))
         break;
       if (p < kSub) {
         stat[sq * 2 * kSub + p] = l2;
@@ -808,6 +806,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       m = m_next;
       s = s_next;
     }
+    bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: raw K, V, raw Q
     if (lane_id == 0) {

@@ -45,6 +45,11 @@ constexpr int kFwdThreads = kFwdWarps * 32;
 // rescale O only when the running max grows by more than 8 (base 2); exact
 // either way since O and l always share the same reference max
 constexpr float kRescaleThreshold = 8.0f;
+// Largest score bound (base 2) for which the fixed-reference softmax is used:
+// every P = 2^(s - bound) then lies in [2^-2 bound, 1], normal in fp32 and in
+// bf16 (which has fp32's exponent range; fp16 operands keep the online
+// maximum, as P would fall below fp16's range).
+constexpr float kFixedRefMax = 56.0f;
 
 // shared memory layout (offsets from a 1024-byte aligned base)
 constexpr uint32_t kOffQ = 0;                                  // 2 tiles
@@ -323,7 +328,33 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     constexpr int kVecElems = MK == kMaskBF16 ? 8 : 4;  // elements per 16 bytes
     const bool mask_vec = (reinterpret_cast<uintptr_t>(c.mask) & 15u) == 0 && c.m_sb % kVecElems == 0 &&
                           c.m_sh % kVecElems == 0 && c.m_sq % kVecElems == 0;
-    float m_run = -INFINITY, l_run = 0.f;
+    // Fixed-reference softmax. The operands are RMS-normalised rows scaled by
+    // the norm weights and rotated, so |q'| <= sqrt(D) max|w_q| and
+    // |k'| <= sqrt(D) max|w_k|, and every score obeys
+    //   |s * scale * log2(e)| <= bound = scale * log2(e) * D * max|w_q| * max|w_k|
+    // (times 1.02 for the rounding of q', k' to the 16-bit operand type). When
+    // the mask adds no values (none, bool, causal) and the bound is small
+    // enough, P = 2^(s * scale * log2(e) - bound) needs no row maximum: one
+    // pass over the scores, no rescaling of O; LSE = bound + log2(l). (Softmax
+    // is invariant to the reference; only its range matters.)
+    float fixed_ref = INFINITY;
+    if constexpr ((MK == kMaskNone || MK == kMaskBool) && !F16) {
+      float wq_m = 0.f, wk_m = 0.f;
+#pragma unroll
+      for (int d = lane_id; d < kD; d += 32) {
+        wq_m = fmaxf(wq_m, fabsf(sW[d]));
+        wk_m = fmaxf(wk_m, fabsf(sW[kD + d]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        wq_m = fmaxf(wq_m, __shfl_xor_sync(0xffffffffu, wq_m, o));
+        wk_m = fmaxf(wk_m, __shfl_xor_sync(0xffffffffu, wk_m, o));
+      }
+      const float bound = sc * static_cast<float>(kD) * wq_m * wk_m * 1.02f;
+      if (bound <= kFixedRefMax) fixed_ref = bound;  // the same decision in every thread (same weights)
+    }
+    const bool fixed = fixed_ref != INFINITY;
+    float m_run = fixed ? fixed_ref : -INFINITY, l_run = 0.f;
     int n = 0, useful = 0;
     bool ok = true;
     for (int u = next_tile<MK>(fl, kw, 0); u < kw.L; u = next_tile<MK>(fl, kw, u + 1), ++n) {
@@ -349,6 +380,55 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       }
       if (!(ok = wait_bar_warp(&bars[kBarSFull + ti], n & 1, abort_flag, budget))) break;
       tc_fence_after();
+      if (fixed) {
+        // one pass: P = exp2(s - bound) (16-bit, into the first 64 S columns), row sum
+        float ls0 = 0.f, ls1 = 0.f;
+        if (plain) {
+          uint32_t ra[16], rb[16];
+          const float2 sc2 = make_float2(sc, sc), nb2 = make_float2(-fixed_ref, -fixed_ref);
+          float2 ls = make_float2(0.f, 0.f);
+          tmem_ld16_issue(tS, ra);
+#pragma unroll
+          for (int q8 = 0; q8 < 8; ++q8) {
+            uint32_t(&cur)[16] = (q8 & 1) ? rb : ra;
+            uint32_t(&nxt)[16] = (q8 & 1) ? ra : rb;
+            tmem_ld_wait16(cur);
+            if (q8 < 7) tmem_ld16_issue(tS + 16 * (q8 + 1), nxt);
+            uint32_t pw[8];
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              const float2 x = __ffma2_rn(make_float2(__uint_as_float(cur[2 * t]), __uint_as_float(cur[2 * t + 1])), sc2, nb2);
+              const float p0 = ex2(x.x), p1 = ex2(x.y);
+              ls = __fadd2_rn(ls, make_float2(p0, p1));
+              pw[t] = pack16<F16>(p0, p1);
+            }
+            tmem_st8(tS + 8 * q8, pw);
+          }
+          ls0 = ls.x;
+          ls1 = ls.y;
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint32_t raw[32], pw[16];
+            tmem_ld32(tS + 32 * q4, raw);
+            float sv[32];
+            masked_scores32<MK, CAUSAL>(c, raw, b, h, i, j0 + 32 * q4, flag, mbits[q4], sv, mask_vec, scratch);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+              const float p0 = ex2(sv[2 * t] - fixed_ref), p1 = ex2(sv[2 * t + 1] - fixed_ref);
+              ls0 += p0;
+              ls1 += p1;
+              pw[t] = pack16<F16>(p0, p1);
+            }
+            tmem_st16(tS + 16 * q4, pw);  // over columns this step or an earlier one has read
+          }
+        }
+        l_run += ls0 + ls1;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[kBarPFull + ti]);
+        continue;
+      }
       // pass 1: row max (raw scores on plain tiles; the scale is positive)
       float mt = -INFINITY;
       if (plain) {

@@ -121,6 +121,10 @@ def test_additive_bf16_mask(cuda_lib):
 @pytest.mark.parametrize("S", [256, 300, 77])
 def test_causal(cuda_lib, S):
     inp = wl.make_custom(2, 2, 128, S, axes=(128,), seed=33 + S, causal=True)
+    # the first rows see one to three keys and their gradients reach 4-6, where
+    # a bf16 ulp leaves no room under the absolute bound: dO at half scale, as
+    # in the other causal cases (test_gpu_gqa.half_do)
+    inp.do = (inp.do.float() * 0.5).to(inp.do.dtype)
     run_case(cuda_lib, inp)
 
 
@@ -260,3 +264,44 @@ def test_bounded_wait_reports_timeout_and_context_survives(cuda_lib):
     assert cuda_lib.st_get_stats()["timeouts"] == before + 1
     cuda_lib.st_check_status()  # the record is cleared
     run_case(cuda_lib, wl.make("tiny_flux"))  # and the context still computes correctly
+
+
+# The forward takes P = exp2(s - bound) with a fixed reference when the mask
+# adds no values, the operands are bf16 and the score bound
+# scale*log2(e)*D*max|w_q|*max|w_k|*1.02 is at most 56 (the normalised operands
+# cannot exceed it), else an online row maximum. With |w| clamped to
+# [0.7, 1.3], scale = 0.2 puts the bound past the limit (63.7) while the scores
+# stay moderate; one pair of q weights at 2.5 puts it just under (52.2), where P
+# spans about 2^-54 .. 2^-40.
+
+def _weights(inp, big=None):
+    inp.wq = inp.wq.clamp(0.7, 1.3)
+    inp.wk = inp.wk.clamp(0.7, 1.3)
+    if big is not None:
+        inp.wq[0:2] = big
+    return inp
+
+
+@pytest.mark.parametrize("mask,causal", [("none", False), ("bool", False), ("none", True)])
+def test_online_maximum_past_the_bound(cuda_lib, mask, causal):
+    kw = dict(mask="bool_random", mask_shape=(1, 1, 1, 260)) if mask == "bool" else {}
+    inp = _weights(wl.make_custom(1, 2, 128, 260, axes=(128,), seed=150, causal=causal, **kw))
+    if causal:
+        inp.do = (inp.do.float() * 0.5).to(inp.do.dtype)  # see test_gpu_gqa.half_do
+    got, ref = gpu_fwd_bwd(cuda_lib, inp, scale=0.2), oracle_fwd_bwd(inp, scale=0.2)
+    compare_all(got, ref, keys=("o", "lse", "dv", "dwq", "dwk"))
+    # dq and dk are proportional to the softmax scale: the absolute bound, set
+    # for scale = 1/sqrt(D), grows with it (0.2 * sqrt(128) = 2.26)
+    for k in ("dq", "dk"):
+        compare(k, got[k], ref[k], atol=2e-2 * 0.2 * 128 ** 0.5)
+
+
+@pytest.mark.parametrize("mask,causal", [("bool", False), ("none", True)])
+def test_fixed_reference_near_its_limit(cuda_lib, mask, causal):
+    kw = dict(mask="bool_random", mask_shape=(2, 1, 1, 300)) if mask == "bool" else {}
+    inp = _weights(wl.make_custom(2, 2, 128, 300, axes=(128,), seed=152, causal=causal, **kw), 2.5)
+    bound = 128 ** -0.5 * np.log2(np.e) * 128 * float(inp.wq.abs().max()) * float(inp.wk.abs().max()) * 1.02
+    assert 50.0 < bound <= 56.0
+    if causal:
+        inp.do = (inp.do.float() * 0.5).to(inp.do.dtype)
+    compare_all(gpu_fwd_bwd(cuda_lib, inp), oracle_fwd_bwd(inp))
