@@ -64,7 +64,8 @@ static_assert(kFwdSmem <= 232448, "forward shared memory exceeds the per-block l
 
 enum {
   kBarQRaw = 0,                       // raw q rows landed (TMA)
-  kBarQFull,                          // Q' ready (prologue)
+  kBarQFull,                          // + query tile (0/1): Q' ready (prologue)
+  kBarQFull1,
   kBarKRaw,                           // + K stage: raw k rows landed (TMA)
   kBarKFull = kBarKRaw + kKStages,    // + K stage: K' ready (prologue)
   kBarKEmpty = kBarKFull + kKStages,  // + K stage: both score MMAs of the tile done
@@ -261,7 +262,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
   }
   if (tid == 0) {
     mbar_init(&bars[kBarQRaw], 1);
-    mbar_init(&bars[kBarQFull], kProlWarps * 32);
+    mbar_init(&bars[kBarQFull + 0], kProlWarps * 32);
+    mbar_init(&bars[kBarQFull + 1], kProlWarps * 32);
     for (int s = 0; s < kKStages; ++s) {
       mbar_init(&bars[kBarKRaw + s], 1);
       mbar_init(&bars[kBarKFull + s], kProlWarps * 32);
@@ -586,9 +588,11 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
           else
             zero_row(tile, p);
         }
+        // each tile is released as soon as it is final: S0 of the first key
+        // tile does not wait for the second query tile
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[kBarQFull + ti]);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars[kBarQFull]);
     }
     // one decision for the prologue warps, which share a named barrier below
     ok = !named_bar_any(kBarIdProl, kProlWarps * 32, !ok);
@@ -715,7 +719,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     } else if (lane_id == 2 && P.save_qp) {
       // the finished Q' tiles go to the workspace for the backward (rows past
       // S_q are clipped by the map); the tiles stay in place for the whole CTA
-      if (wait_bar(&bars[kBarQFull], 0, abort_flag, budget)) {
+      if (wait_bar(&bars[kBarQFull + 0], 0, abort_flag, budget) && wait_bar(&bars[kBarQFull + 1], 0, abort_flag, budget)) {
 #pragma unroll 1
         for (int ti = 0; ti < 2; ++ti) {
           const int row = (qt0 + ti) * kTile;
@@ -735,20 +739,24 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       const uint64_t dK0 = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_u32(sm + kOffV), kHalfBytes, 1024);
       const uint32_t tS0 = tmem, tS1 = tmem + 128, tO0 = tmem + 256, tO1 = tmem + 384;
-      bool ok = wait_bar(&bars[kBarQFull], 0, abort_flag, budget);
       int u = next_tile<MK>(fl, kw, 0);  // walk position (the MMAs need no tile index)
       int n = 0;
       bool issued = false;
-      if (ok && u < kw.L) {
-        ok = wait_bar(&bars[kBarKFull + 0], 0, abort_flag, budget);
+      bool ok = true;
+      if (u < kw.L) {
+        ok = wait_bar(&bars[kBarQFull + 0], 0, abort_flag, budget) &&
+             wait_bar(&bars[kBarKFull + 0], 0, abort_flag, budget);
         if (ok) {
           tc_fence_after();
           issue_s<F16>(tS0, dQ0, dK0);
           mma_commit(&bars[kBarSFull + 0]);
-          issue_s<F16>(tS1, dQ1, dK0);
-          mma_commit(&bars[kBarSFull + 1]);
-          mma_commit(&bars[kBarKEmpty + 0]);
           issued = true;
+          if ((ok = wait_bar(&bars[kBarQFull + 1], 0, abort_flag, budget))) {
+            tc_fence_after();
+            issue_s<F16>(tS1, dQ1, dK0);
+            mma_commit(&bars[kBarSFull + 1]);
+            mma_commit(&bars[kBarKEmpty + 0]);
+          }
         }
       }
       while (ok && u < kw.L) {
