@@ -171,7 +171,8 @@ ST_API size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k
 
 /* Forward.
  *  q, k:   [B, S_q, H, D] / [B, S_kv, H_kv, D], bf16, fp16 or fp32 (q and k
- *          of one dtype).
+ *          of one dtype). D = 128; B, H <= 65535; S_q, S_kv <= 2^30
+ *          (ST_ERR_SHAPE otherwise).
  *  v:      [B, S_kv, H_kv, D], bf16, fp16 or fp32.
  *          Dtype combinations ("Metal Flash Attention", section
  *          "Requirements": FP32 runs natively, FP16/BF16 on low-precision

@@ -47,6 +47,7 @@ __device__ __forceinline__ float table_elem(const void* t, int dtype, int64_t e)
 // the fp32 sincosf so that large ids keep full fp32 accuracy; or, in the table
 // form, entry 2p of the caller's pair-duplicated cos/sin rows.
 __global__ void table_kernel(const __grid_constant__ TableParams p) {
+  grid_dependency_wait();
   if (blockIdx.x == 0 && threadIdx.x < kCtrlWords && p.ctrl) p.ctrl[threadIdx.x] = 0u;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.n_zero; e += (int64_t)gridDim.x * blockDim.x)
     p.zero[e] = 0u;
@@ -78,6 +79,7 @@ __global__ void table_kernel(const __grid_constant__ TableParams p) {
 }
 
 __global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
+  grid_dependency_wait();
   const int kt = blockIdx.x, qt = blockIdx.y;
   const int bm = blockIdx.z / p.Hm, hm = blockIdx.z % p.Hm;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -119,6 +121,7 @@ __global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
 constexpr int kPreRows = 2;
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ PreParams p) {
+  grid_dependency_wait();
   if (blockIdx.x == 0 && threadIdx.x < 2 && p.ctrl) p.ctrl[kCtrlDwDone + threadIdx.x] = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
@@ -195,6 +198,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 constexpr int kPostRows = 1;  // rows per warp and pass, their loads issued together
 
 __global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_constant__ PostParams p) {
+  grid_dependency_wait();
   __shared__ float4 part[kPostWarps][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
@@ -287,6 +291,7 @@ __global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_cons
 // partials. Each block sums up to kDwChunk partials in index order; the last
 // block to finish sums the block results in index order.
 __global__ void __launch_bounds__(128) dw_reduce_kernel(const __grid_constant__ DwParams p) {
+  grid_dependency_wait();
   const int which = blockIdx.y, tid = threadIdx.x;
   const float* part = which ? p.dwk_part : p.dwq_part;
   const int n = which ? p.n_k : p.n_q;
@@ -344,29 +349,25 @@ cudaError_t launch_table(const TableParams& p, cudaStream_t stream) {
   const int threads = 256;
   int blocks = static_cast<int>(std::min<int64_t>((n + threads - 1) / threads, 152 * 16));
   if (blocks < 1) blocks = 1;
-  table_kernel<<<blocks, threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(table_kernel, dim3(blocks), dim3(threads), 0, stream, p);
 }
 
 cudaError_t launch_classify(const ClassifyParams& p, cudaStream_t stream) {
   dim3 grid(p.nKt, p.nQtm, p.Bm * p.Hm);
-  classify_kernel<<<grid, 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(classify_kernel, grid, dim3(128), 0, stream, p);
 }
 
 cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const int64_t warps = (nrows + kPreRows - 1) / kPreRows;
   const int64_t blocks = (warps * 32 + 255) / 256;
-  bwd_pre_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(bwd_pre_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
 }
 
 cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const int64_t blocks = (nrows + kTile - 1) / kTile;
-  dq_post_kernel<<<static_cast<unsigned>(blocks), kPostThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(dq_post_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPostThreads), 0, stream, p);
 }
 
 // One thread per row, with the forward prologues' arithmetic in their order,
@@ -377,6 +378,7 @@ cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
 // y = (n0 cos - n1 sin, n0 sin + n1 cos) with the fp16 (16-bit q) or fp32
 // (fp32 q) table, rounded once to the operand type.
 __global__ void __launch_bounds__(128) qprime_kernel(const __grid_constant__ QPrimeParams p) {
+  grid_dependency_wait();
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const int64_t row = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= nrows) return;
@@ -458,14 +460,12 @@ __global__ void __launch_bounds__(128) qprime_kernel(const __grid_constant__ QPr
 cudaError_t launch_qprime(const QPrimeParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const int64_t blocks = (nrows + 127) / 128;
-  qprime_kernel<<<static_cast<unsigned>(blocks), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(qprime_kernel, dim3(static_cast<unsigned>(blocks)), dim3(128), 0, stream, p);
 }
 
 cudaError_t launch_dw_reduce(const DwParams& p, cudaStream_t stream) {
   dim3 grid(dw_reduce_blocks(p.n_q, p.n_k), 2);
-  dw_reduce_kernel<<<grid, kD, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(dw_reduce_kernel, grid, dim3(kD), 0, stream, p);
 }
 
 }  // namespace st

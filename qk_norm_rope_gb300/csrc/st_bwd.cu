@@ -480,6 +480,7 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
 template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 1)
     bwd_kernel(const __grid_constant__ BwdParams P) {
+  grid_dependency_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   if (smem_u32(sm) & 1023u) {  // the layout has no slack: refuse an unaligned base (uniform over the grid)
@@ -1003,8 +1004,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, cudaStream_t stream) {
   cudaError_t e = opt_in_smem(kern, kBwdSmem, configured);
   if (e != cudaSuccess) return e;
   dim3 grid((p.c.nKt + kCluster - 1) / kCluster * kCluster, p.c.Hkv, p.c.B);  // whole clusters
-  kern<<<grid, kBwdThreads, kBwdSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(kern, grid, dim3(kBwdThreads), kBwdSmem, stream, p);
 }
 
 template <bool QKT, bool F16>

@@ -1,8 +1,10 @@
 // Device-side parameter blocks and row helpers shared by the kernels.
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include "st_ptx.cuh"
 
 namespace st {
@@ -255,6 +257,30 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Kernels of a call are chained with programmatic dependent launch: a kernel
+// may be scheduled while its predecessor on the stream finishes, and waits
+// here, before its first global-memory access, until that predecessor has
+// completed and its writes are visible (a no-op when launched without it).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kern` with the programmatic-stream-serialisation attribute (see
+// grid_dependency_wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                           Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 __device__ __forceinline__ void record_timeout(const Common& c) {

@@ -233,6 +233,7 @@ __device__ __forceinline__ void column_sums(const float (&acc)[4][8], float* red
 
 template <int MK, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) f32_fwd_kernel(const __grid_constant__ F32Params P) {
+  grid_dependency_wait();
   extern __shared__ float smf[];
   float *sQ = smf, *sK = sQ + kTileF, *sV = sK + kTileF, *sP = sV + kTileF;
   const Common& c = P.c;
@@ -326,6 +327,7 @@ __device__ __forceinline__ void p_ds_tile(const F32Params& P, const float* sQ, c
 
 template <int MK, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) f32_bwd_kv_kernel(const __grid_constant__ F32Params P) {
+  grid_dependency_wait();
   extern __shared__ float smf[];
   float *sK = smf, *sV = sK + kTileF, *sQ = sV + kTileF, *sdO = sQ + kTileF, *sP = sdO + kTileF, *sdS = sP + kTileP;
   const Common& c = P.c;
@@ -378,6 +380,7 @@ __global__ void __launch_bounds__(kThreads) f32_bwd_kv_kernel(const __grid_const
 
 template <int MK, bool CAUSAL>
 __global__ void __launch_bounds__(kThreads) f32_bwd_q_kernel(const __grid_constant__ F32Params P) {
+  grid_dependency_wait();
   extern __shared__ float smf[];
   float *sQ = smf, *sdO = sQ + kTileF, *sK = sdO + kTileF, *sV = sK + kTileF, *sdS = sV + kTileF;
   float* sP = sdS;  // P is not kept: only dS feeds dQ'
@@ -425,8 +428,7 @@ cudaError_t launch_f32(K kern, dim3 grid, uint32_t smem, std::atomic<uint64_t>& 
                        cudaStream_t stream) {
   cudaError_t e = opt_in_smem(kern, smem, done);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(kern, grid, dim3(kThreads), smem, stream, p);
 }
 
 template <int MK, bool CAUSAL>

@@ -237,6 +237,7 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
 
 template <int MK, bool CAUSAL, bool QKT, bool F16>
 __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
+  grid_dependency_wait();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   if (smem_u32(sm) & 1023u) {  // the layout has no slack: refuse an unaligned base (uniform over the grid)
@@ -817,8 +818,7 @@ cudaError_t launch_fwd_t(const FwdParams& p, cudaStream_t stream) {
   cudaError_t e = opt_in_smem(kern, kFwdSmem, configured);
   if (e != cudaSuccess) return e;
   dim3 grid((p.c.nQt + 1) / 2, p.c.H, p.c.B);
-  kern<<<grid, kFwdThreads, kFwdSmem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_chained(kern, grid, dim3(kFwdThreads), kFwdSmem, stream, p);
 }
 
 template <bool QKT, bool F16>
