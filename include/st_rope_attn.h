@@ -114,8 +114,10 @@ typedef struct {
  *        st_rope_attn_fwd call on the same workspace pointer with a backward-
  *        sized workspace_bytes, stream-ordered before the backward (its first
  *        bytes have the forward's layout); the backward then skips rebuilding
- *        them. Anything else is undefined results (not a fault). 0: the
- *        backward rebuilds them. */
+ *        them, and relies on the forward having zeroed its dQ accumulator
+ *        there, which it consumes: one reusing backward per forward. Anything
+ *        else is undefined results (not a fault). 0: the backward rebuilds
+ *        them. */
 typedef struct {
   const st_tensor* ids;
   const st_tensor* ids_k;
@@ -204,7 +206,8 @@ ST_API size_t st_rope_attn_workspace_size(const st_tensor* q, const st_tensor* k
  *          (and q, k, v are not all fp32), the forward leaves its Q' rows
  *          ([B, S_q, H, D] in the 16-bit operand type, the bf16 or fp16 values
  *          its attention kernel multiplies) in the backward's part of the
- *          workspace, for a backward with rope->reuse_tables = 1.
+ *          workspace and zeroes the backward's fp32 dQ accumulator there, for
+ *          a backward with rope->reuse_tables = 1.
  *  stream: cudaStream_t. */
 ST_API st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tensor* v, const st_tensor* q_norm_w,
                            const st_tensor* k_norm_w, float eps, const st_rope* rope, const st_tensor* mask,

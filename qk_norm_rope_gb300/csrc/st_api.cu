@@ -373,7 +373,7 @@ st_status plan_call(const st_tensor* q, const st_tensor* k, const st_tensor* v, 
     if (P->f32) P->n_dwk = s.B * s.Hkv * ((s.Skv + kF32Tile - 1) / kF32Tile);  // per fp32 key tile
     P->off_dwk = off;
     off = align_up(off + (size_t)P->n_dwk * kD * sizeof(float), 256);
-    P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kTile - 1) / kTile);
+    P->n_dwq = static_cast<int>(((int64_t)s.B * s.Sq * s.H + kPostBlockRows - 1) / kPostBlockRows);
     if (P->f32) P->n_dwq = s.B * s.H * ((s.Sq + kF32Tile - 1) / kF32Tile);  // per fp32 query tile
     P->off_dwq = off;
     off = align_up(off + (size_t)P->n_dwq * kD * sizeof(float), 256);
@@ -638,7 +638,8 @@ st_status encode_operand_rows_map(uint8_t* base, int B, int S, int H, bool f16, 
 st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k, const st_tensor* v,
                           const st_tensor* q_norm_w, const st_tensor* k_norm_w, float eps, const st_rope* rope,
                           const st_tensor* mask, int causal, float scale, st_tensor* o, const RowTensor& ro,
-                          st_tensor* lse, uint8_t* ws, uint8_t* qp, bool kcache, cudaStream_t stream) {
+                          st_tensor* lse, uint8_t* ws, uint8_t* qp, float* dq_zero, bool kcache,
+                          cudaStream_t stream) {
   st_status st;
   Dev dev;
   if ((st = device_globals(&dev)) != ST_OK) return st;
@@ -673,6 +674,7 @@ st_status enqueue_forward(const Plan& P, const st_tensor* q, const st_tensor* k,
   if (qp) {
     if ((st = encode_operand_rows_map(qp, P.sh.B, P.sh.Sq, P.sh.H, v->dtype == ST_F16, kTile, &fp.tmap_qp)) != ST_OK) return st;
     fp.save_qp = 1;
+    fp.dq_zero = dq_zero;
   }
   kcache = kcache && P.kcache;
   if (kcache) {
@@ -726,14 +728,18 @@ st_status st_rope_attn_fwd(const st_tensor* q, const st_tensor* k, const st_tens
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   // a workspace that can also serve the backward receives the Q' rows, which
   // a backward reusing it reads instead of normalising and rotating q again
+  // and a zeroed dQ' accumulator
   uint8_t* qp = nullptr;
+  float* dq_zero = nullptr;
   if (!P.f32) {
     Plan PB;
-    if (plan_call(q, k, v, mask, causal, rope, 1, &PB) == ST_OK && workspace_bytes >= PB.total)
+    if (plan_call(q, k, v, mask, causal, rope, 1, &PB) == ST_OK && workspace_bytes >= PB.total) {
       qp = static_cast<uint8_t*>(workspace) + PB.off_qp;
+      dq_zero = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + PB.off_dqacc);
+    }
   }
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(workspace), qp, true, stream)) != ST_OK)
+                            static_cast<uint8_t*>(workspace), qp, dq_zero, true, stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;
@@ -835,7 +841,7 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
     pp.dout = d_o->data;
     pp.do_sb = rdo.sb; pp.do_ss = rdo.ss; pp.do_sh = rdo.sh;
     pp.delta = delta;
-    pp.dq_acc = dq_acc;
+    pp.dq_acc = reuse ? nullptr : dq_acc;  // a reused workspace: the forward zeroed it
     pp.ctrl = reinterpret_cast<unsigned*>(ws + P.off_ctrl);
     pp.B = s.B; pp.H = s.H; pp.Sq = s.Sq;
     if ((st = cuda_check(launch_counted(ST_K_BWD_PRE, stream, [&] { return launch_bwd_pre(pp, stream); }), "backward pre launch")) != ST_OK) return st;
@@ -983,7 +989,8 @@ st_status st_rope_attn_fwd_noalloc(const st_tensor* q, const st_tensor* k, const
   if ((st = noalloc_scratch_address(&scratch)) != ST_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   if ((st = enqueue_forward(P, q, k, v, q_norm_w, k_norm_w, eps, rope, mask, causal, scale, o, ro, lse,
-                            static_cast<uint8_t*>(scratch), nullptr, P.total <= ST_NOALLOC_SCRATCH_BYTES, stream)) != ST_OK)
+                            static_cast<uint8_t*>(scratch), nullptr, nullptr, P.total <= ST_NOALLOC_SCRATCH_BYTES,
+                            stream)) != ST_OK)
     return st;
   ++h_fwd_calls;
   if (q->dtype == ST_F32 && !P.f32) ++h_mixed;

@@ -203,11 +203,11 @@ __global__ void __launch_bounds__(kPostThreads) dq_post_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const bool small = nrows < (int64_t(1) << 31);
-  const int64_t row0 = (int64_t)blockIdx.x * kTile;
+  const int64_t row0 = (int64_t)blockIdx.x * kPostBlockRows;
   const float4 w = __ldg(reinterpret_cast<const float4*>(p.wq) + lane);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-  for (int k0 = warp * kPostRows; k0 < kTile; k0 += kPostWarps * kPostRows) {
+  for (int k0 = warp * kPostRows; k0 < kPostBlockRows; k0 += kPostWarps * kPostRows) {
     float4 g[kPostRows], x[kPostRows], cs[kPostRows];
     int64_t yoff[kPostRows];
     bool valid[kPostRows];
@@ -366,7 +366,7 @@ cudaError_t launch_bwd_pre(const PreParams& p, cudaStream_t stream) {
 
 cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
-  const int64_t blocks = (nrows + kTile - 1) / kTile;
+  const int64_t blocks = (nrows + kPostBlockRows - 1) / kPostBlockRows;
   return launch_chained(dq_post_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kPostThreads), 0, stream, p);
 }
 

@@ -73,6 +73,7 @@ struct FwdParams {
   int qk_tma;          // 1: q and k are 16-bit and staged by TMA, normalised in place
   CUtensorMap tmap_qp; // the workspace's Q' rows ([B, Sq, H, D], operand type), 128-row boxes (TMA store)
   int save_qp;         // 1: the CTA stores its Q' tiles there for the backward
+  float* dq_zero;      // the backward's fp32 dQ' accumulator [B, Sq, H, D], zeroed here (or null)
   CUtensorMap tmap_kc; // the workspace's K' tiles ([B, Skv, Hkv, D], operand type), 128-row boxes
   uint32_t* kflags;    // [B, Hkv, nKt]: 1 once K' of the tile is in tmap_kc's buffer (zeroed per call)
   int kcache;          // 1: K' tiles are shared between CTAs through that buffer

@@ -657,6 +657,19 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
       mbar_arrive(&bars[kBarKFull + slot]);
     }
     if (p == 0) raise_pending();
+    // the backward's dQ' accumulator rows of this CTA's queries start at zero
+    // (a backward that reuses this workspace skips its own zeroing pass): one
+    // 512-byte row per warp instruction
+    if (ok && P.dq_zero) {
+      const int pw = p >> 5;
+#pragma unroll 1
+      for (int rr = pw; rr < 2 * kTile; rr += kProlWarps) {
+        const int i = qt0 * kTile + rr;
+        if (i >= c.Sq) break;
+        reinterpret_cast<float4*>(P.dq_zero + (((int64_t)b * c.Sq + i) * c.H + h) * kD)[lane_id] =
+            make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
   } else if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA: raw Q, raw K (lane 0), V (lane 1)
     if (lane_id == 0) {
