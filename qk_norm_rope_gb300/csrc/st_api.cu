@@ -598,7 +598,7 @@ st_status encode_table_map(const float2* tab, int64_t rows, CUtensorMap* map) {
 // 4-D tiled map over the fp32 dQ accumulator [B, S_q, H, D] (contiguous) as
 // (d, h, s, b) for 32-column x 64-row boxes with 128-byte swizzle: the target
 // of the backward kernel's bulk reductions (one box per 32 head dims of a
-// 64-query sub-tile).
+// 64-query half of a query tile).
 st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* map) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) return fail(ST_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -616,8 +616,8 @@ st_status encode_dq_acc_map(float* dq_acc, int B, int Sq, int H, CUtensorMap* ma
 
 // 4-D tiled map over contiguous operand rows [B, S, H, D] of the workspace (the
 // 16-bit operand type) as (d, h, s, b), for 64-column x box_rows boxes with
-// 128-byte swizzle: the Q' rows (the forward stores its tiles, the backward
-// loads sub-tiles) and the forward's shared K' tiles.
+// 128-byte swizzle: the Q' rows (the forward stores its tiles, each backward
+// CTA of a pair loads half of a tile) and the forward's shared K' tiles.
 st_status encode_operand_rows_map(uint8_t* base, int B, int S, int H, bool f16, int box_rows, CUtensorMap* map) {
   st_tensor t;
   memset(&t, 0, sizeof(t));
@@ -787,14 +787,14 @@ st_status st_rope_attn_bwd(const st_tensor* q, const st_tensor* k, const st_tens
   memset(&bp, 0, sizeof(bp));
   if (P.nKt > 0 && !P.f32) {
     if ((st = encode_rows_map(v, &bp.tmap_v, &bp.v_s_first)) != ST_OK) return st;
-    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first, kTile / 2)) != ST_OK)
+    if ((int64_t)s.B * s.Sq * s.H > 0 && (st = encode_rows_map(d_o, &bp.tmap_do, &bp.do_s_first, kTile)) != ST_OK)
       return st;
     bp.qk_tma = q->dtype != ST_F32 ? 1 : 0;
     // raw k rows: the prologue's TMA source (bf16) and the epilogue's (both dtypes)
     if ((st = encode_rows_map(k, &bp.tmap_k, &bp.k_s_first)) != ST_OK) return st;
-    // the Q' rows of the workspace, 32-row boxes (each CTA of a pair loads half a sub-tile)
+    // the Q' rows of the workspace, 64-row boxes (each CTA of a pair loads half a tile)
     if ((int64_t)s.B * s.Sq * s.H > 0 &&
-        (st = encode_operand_rows_map(ws + P.off_qp, s.B, s.Sq, s.H, v->dtype == ST_F16, kTile / 4, &bp.tmap_q)) != ST_OK)
+        (st = encode_operand_rows_map(ws + P.off_qp, s.B, s.Sq, s.H, v->dtype == ST_F16, kTile / 2, &bp.tmap_q)) != ST_OK)
       return st;
     if ((st = encode_table_map(reinterpret_cast<const float2*>(ws + P.off_tab_k), (int64_t)P.ids_k.Bt * s.Skv,
                                &bp.tmap_tab_k)) != ST_OK)

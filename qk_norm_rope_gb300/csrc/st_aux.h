@@ -11,7 +11,7 @@ namespace st {
 // (always the first launch of a call).
 enum { kCtrlAnyFalse = 0, kCtrlClassifyDone = 1, kCtrlDwDone = 2 /* +0 q, +1 k */, kCtrlWords = 8 };
 constexpr int kDwChunk = 32;  // weight-gradient partials summed per block
-constexpr int kPostBlockRows = 128;  // rows of one dq_post block (and of one dW_q partial)
+constexpr int kPostBlockRows = 64;   // rows of one dq_post block (and of one dW_q partial)
 
 inline int dw_reduce_blocks(int n_q, int n_k) {
   const int a = (n_q + kDwChunk - 1) / kDwChunk, b = (n_k + kDwChunk - 1) / kDwChunk;

@@ -2,43 +2,46 @@
 // in clusters of two CTAs over adjacent key tiles (kt0 = 2p, kt0 + 1) that
 // walk the same query tiles in lockstep, for every query head that shares the
 // K/V head (grouped K/V heads: dK' and dV accumulate over the whole group in
-// TMEM, so dk and dv leave the epilogue final). Query tiles are processed as two 64-query
-// sub-tiles; per sub-tile, with Q' = RoPE(RMSNorm(q)) and K' the same for k
-// (bf16, 128B-swizzled operand tiles):
+// TMEM, so dk and dv leave the epilogue final). Per query tile of 128 rows,
+// with Q' = RoPE(RMSNorm(q)) and K' the same for k (16-bit, 128B-swizzled
+// operand tiles):
 //   S^T = K' Q'^T, dP^T = V dO^T                      (tensor core, TMEM)
 //   P^T = exp2(S^T scale log2e - LSE log2e)            (compute warps)
 //   dS^T = P^T (dP^T - Delta)
 //   dV += P^T dO, dK' += dS^T Q', dQ'^T = K'^T dS^T    (tensor core, TMEM)
-// dQ'^T (this CTA's 128 keys) is added into a global fp32 accumulator by TMA
-// bulk reduces. Q' comes from the workspace, where the forward kernel left
-// the tiles it normalised and rotated (a standalone row kernel fills it when
-// the forward did not run on this workspace); each CTA of a cluster loads half
-// of a sub-tile's rows by TMA multicast into both CTAs' stage.
+// Every MMA is M = 128, N = 128: a tcgen05 MMA with N = 64 takes as long as
+// one with N = 128 (measured on GB300: 64 cycles per K-step either way), so
+// whole 128-query tiles keep the tensor core at its full rate. dQ'^T (this
+// CTA's 128 keys) is added into a global fp32 accumulator by TMA bulk
+// reduces. Q' comes from the workspace, where the forward kernel left the
+// tiles it normalised and rotated (a standalone row kernel fills it when the
+// forward did not run on this workspace); each CTA of a cluster loads half of
+// a tile's rows by TMA multicast into both CTAs' stage.
 //
 // Warp roles (608 threads; 96 registers per thread):
 //   warps 0-7    compute: warp w owns TMEM lanes 32*(w%4).. (key rows) and
-//                queries [32*(w/4), +32) of each sub-tile; P^T goes to TMEM
-//                (bf16, inside the warp's own S^T columns), dS^T to shared
-//                memory
-//   warps 8-11   dQ drain: TMEM lanes = head dims; a sub-tile's dQ'^T is read
-//                out at once and its columns released; each warp then stages
-//                its 32 head dims in its own shared-memory box and adds the box
-//                into global memory with a TMA bulk reduce of its own
+//                queries [64*(w/4), +64) of each tile, in two 32-query chunks;
+//                P^T goes to TMEM (16-bit, inside the chunk's own S^T
+//                columns), dS^T to shared memory
+//   warps 8-11   dQ drain: TMEM lanes = head dims; a tile's dQ'^T is read out
+//                in two 64-query halves and its columns released; each warp
+//                stages its 32 head dims as a [64 query][32] box in the tile's
+//                (then idle) dO stage and adds it into global memory with a TMA
+//                bulk reduce of its own
 //   warps 12-15  prologue: K' once (normalised and rotated in place); then
-//                each sub-tile's LSE and Delta
+//                each tile's LSE and Delta
 //   warp 16      TMEM allocation + tcgen05.mma issue (one thread)
-//   warp 17      TMA: raw K, V once; this CTA's 32 Q' rows per sub-tile,
-//                multicast to both CTAs (4-stage ring, a stage reused once both
+//   warp 17      TMA: raw K, V once; this CTA's 64 Q' rows per tile,
+//                multicast to both CTAs (2-stage ring, a stage reused once both
 //                CTAs' MMAs released it)
-//   warp 18      TMA: dO sub-tiles (2-stage ring), so that the Q' ring never
-//                waits behind a dO stage
-// TMEM (512 columns): two sub-tile buffers of 128 columns, dV, dK'. A buffer
-// holds S^T (later P^T, later dQ'^T) in one 64-column half and dP^T in the
-// other; the halves swap roles on each use of the buffer.
-// MMA order for sub-tile n (buffer n % 2): [compute done] dV, dK', dQ'^T (over
-// P^T) | S^T(n+2) (over dP^T(n)) | [dQ'^T drained] dP^T(n+2), so the compute
-// warps work on one buffer while the tensor core finishes the other, and the
-// drain overlaps the next scores.
+//   warp 18      TMA: dO tiles (2-stage ring)
+// TMEM (512 columns): X = S^T (later P^T), Y = dP^T (later dQ'^T), dV, dK',
+// 128 columns each.
+// MMA order for tile n: [P^T(n) in TMEM] dV, S^T(n+1) over P^T(n) (the dV
+// MMAs read it first: same issuing thread, in order) | [dS^T(n) in shared
+// memory] dQ'^T(n) over dP^T(n), dK' | [dQ'^T(n) drained] dP^T(n+1). The
+// compute warps build P^T(n+1) while the tensor core finishes tile n, and keep
+// it in registers for dS^T(n+1), since S^T(n+2) overwrites it in TMEM.
 #include "st_common.cuh"
 #include "st_kernels.h"
 #include "st_prologue.cuh"
@@ -59,14 +62,13 @@ constexpr int kWarpMma = 16, kWarpTma = 17, kWarpTmaDO = 18;
 constexpr int kBwdWarps = 19;
 constexpr int kBwdThreads = kBwdWarps * 32;
 constexpr int kProlThreads = kProlWarps * 32;
-constexpr int kSub = 64;                                   // queries per sub-tile
-constexpr int kQStages = 4;                                // Q' ring, in sub-tiles
-constexpr int kDOStages = 2;                               // dO ring, in sub-tiles
-constexpr uint32_t kSubBytes = kSub * kD * 2;              // 16 KB bf16 sub-tile (two 8 KB column halves)
-constexpr uint32_t kSubHalf = kSubBytes / 2;
-constexpr int kPeerRows = kSub / kCluster;                 // Q' rows produced per CTA per sub-tile
+constexpr int kQStages = 2;                                // Q' ring, in tiles
+constexpr int kDOStages = 2;                               // dO ring, in tiles
+constexpr uint32_t kQTileBytes = kTile * kD * 2;           // 32 KB 16-bit tile (two 16 KB column halves)
+constexpr int kPeerRows = kTile / kCluster;                // Q' rows produced per CTA per tile
 constexpr uint32_t kPeerRowsBytes = kPeerRows * 128;       // those rows in one column half
-constexpr uint32_t kRBoxBytes = kSub * 32 * 4;             // one [64 queries][32 head dims] fp32 box
+constexpr int kDrainRows = 64;                             // queries per drain box (the dQ map's box)
+constexpr uint32_t kRBoxBytes = kDrainRows * 32 * 4;       // one [64 queries][32 head dims] fp32 box
 // named barrier of the epilogue: the compute, drain and prologue warps (16)
 constexpr int kBarIdEpi = 4, kEpiThreads = (kComputeWarps + kDrainWarps + kProlWarps) * 32;
 static_assert(kComputeWarps + kDrainWarps + kProlWarps == 16 && kWarpProl0 + kProlWarps == kWarpMma,
@@ -76,18 +78,19 @@ constexpr uint32_t kBoxBytes = 128 * 128;                  // a [128 rows][128 b
 // shared memory layout (offsets from the 1024-byte aligned dynamic base)
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kTileBytes;
-constexpr uint32_t kOffQ = 2 * kTileBytes;                      // kQStages sub-tiles
-constexpr uint32_t kOffDO = kOffQ + kQStages * kSubBytes;       // kDOStages sub-tiles
-constexpr uint32_t kOffDS = kOffDO + kDOStages * kSubBytes;     // 2 buffers of [128 keys][64 queries] bf16
-constexpr uint32_t kOffR = kOffDS + 2 * kSubBytes;              // dQ'^T staging: a box per drain warp
-constexpr uint32_t kOffStat = kOffR + kDrainWarps * kRBoxBytes; // [stage][LSE*log2e | Delta][64] fp32
-constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kSub * 4;
+constexpr uint32_t kOffQ = 2 * kTileBytes;                      // kQStages tiles
+constexpr uint32_t kOffDO = kOffQ + kQStages * kQTileBytes;     // kDOStages tiles
+constexpr uint32_t kOffDS = kOffDO + kDOStages * kQTileBytes;   // [128 keys][128 queries] 16-bit
+constexpr uint32_t kOffStat = kOffDS + kQTileBytes;             // [stage][LSE*log2e | Delta][128] fp32
+constexpr uint32_t kOffBar = kOffStat + kQStages * 2 * kTile * 4;
 constexpr uint32_t kBarBytes = 512;
 constexpr uint32_t kOffW = kOffBar + kBarBytes;                 // k norm weights for the epilogue, fp32
 constexpr uint32_t kBwdSmem = kOffW + kD * 4;                   // the base must be 1024-byte aligned
 static_assert(kBwdSmem <= 232448, "backward shared memory exceeds the per-block limit");
-static_assert(kProlThreads >= kSub, "one prologue thread per stat row");
-static_assert(kQStages * 2 * kSub >= 4 * kTile, "the epilogue's row-sum exchange fits in the stat area");
+static_assert(kProlThreads >= kTile, "one prologue thread per stat row");
+static_assert(kDrainWarps * kRBoxBytes <= kQTileBytes, "the drain boxes fit in a dO stage");
+static_assert(kQStages * 2 * kTile >= 4 * kTile, "the epilogue's row-sum exchange fits in the stat area");
+static_assert(kDOStages >= 2, "the epilogue stages dV in the first dO stage and a row-sum exchange in the second");
 
 enum {
   kBarKRaw = 0,                          // raw k rows landed (TMA)
@@ -97,25 +100,27 @@ enum {
   kBarQFull = kBarQRaw + kQStages,       // + stage: the stage's LSE/Delta written (prologue threads)
   kBarQFree = kBarQFull + kQStages,      // + stage: both CTAs' MMAs done with the stage
   kBarDOFull = kBarQFree + kQStages,     // + stage: dO rows landed
-  kBarDOFree = kBarDOFull + kDOStages,   // + stage: MMAs done with the dO rows
-  kBarSFull = kBarDOFree + kDOStages,    // + buffer: S^T in TMEM
-  kBarDPFull = kBarSFull + 2,            // + buffer: dP^T in TMEM
-  kBarCDone = kBarDPFull + 2,            // + buffer: P^T in TMEM, dS^T in shared memory (256 arrivals)
-  kBarDQ = kBarCDone + 2,                // + buffer: dQ'^T in TMEM (and every earlier MMA done)
-  kBarBFree = kBarDQ + 2,                // + buffer: dQ'^T read out (128 arrivals)
-  kBarFinal = kBarBFree + 2,             // abort path: all issued MMAs done
+  kBarDOFree = kBarDOFull + kDOStages,   // + stage: MMAs done with the dO rows, drain boxes read
+  kBarSFull = kBarDOFree + kDOStages,    // S^T in TMEM
+  kBarDPFull,                            // dP^T in TMEM
+  kBarPDone,                             // P^T in TMEM (256 arrivals)
+  kBarCDone,                             // dS^T in shared memory, dP^T read (256 arrivals)
+  kBarDQ,                                // dQ'^T in TMEM (and every earlier MMA done)
+  kBarBFree,                             // dQ'^T read out (128 arrivals)
+  kBarFinal,                             // abort path: all issued MMAs done
   kBarEpi,                               // epilogue: raw k rows and (cos, sin) rows staged
   kNumBars
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");  // + TMEM slot, abort flag, sink, K tile mode
 
 __device__ __forceinline__ uint32_t kofs128(int kk) { return (kk >> 2) * kHalfBytes + (kk & 3) * 32; }  // K-major, 128 rows
-__device__ __forceinline__ uint32_t kofs64(int kk) { return (kk >> 2) * kSubHalf + (kk & 3) * 32; }     // K-major, 64 rows
 __device__ __forceinline__ uint32_t mofs(int kk) { return kk * 2048; }                                   // MN-major, 16 rows
-// TMEM column of sub-tile n's S^T half and of its dP^T half (the halves of
-// buffer n % 2 swap roles on every use of the buffer)
-__device__ __forceinline__ uint32_t s_col(int n) { return 128 * (n & 1) + 64 * ((n >> 1) & 1); }
-__device__ __forceinline__ uint32_t dp_col(int n) { return s_col(n) ^ 64u; }
+// TMEM columns: X holds S^T and then P^T, Y dP^T and then dQ'^T
+constexpr uint32_t kColX = 0, kColY = 128, kColDV = 256, kColDK = 384;
+// P^T of queries 32 c .. 32 c + 31 (chunk c of the tile) is packed, two
+// 16-bit values per column, into the first 16 of the chunk's 32 S^T columns:
+// the A operand of K-step kk (queries 16 kk ..) starts at this column of X.
+__device__ __forceinline__ uint32_t p_col(int kk) { return 32 * (kk >> 1) + 8 * (kk & 1); }
 
 // Tile class of (query tile qt, key tile kt) for this CTA's own key tile; a
 // CTA past the last key tile sees nothing.
@@ -341,10 +346,10 @@ __device__ __noinline__ float dk_quarter_rows(const BwdParams& P, const uint8_t*
   return colsum;
 }
 
-// P^T of this thread's key against 32 queries iq0 .. iq0 + 31 on a sub-tile
+// P^T of this thread's key against 32 queries iq0 .. iq0 + 31 of a chunk
 // that needs masking (a bool tile with False elements, an additive mask
 // broadcast over the queries, the causal diagonal, rows past S_q). Out of
-// line: sub-tiles without masking never run it, and inlined it would spread
+// line: chunks without masking never run it, and inlined it would spread
 // the compute warps' hot loop over more instruction-cache lines.
 // It reads the warp's 32 S^T columns at TMEM address tS and writes P^T (16-bit
 // pairs) over the first 16 of them itself, so that no array crosses the call.
@@ -370,7 +375,7 @@ __device__ __noinline__ void p_masked(const Common& c, uint32_t tS, float key_te
 }
 
 // ---- epilogue of the sixteen compute, drain and prologue warps, once their
-// walks are over (n sub-tiles; `ok` is false after an abort). Warp w holds key
+// walks are over (n query tiles; `ok` is false after an abort). Warp w holds key
 // rows 32 (w % 4) .. (its TMEM lanes) and head dims [32 cq, 32 cq + 32)
 // (cq = w / 4) of dV and dK'. Once every MMA has completed, the K tile, the Q'
 // ring and the dO ring are free: the raw k rows and the tile's fp32 (cos, sin)
@@ -378,8 +383,8 @@ __device__ __noinline__ void p_masked(const Common& c, uint32_t tS, float key_te
 // and stored by TMA; then dk (inverse rotation + RMSNorm backward) is laid out
 // in the dS buffers and stored by TMA (16-bit k; fp32 rows are stored
 // directly), and each warp writes its partial sums of the k norm-weight
-// gradient. The row sums are exchanged through the stat area and the drain's
-// staging boxes (free once the drain is done).
+// gradient. The row sums are exchanged through the stat area and the second
+// dO stage.
 // Out of line, with every index derived again from the thread and block
 // coordinates, so that nothing it needs stays live in registers through the
 // main loops: with its values held across the loop (inlined, or called with
@@ -403,13 +408,12 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
   const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
   // the compute warps learn here that every MMA is done (the drain warps
   // waited for the last dQ'^T themselves; the barrier below orders the rest)
-  if (warp < kComputeWarps && ok && n > 0)
-    ok = wait_bar_warp(&bars[kBarDQ + ((n - 1) & 1)], ((n - 1) >> 1) & 1, abort_flag, budget);
+  if (warp < kComputeWarps && ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ], (n - 1) & 1, abort_flag, budget);
   // one decision for the sixteen warps (they share named barriers below)
   if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
     tc_fence_after();
     float* ex_ss = reinterpret_cast<float*>(sm + kOffStat);  // the stats are consumed (2 KB)
-    float* ex_xg = reinterpret_cast<float*>(sm + kOffR);     // the drain is done with its boxes
+    float* ex_xg = reinterpret_cast<float*>(sm + kOffDO + kQTileBytes);  // the second dO stage
     float* sWk = reinterpret_cast<float*>(sm + kOffW);       // k norm weights
     const int ty = P.k_s_first ? kt * kTile : hk, tz = P.k_s_first ? hk : kt * kTile;
     if (tid == 0) {
@@ -513,15 +517,14 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     }
     for (int s = 0; s < kDOStages; ++s) {
       mbar_init(&bars[kBarDOFull + s], 1);
-      mbar_init(&bars[kBarDOFree + s], 1);
+      mbar_init(&bars[kBarDOFree + s], 1 + kDrainWarps);  // the dV MMAs, and the drain's box reads
     }
-    for (int u = 0; u < 2; ++u) {
-      mbar_init(&bars[kBarSFull + u], 1);
-      mbar_init(&bars[kBarDPFull + u], 1);
-      mbar_init(&bars[kBarCDone + u], kComputeWarps * 32);
-      mbar_init(&bars[kBarDQ + u], 1);
-      mbar_init(&bars[kBarBFree + u], kDrainWarps * 32);
-    }
+    mbar_init(&bars[kBarSFull], 1);
+    mbar_init(&bars[kBarDPFull], 1);
+    mbar_init(&bars[kBarPDone], kComputeWarps * 32);
+    mbar_init(&bars[kBarCDone], kComputeWarps * 32);
+    mbar_init(&bars[kBarDQ], 1);
+    mbar_init(&bars[kBarBFree], kDrainWarps * 32);
     mbar_init(&bars[kBarFinal], 1);
     mbar_init(&bars[kBarEpi], 1);
     *abort_flag = 0;
@@ -554,7 +557,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 
   if (warp < kComputeWarps) {
     // ------------------------------------------------------------ compute
-    const int qd = warp & 3, hq = warp >> 2;  // TMEM lane quarter, query half of a sub-tile
+    const int qd = warp & 3, hq = warp >> 2;  // TMEM lane quarter, query half of a tile
     const int r = qd * 32 + lane_id;          // key row in the tile / TMEM lane
     const int j = kt * kTile + r;
     const bool key_ok = j < c.Skv;
@@ -574,10 +577,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     int key_h = W.h0;
     float key_term = key_term_of(key_h);
     const float sc = c.scale_log2;
-    const int q0 = 32 * hq;  // this warp's first query of a sub-tile
+    const int qh0 = 64 * hq;  // this warp's first query of a tile
     bool ok = true;
     int n = 0;
-    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m);
+         m = next_pos<MK>(c, b, W, W.step(m), kt0), ++n) {
       const int qt = W.qt(m), h = W.head(m);
       if (h != key_h) {
         key_h = h;
@@ -585,30 +589,34 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       }
       const uint8_t flag = own_flag<MK>(c, b, h, qt, kt);
       useful += (flag != kTileAllFalse && (!CAUSAL || qt >= kt)) ? 1 : 0;
-      for (int s = 0; s < 2; ++s, ++n) {
-        const int bf = n & 1, sq = n % kQStages;
-        const int iq0 = qt * kTile + kSub * s;  // first query of the sub-tile
-        if (!(ok = wait_bar_warp(&bars[kBarSFull + bf], (n >> 1) & 1, abort_flag, budget))) break;
-        // the prologue's LSE/Delta for this stage become visible through this wait
-        if (!(ok = wait_bar_warp(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget))) break;
-        tc_fence_after();
-        const float* st_lse = stat + sq * 2 * kSub;
-        const float* st_dl = st_lse + kSub;
-        const uint32_t tS = tmem + lanebits + s_col(n), tdP = tmem + lanebits + dp_col(n);
-        // plain sub-tiles: every query row valid, no mask values, no causal diagonal
-        const bool plain = flag != kTileAllFalse && iq0 + kSub <= c.Sq &&
+      const int sq = n % kQStages;
+      if (!(ok = wait_bar_warp(&bars[kBarSFull], n & 1, abort_flag, budget))) break;
+      // the prologue's LSE/Delta for this stage become visible through this wait
+      if (!(ok = wait_bar_warp(&bars[kBarQFull + sq], (n / kQStages) & 1, abort_flag, budget))) break;
+      tc_fence_after();
+      const float* st_lse = stat + sq * 2 * kTile;
+      const float* st_dl = st_lse + kTile;
+      // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), 16-bit into TMEM, per 32-query chunk;
+      // kept in registers for dS^T as well, since S^T(n+1) overwrites X as soon
+      // as the dV MMAs have read it
+      uint32_t pwa[32];
+#pragma unroll
+      for (int ch = 0; ch < 2; ++ch) {
+        const int q0 = qh0 + 32 * ch;  // the chunk's first query in the tile
+        const int iq0 = qt * kTile + q0;
+        const uint32_t tS = tmem + lanebits + kColX + q0;
+        // plain chunks: every query row valid, no mask values, no causal diagonal
+        const bool plain = flag != kTileAllFalse && iq0 + 32 <= c.Sq &&
                            (MK == kMaskNone || mask_bcast_q || (MK == kMaskBool && flag == kTileAllTrue)) &&
                            (!CAUSAL || iq0 >= kt * kTile + kTile - 1);
-        // ---- P^T = exp2(S^T * scale*log2e - LSE*log2e), bf16 into TMEM
         uint32_t pw[16];
         if (!plain && !ELEM) {
-          // masked sub-tile, out of line; P^T comes back from TMEM for dS^T
-          p_masked<MK, CAUSAL, F16>(c, tS + q0, key_term, b, h, iq0 + q0, j, key_ok, flag, mask_bcast_q, st_lse + q0);
-          tmem_ld16_issue(tS + q0, pw);
+          p_masked<MK, CAUSAL, F16>(c, tS, key_term, b, h, iq0, j, key_ok, flag, mask_bcast_q, st_lse + q0);
+          tmem_ld16_issue(tS, pw);
           tmem_ld_wait16(pw);
         } else {
           uint32_t sv[32];
-          tmem_ld32(tS + q0, sv);
+          tmem_ld32(tS, sv);
           if (plain) {
             const float2 sc2 = make_float2(sc, sc), kt2 = make_float2(key_term, key_term);
 #pragma unroll
@@ -630,7 +638,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
 #pragma unroll
               for (int t = 0; t < 16; ++t) {
                 raw[t] = 0u;
-                const int iq = iq0 + q0 + 16 * hh + t;
+                const int iq = iq0 + 16 * hh + t;
                 if (elem_mask && iq < c.Sq) {
                   const int64_t off = b * c.m_sb + h * c.m_sh + (int64_t)iq * c.m_sq + j;
                   if constexpr (MK == kMaskBool) raw[t] = __ldg(static_cast<const uint8_t*>(c.mask) + off) ? 0u : 1u;
@@ -650,24 +658,40 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
                 for (int e = 0; e < 2; ++e) {
                   const int tl = 2 * t2 + e, t = 16 * hh + tl;
                   const float mterm = (MK == kMaskBool) ? (raw[tl] ? -INFINITY : 0.f) : __uint_as_float(raw[tl]) * kLog2e;
-                  const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mterm, iq0 + q0 + t, j, flag);
+                  const float s2 = score2_term<CAUSAL>(c, __uint_as_float(sv[t]), key_term, mterm, iq0 + t, j, flag);
                   p2[e] = ex2(s2 - st_lse[q0 + t]);
                 }
                 pw[8 * hh + t2] = pack16<F16>(p2[0], p2[1]);
               }
             }
           }
-          tmem_st16(tS + q0, pw);  // the first 16 of the warp's own 32 S^T columns
+          tmem_st16(tS, pw);  // the first 16 of the chunk's 32 S^T columns
         }
-        // ---- dS^T = P^T (dP^T - Delta), bf16 into shared memory (row r, K-major)
-        if (!(ok = wait_bar_warp(&bars[kBarDPFull + bf], (n >> 1) & 1, abort_flag, budget))) break;
-        tc_fence_after();
-        {
-          uint32_t dpv[32];
-          tmem_ld32(tdP + q0, dpv);
-          uint8_t* dsb = sm + kOffDS + bf * kSubBytes;
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {  // 8 queries = one 16-byte chunk of the dS^T row
+        for (int i = 0; i < 16; ++i) pwa[16 * ch + i] = pw[i];
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarPDone]);
+      // ---- dS^T = P^T (dP^T - Delta), 16-bit into shared memory (row r, K-major)
+      // (dS^T(n-1) is consumed: its MMAs completed before dP^T(n) did)
+      if (!(ok = wait_bar_warp(&bars[kBarDPFull], n & 1, abort_flag, budget))) break;
+      tc_fence_after();
+      {
+        // 16 queries at a time; each TMEM load is issued before the previous
+        // block is processed
+        uint32_t da[16], db[16];
+        uint8_t* dsb = sm + kOffDS + hq * kHalfBytes;
+        tmem_ld16_issue(tmem + lanebits + kColY + qh0, da);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t(&cur)[16] = (k & 1) ? db : da;
+          uint32_t(&nxt)[16] = (k & 1) ? da : db;
+          tmem_ld_wait16(cur);
+          if (k < 3) tmem_ld16_issue(tmem + lanebits + kColY + qh0 + 16 * (k + 1), nxt);
+          const int q0 = qh0 + 16 * k;
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {  // 8 queries = one 16-byte chunk of the dS^T row
             const float4 d0 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u);
             const float4 d1 = *reinterpret_cast<const float4*>(st_dl + q0 + 8 * u + 4);
             const float2 ndl[4] = {make_float2(-d0.x, -d0.y), make_float2(-d0.z, -d0.w), make_float2(-d1.x, -d1.y),
@@ -675,65 +699,75 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
             uint32_t out[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const uint32_t pp = pw[4 * u + e];
-              const float2 dp = make_float2(__uint_as_float(dpv[8 * u + 2 * e]), __uint_as_float(dpv[8 * u + 2 * e + 1]));
+              const uint32_t pp = pwa[8 * k + 4 * u + e];
+              const float2 dp = make_float2(__uint_as_float(cur[8 * u + 2 * e]), __uint_as_float(cur[8 * u + 2 * e + 1]));
               const float2 ds = __fmul2_rn(make_float2(lo16<F16>(pp), hi16<F16>(pp)), __fadd2_rn(dp, ndl[e]));
               out[e] = pack16<F16>(ds.x, ds.y);
             }
-            *reinterpret_cast<uint4*>(dsb + sw128_off(r, 4 * hq + u)) = make_uint4(out[0], out[1], out[2], out[3]);
+            *reinterpret_cast<uint4*>(dsb + sw128_off(r, 2 * k + u)) = make_uint4(out[0], out[1], out[2], out[3]);
           }
         }
-        fence_proxy_async_smem();
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars[kBarCDone + bf]);
       }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars[kBarCDone]);
     }
     bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp < kWarpDrain0 + kDrainWarps) {
     // ------------------------------------------------------------ dQ drain
-    // A sub-tile's dQ'^T (128 head dims x 64 queries, fp32) leaves TMEM at once
-    // (64 registers per thread) and its columns are released. Warp qd stages
-    // head dims [32 qd, +32) as a [64 query][32] box and lane 0 adds it into
-    // the global accumulator (TMA bulk reduce); the box is rewritten one
-    // sub-tile later, once that reduce has read it. The warps never wait for
-    // one another.
+    // A tile's dQ'^T (128 head dims x 128 queries, fp32) leaves TMEM in two
+    // 64-query halves (64 registers per thread); the columns are released once
+    // both are read. Warp qd stages head dims [32 qd, +32) of a half as a
+    // [64 query][32] box in the tile's dO stage (idle once the dV MMAs are
+    // done; the dO loads refill it only after kBarDOFree has the drain's
+    // arrivals as well) and lane 0 adds the box into the global accumulator
+    // (TMA bulk reduce); the second half reuses the box once the first reduce
+    // has read it. Nothing on the tensor core's path waits for these copies,
+    // and the warps never wait for one another.
     const int qd = warp & 3;
     const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
-    uint8_t* box = sm + kOffR + qd * kRBoxBytes;
     const float scale = c.scale;
     const bool leader = lane_id == 0;
     const uint32_t chunk = static_cast<uint32_t>(lane_id) >> 2, word = (lane_id & 3) * 4;
     int n = 0;
     bool ok = true;
-    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+    for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); ok && W.more(m);
+         m = next_pos<MK>(c, b, W, W.step(m), kt0), ++n) {
       const int qt = W.qt(m), h = W.head(m);
-      for (int s = 0; s < 2; ++s, ++n) {
-        const int bf = n & 1;
-        if (!(ok = wait_bar_warp(&bars[kBarDQ + bf], (n >> 1) & 1, abort_flag, budget))) break;
-        tc_fence_after();
+      const int sd = n % kDOStages;
+      uint8_t* box = sm + kOffDO + sd * kQTileBytes + qd * kRBoxBytes;
+      if (!(ok = wait_bar_warp(&bars[kBarDQ], n & 1, abort_flag, budget))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
         uint32_t v0[32], v1[32];
-        tmem_ld32(tmem + lanebits + s_col(n), v0);
-        tmem_ld32(tmem + lanebits + s_col(n) + 32, v1);
-        tc_fence_before();
-        mbar_arrive(&bars[kBarBFree + bf]);
-        if (leader) bulk_wait_read_all();  // the previous reduce has read the box
-        __syncwarp();
+        tmem_ld32(tmem + lanebits + kColY + kDrainRows * half, v0);
+        tmem_ld32(tmem + lanebits + kColY + kDrainRows * half + 32, v1);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bars[kBarBFree]);
+          if (leader) bulk_wait_read_all();  // the first half's reduce has read the box
+          __syncwarp();
+        }
 #pragma unroll
-        for (int q = 0; q < kSub; ++q) {  // row q of the box: 32 consecutive head dims, 128B-swizzled
+        for (int q = 0; q < kDrainRows; ++q) {  // row q of the box: 32 consecutive head dims, 128B-swizzled
           const uint32_t v = q < 32 ? v0[q] : v1[q - 32];
           *reinterpret_cast<float*>(box + q * 128 + ((chunk ^ (q & 7)) << 4) + word) = __uint_as_float(v) * scale;
         }
         fence_proxy_async_smem();
         __syncwarp();
-        const int row = qt * kTile + kSub * s;
-        if (leader && row < c.Sq) {  // a sub-tile wholly past S_q adds nothing
+        const int row = qt * kTile + kDrainRows * half;
+        if (leader && row < c.Sq) {  // a half wholly past S_q adds nothing
           tma_reduce_add_4d(&P.tmap_dq, box, 32 * qd, h, row, b);
           bulk_commit_group();
         }
       }
+      if (leader) {
+        bulk_wait_read_all();  // the second half's reduce has read the box
+        mbar_arrive(&bars[kBarDOFree + sd]);
+      }
     }
-    if (leader) bulk_wait_all();  // the boxes are free for the epilogue's exchange
+    if (leader) bulk_wait_all();  // the reduces are complete before the epilogue reuses the buffer
     bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp < kWarpProl0 + kProlWarps) {
     // ------------------------------------------------------------ Q' / K' prologue
@@ -772,40 +806,35 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     // and the loop below has named barriers of its own
     ok = !named_bar_any(3, kProlThreads, *abort_flag != 0);
     // Q' rows arrive by TMA from the workspace (the forward's normalised,
-    // rotated q rows); these threads stage each sub-tile's LSE (base 2; +inf
-    // for rows without keys or past S_q, so that P = 0) and Delta, loaded one
-    // sub-tile ahead. A stage's values are rewritten once both CTAs' MMAs have
-    // released the stage (the compute warps have read them by then).
+    // rotated q rows); these threads stage each tile's LSE (base 2; +inf for
+    // rows without keys or past S_q, so that P = 0) and Delta, loaded one tile
+    // ahead. A stage's values are rewritten once both CTAs' MMAs have released
+    // the stage (the compute warps have read them by then).
     float lse_c = -INFINITY, dl_c = 0.f;
     auto load_stats = [&](int iq0, int h) {
       lse_c = -INFINITY;
       dl_c = 0.f;
-      if (p < kSub && iq0 + p < c.Sq) {
+      if (iq0 + p < c.Sq) {
         const int64_t ri = ((int64_t)b * c.H + h) * c.Sq + iq0 + p;
         lse_c = ldg_nc_f32(P.lse + ri);
         dl_c = ldg_nc_f32(P.delta + ri);
       }
     };
     WPos m = next_pos<MK>(c, b, W, W.start(), kt0);
-    int s = 0;
     if (W.more(m)) load_stats(W.qt(m) * kTile, W.head(m));
     int n = 0;
     for (; ok && W.more(m); ++n) {
-      const WPos m_next = s == 0 ? m : next_pos<MK>(c, b, W, W.step(m), kt0);
-      const int s_next = s ^ 1;
+      const WPos m_next = next_pos<MK>(c, b, W, W.step(m), kt0);
       const int sq = n % kQStages;
       const float l2 = (lse_c == -INFINITY) ? INFINITY : lse_c * kLog2e, dl = dl_c;
       if (n >= kQStages &&
           !(ok = wait_bar_cluster_warp(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)))
         break;
-      if (p < kSub) {
-        stat[sq * 2 * kSub + p] = l2;
-        stat[sq * 2 * kSub + kSub + p] = dl;
-      }
-      if (W.more(m_next)) load_stats(W.qt(m_next) * kTile + kSub * s_next, W.head(m_next));
+      stat[sq * 2 * kTile + p] = l2;
+      stat[sq * 2 * kTile + kTile + p] = dl;
+      if (W.more(m_next)) load_stats(W.qt(m_next) * kTile, W.head(m_next));
       mbar_arrive(&bars[kBarQFull + sq]);
       m = m_next;
-      s = s_next;
     }
     bwd_epilogue<QKT, F16>(P, sm, n, ok);
   } else if (warp == kWarpTma) {
@@ -836,25 +865,19 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         mbar_arrive(&bars[kBarVFull]);  // V is zeroed by the prologue, before K' is declared ready
       }
       int n = 0, q_issued = 0;
-      bool stop = false;
-      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0), ++n) {
         const int qt = W.qt(m), h = W.head(m);
-        for (int s = 0; s < 2; ++s, ++n) {
-          // this CTA's 32 Q' rows of the sub-tile, into both CTAs' stage; the
-          // stage holds the peer's 32 rows as well once kSubBytes have landed
-          const int sq = n % kQStages;
-          if (n >= kQStages &&
-              !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget)) {
-            stop = true;
-            break;
-          }
-          uint8_t* qrows = sm + kOffQ + sq * kSubBytes + kPeerRowsBytes * crank;
-          const int row = qt * kTile + kSub * s + kPeerRows * static_cast<int>(crank);
-          mbar_arrive_expect_tx(&bars[kBarQRaw + sq], kSubBytes);
-          tma_load_4d_mc(qrows, &P.tmap_q, &bars[kBarQRaw + sq], 0, h, row, b, 0x3);
-          tma_load_4d_mc(qrows + kSubHalf, &P.tmap_q, &bars[kBarQRaw + sq], 64, h, row, b, 0x3);
-          ++q_issued;
-        }
+        // this CTA's 64 Q' rows of the tile, into both CTAs' stage; the stage
+        // holds the peer's 64 rows as well once kQTileBytes have landed
+        const int sq = n % kQStages;
+        if (n >= kQStages && !wait_bar_cluster(&bars[kBarQFree + sq], ((n / kQStages) - 1) & 1, abort_flag, budget))
+          break;
+        uint8_t* qrows = sm + kOffQ + sq * kQTileBytes + kPeerRowsBytes * crank;
+        const int row = qt * kTile + kPeerRows * static_cast<int>(crank);
+        mbar_arrive_expect_tx(&bars[kBarQRaw + sq], kQTileBytes);
+        tma_load_4d_mc(qrows, &P.tmap_q, &bars[kBarQRaw + sq], 0, h, row, b, 0x3);
+        tma_load_4d_mc(qrows + kHalfBytes, &P.tmap_q, &bars[kBarQRaw + sq], 64, h, row, b, 0x3);
+        ++q_issued;
       }
       // drain: every issued load lands before the CTA exits (these waits do not
       // give up on abort; each is bounded)
@@ -869,23 +892,17 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     // ------------------------------------------------------------ TMA: dO
     if (lane_id == 0) {
       int n = 0, do_issued = 0;
-      bool stop = false;
-      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); !stop && W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) {
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0), ++n) {
         const int qt = W.qt(m), h = W.head(m);
-        for (int s = 0; s < 2; ++s, ++n) {
-          const int sd = n % kDOStages;
-          if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) {
-            stop = true;
-            break;
-          }
-          const int row = qt * kTile + kSub * s;
-          const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
-          uint8_t* dst = sm + kOffDO + sd * kSubBytes;
-          mbar_arrive_expect_tx(&bars[kBarDOFull + sd], kSubBytes);
-          tma_load_4d(dst, &P.tmap_do, &bars[kBarDOFull + sd], 0, y, z, b);
-          tma_load_4d(dst + kSubHalf, &P.tmap_do, &bars[kBarDOFull + sd], 64, y, z, b);
-          ++do_issued;
-        }
+        const int sd = n % kDOStages;
+        if (n >= kDOStages && !wait_bar(&bars[kBarDOFree + sd], ((n / kDOStages) - 1) & 1, abort_flag, budget)) break;
+        const int row = qt * kTile;
+        const int y = P.do_s_first ? row : h, z = P.do_s_first ? h : row;
+        uint8_t* dst = sm + kOffDO + sd * kQTileBytes;
+        mbar_arrive_expect_tx(&bars[kBarDOFull + sd], kQTileBytes);
+        tma_load_4d(dst, &P.tmap_do, &bars[kBarDOFull + sd], 0, y, z, b);
+        tma_load_4d(dst + kHalfBytes, &P.tmap_do, &bars[kBarDOFull + sd], 64, y, z, b);
+        ++do_issued;
       }
       for (int x = max(0, do_issued - kDOStages); x < do_issued; ++x)
         mbar_wait(&bars[kBarDOFull + x % kDOStages], (x / kDOStages) & 1, budget);
@@ -893,79 +910,80 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     if (lane_id == 0) {
-      constexpr uint32_t idesc_sdp = idesc16(F16, 128, kSub, 0, 0);  // S^T, dP^T: N = 64 queries
-      constexpr uint32_t idesc_kv = idesc16(F16, 128, 128, 0, 1);    // dV, dK': N = 128 head dims
-      constexpr uint32_t idesc_q = idesc16(F16, 128, kSub, 1, 1);    // dQ'^T = K'^T dS^T
+      constexpr uint32_t idesc_sdp = idesc16(F16, 128, 128, 0, 0);  // S^T, dP^T: N = 128 queries
+      constexpr uint32_t idesc_kv = idesc16(F16, 128, 128, 0, 1);   // dV, dK': N = 128 head dims
+      constexpr uint32_t idesc_q = idesc16(F16, 128, 128, 1, 1);    // dQ'^T = K'^T dS^T
       const uint64_t dKk = sdesc_sw128(smem_u32(sm + kOffK), 16, 1024);
       const uint64_t dKm = sdesc_sw128(smem_u32(sm + kOffK), kHalfBytes, 1024);
       const uint64_t dVk = sdesc_sw128(smem_u32(sm + kOffV), 16, 1024);
       const uint64_t dQk0 = sdesc_sw128(smem_u32(sm + kOffQ), 16, 1024);
-      const uint64_t dQm0 = sdesc_sw128(smem_u32(sm + kOffQ), kSubHalf, 1024);
+      const uint64_t dQm0 = sdesc_sw128(smem_u32(sm + kOffQ), kHalfBytes, 1024);
       const uint64_t dOk0 = sdesc_sw128(smem_u32(sm + kOffDO), 16, 1024);
-      const uint64_t dOm0 = sdesc_sw128(smem_u32(sm + kOffDO), kSubHalf, 1024);
-      const uint64_t dSk0 = sdesc_sw128(smem_u32(sm + kOffDS), 16, 1024);
-      const uint64_t dSm0 = sdesc_sw128(smem_u32(sm + kOffDS), kSubHalf, 1024);
-      const uint32_t tdV = tmem + 256, tdK = tmem + 384;
-      int nsub = 0;  // sub-tiles in the walk
-      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) nsub += 2;
-      auto issue_s = [&](int n) -> bool {  // S^T(n) into its half of buffer n % 2
+      const uint64_t dOm0 = sdesc_sw128(smem_u32(sm + kOffDO), kHalfBytes, 1024);
+      const uint64_t dSk = sdesc_sw128(smem_u32(sm + kOffDS), 16, 1024);
+      const uint64_t dSm = sdesc_sw128(smem_u32(sm + kOffDS), kHalfBytes, 1024);
+      const uint32_t tX = tmem + kColX, tY = tmem + kColY, tdV = tmem + kColDV, tdK = tmem + kColDK;
+      int ntiles = 0;  // query tiles in the walk
+      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) ++ntiles;
+      auto issue_s = [&](int n) -> bool {  // S^T(n) into X
         const int sq = n % kQStages;
         if (!wait_bar(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
         tc_fence_after();
-        const uint64_t dQk = sdesc_add(dQk0, sq * kSubBytes);
+        const uint64_t dQk = sdesc_add(dQk0, sq * kQTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + s_col(n), sdesc_add(dKk, kofs128(kk)), sdesc_add(dQk, kofs64(kk)), idesc_sdp, kk > 0);
-        mma_commit(&bars[kBarSFull + (n & 1)]);
+          mma_ss(tX, sdesc_add(dKk, kofs128(kk)), sdesc_add(dQk, kofs128(kk)), idesc_sdp, kk > 0);
+        mma_commit(&bars[kBarSFull]);
         return true;
       };
-      auto issue_dp = [&](int n) -> bool {  // dP^T(n) into the other half
+      auto issue_dp = [&](int n) -> bool {  // dP^T(n) into Y
         const int sd = n % kDOStages;
         if (!wait_bar(&bars[kBarDOFull + sd], (n / kDOStages) & 1, abort_flag, budget)) return false;
         tc_fence_after();
-        const uint64_t dOk = sdesc_add(dOk0, sd * kSubBytes);
+        const uint64_t dOk = sdesc_add(dOk0, sd * kQTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tmem + dp_col(n), sdesc_add(dVk, kofs128(kk)), sdesc_add(dOk, kofs64(kk)), idesc_sdp, kk > 0);
-        mma_commit(&bars[kBarDPFull + (n & 1)]);
+          mma_ss(tY, sdesc_add(dVk, kofs128(kk)), sdesc_add(dOk, kofs128(kk)), idesc_sdp, kk > 0);
+        mma_commit(&bars[kBarDPFull]);
         return true;
       };
       bool ok = wait_bar(&bars[kBarKFull], 0, abort_flag, budget) && wait_bar(&bars[kBarVFull], 0, abort_flag, budget);
       bool issued = false;
-      for (int n = 0; ok && n < nsub && n < 2; ++n) {
+      if (ok && ntiles > 0) {
         issued = true;
-        ok = issue_s(n) && issue_dp(n);
+        ok = issue_s(0) && issue_dp(0);
       }
-      for (int n = 0; ok && n < nsub; ++n) {
-        const int bf = n & 1, sq = n % kQStages, sd = n % kDOStages;
-        if (!(ok = wait_bar(&bars[kBarCDone + bf], (n >> 1) & 1, abort_flag, budget))) break;
+      for (int n = 0; ok && n < ntiles; ++n) {
+        const int sq = n % kQStages, sd = n % kDOStages;
+        // dV += P^T dO: P^T (16-bit) in X, read from TMEM
+        if (!(ok = wait_bar(&bars[kBarPDone], n & 1, abort_flag, budget))) break;
         tc_fence_after();
-        // dV += P^T dO: P^T (bf16) in TMEM, queries 0-31 packed in columns 0-15 of
-        // the S^T half, queries 32-63 in columns 32-47
-        const uint32_t tP = tmem + s_col(n);
-        const uint64_t dOm = sdesc_add(dOm0, sd * kSubBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tdV, tP + 8 * kk + (kk >= 2 ? 16 : 0), sdesc_add(dOm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
-        mma_commit(&bars[kBarDOFree + sd]);
-        // dK' += dS^T Q'
-        const uint64_t dQm = sdesc_add(dQm0, sq * kSubBytes), dSk = sdesc_add(dSk0, bf * kSubBytes);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tdK, sdesc_add(dSk, kk * 32), sdesc_add(dQm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
-        mma_commit_mc(&bars[kBarQFree + sq], 0x3);  // the Q' stage is released in both CTAs' view
-        // dQ'^T = K'^T dS^T over P^T (the MMAs above read it first: same issuing thread, in order)
-        const uint64_t dSm = sdesc_add(dSm0, bf * kSubBytes);
+        const uint64_t dOm = sdesc_add(dOm0, sd * kQTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tP, sdesc_add(dKm, mofs(kk)), sdesc_add(dSm, mofs(kk)), idesc_q, kk > 0);
-        mma_commit(&bars[kBarDQ + bf]);
-        if (n + 2 < nsub) {
-          // S^T(n+2) over dP^T(n) (read by the compute warps before they signalled),
-          // dP^T(n+2) over dQ'^T(n) once the drain has read it
-          if (!(ok = issue_s(n + 2))) break;
-          if (!(ok = wait_bar(&bars[kBarBFree + bf], (n >> 1) & 1, abort_flag, budget))) break;
-          ok = issue_dp(n + 2);
+          mma_ts(tdV, tX + p_col(kk), sdesc_add(dOm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
+        mma_commit(&bars[kBarDOFree + sd]);
+        // S^T(n+1) over P^T(n) (the dV MMAs above read it first: same issuing
+        // thread, in order), so that the compute warps find it when they are
+        // done with dS^T(n)
+        if (n + 1 < ntiles && !(ok = issue_s(n + 1))) break;
+        if (!(ok = wait_bar(&bars[kBarCDone], n & 1, abort_flag, budget))) break;
+        tc_fence_after();
+        // dQ'^T = K'^T dS^T over dP^T (read by the compute warps before they
+        // signalled); first, so that the drain starts early
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tY, sdesc_add(dKm, mofs(kk)), sdesc_add(dSm, mofs(kk)), idesc_q, kk > 0);
+        mma_commit(&bars[kBarDQ]);
+        // dK' += dS^T Q'
+        const uint64_t dQm = sdesc_add(dQm0, sq * kQTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tdK, sdesc_add(dSk, kofs128(kk)), sdesc_add(dQm, mofs(kk)), idesc_kv, (n > 0 || kk > 0));
+        mma_commit_mc(&bars[kBarQFree + sq], 0x3);  // the Q' stage is released in both CTAs' view
+        // dP^T(n+1) over dQ'^T(n) once the drain has read it
+        if (n + 1 < ntiles) {
+          if (!(ok = wait_bar(&bars[kBarBFree], n & 1, abort_flag, budget))) break;
+          ok = issue_dp(n + 1);
         }
       }
       if (issued && !ok) {

@@ -164,6 +164,10 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 // Wait until every committed bulk group of this thread has finished reading
 // its shared-memory source.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Same, except that the most recently committed group may still be reading.
+__device__ __forceinline__ void bulk_wait_read_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 // Wait until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Orders this thread's global-memory accesses of the generic proxy with those
