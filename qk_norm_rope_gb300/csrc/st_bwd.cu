@@ -107,7 +107,7 @@ enum {
   kBarCDone,                             // dS^T in shared memory, dP^T read (256 arrivals)
   kBarDQ,                                // dQ'^T in TMEM (and every earlier MMA done)
   kBarBFree,                             // dQ'^T read out (128 arrivals)
-  kBarFinal,                             // abort path: all issued MMAs done
+  kBarFinal,                             // every issued MMA done (end of the walk, or abort)
   kBarEpi,                               // epilogue: raw k rows and (cos, sin) rows staged
   kNumBars
 };
@@ -406,9 +406,9 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
   const int j = kt * kTile + r;
   const bool key_ok = j < c.Skv;
   const uint32_t lanebits = static_cast<uint32_t>(qd * 32) << 16;
-  // the compute warps learn here that every MMA is done (the drain warps
-  // waited for the last dQ'^T themselves; the barrier below orders the rest)
-  if (warp < kComputeWarps && ok && n > 0) ok = wait_bar_warp(&bars[kBarDQ], (n - 1) & 1, abort_flag, budget);
+  // the compute warps learn here that every MMA is done (the MMA thread's last
+  // commit; the barrier below orders the rest)
+  if (warp < kComputeWarps && ok && n > 0) ok = wait_bar_warp(&bars[kBarFinal], 0, abort_flag, budget);
   // one decision for the sixteen warps (they share named barriers below)
   if (!named_bar_any(kBarIdEpi, kEpiThreads, !ok) && !phantom) {
     tc_fence_after();
@@ -923,8 +923,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       const uint64_t dSk = sdesc_sw128(smem_u32(sm + kOffDS), 16, 1024);
       const uint64_t dSm = sdesc_sw128(smem_u32(sm + kOffDS), kHalfBytes, 1024);
       const uint32_t tX = tmem + kColX, tY = tmem + kColY, tdV = tmem + kColDV, tdK = tmem + kColDK;
-      int ntiles = 0;  // query tiles in the walk
-      for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) ++ntiles;
+      int ntiles = W.len * W.group;  // query tiles in the walk (bool masks skip the tiles both key tiles mask out)
+      if constexpr (MK == kMaskBool) {
+        ntiles = 0;
+        for (WPos m = next_pos<MK>(c, b, W, W.start(), kt0); W.more(m); m = next_pos<MK>(c, b, W, W.step(m), kt0)) ++ntiles;
+      }
       auto issue_s = [&](int n) -> bool {  // S^T(n) into X
         const int sq = n % kQStages;
         if (!wait_bar(&bars[kBarQRaw + sq], (n / kQStages) & 1, abort_flag, budget)) return false;
@@ -986,15 +989,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
           ok = issue_dp(n + 1);
         }
       }
-      if (issued && !ok) {
-        // abort: let every issued MMA finish before TMEM is released
+      if (issued) {
+        // every issued MMA done: the epilogue reads dV and dK' (on abort: before TMEM is released)
         mma_commit(&bars[kBarFinal]);
-        mbar_wait(&bars[kBarFinal], 0, budget);
+        if (!ok) mbar_wait(&bars[kBarFinal], 0, budget);
       }
     }
   }
 
   // ---- tile counters
+  // the lanes of the single-thread roles wait for their lane 0 here, at a warp
+  // barrier, rather than at the block barrier below
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (!*abort_flag) {

@@ -86,8 +86,8 @@ struct FwdParams {
 struct BwdParams {
   Common c;
   CUtensorMap tmap_v;   // V rows, as in FwdParams
-  CUtensorMap tmap_do;  // dO rows, 64-row boxes
-  CUtensorMap tmap_q;   // Q' rows of the workspace ([B, Sq, H, D], operand type), 32-row boxes
+  CUtensorMap tmap_do;  // dO rows, 128-row boxes
+  CUtensorMap tmap_q;   // Q' rows of the workspace ([B, Sq, H, D], operand type), 64-row boxes
   CUtensorMap tmap_k;   // raw k rows, 128-row boxes (16-bit: 64 columns; fp32: 32 columns, epilogue only)
   CUtensorMap tmap_tab_k;  // the fp32 (cos, sin) table of the keys as [Bt_k * Skv, 128] floats, 32 x 128 boxes
   CUtensorMap tmap_dv;     // dv rows, 128-row boxes (TMA store of the epilogue)

@@ -813,6 +813,9 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     }
   }
 
+  // the lanes of the single-thread roles wait for their lane 0 here, at a warp
+  // barrier, rather than at the block barrier below
+  __syncwarp();
   if (*abort_flag && tid == 0) record_timeout(c);
   tc_fence_before();
   __syncthreads();
