@@ -114,7 +114,7 @@ __global__ void classify_kernel(const __grid_constant__ ClassifyParams p) {
   }
 }
 
-// Four (b, i, h) rows per warp and pass, their loads issued together; lane l
+// kPreRows (b, i, h) rows per warp, their loads issued together; lane l
 // owns head dims 4l..4l+3 of each row. Block 0 also clears the weight-gradient
 // reduction counters (the table kernel, which clears them otherwise, may be
 // skipped by a backward that reuses the forward's tables).
