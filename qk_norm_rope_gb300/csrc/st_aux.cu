@@ -127,17 +127,21 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Pr
   const int64_t nrows = (int64_t)p.B * p.Sq * p.H;
   const bool small = nrows < (int64_t(1) << 31);
   const int64_t row0 = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kPreRows;
+  // lane u < kPreRows splits row row0 + u into (b, i, h) once; the warp reads
+  // it by shuffles (the divisions cost more than the row's loads otherwise)
+  RowIdx mine = {0, 0, 0};
+  if (lane < kPreRows && row0 + lane < nrows) mine = row_idx(row0 + lane, p.Sq, p.H, small);
   float o[kPreRows][4], g[kPreRows][4];
 #pragma unroll
   for (int u = 0; u < kPreRows; ++u) {
     const int64_t row = row0 + u;
+    const int b = __shfl_sync(0xffffffffu, mine.b, u), i = __shfl_sync(0xffffffffu, mine.i, u),
+              h = __shfl_sync(0xffffffffu, mine.h, u);
     if (row >= nrows) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[u][e] = g[u][e] = 0.f;
       continue;
     }
-    const RowIdx x = row_idx(row, p.Sq, p.H, small);
-    const int b = x.b, i = x.i, h = x.h;
     const int64_t oo = b * p.o_sb + (int64_t)i * p.o_ss + h * p.o_sh + 4 * lane;
     const int64_t go = b * p.do_sb + (int64_t)i * p.do_ss + h * p.do_sh + 4 * lane;
     if (p.o_dt == kDtF32) {
@@ -173,11 +177,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __grid_constant__ Pr
 #pragma unroll
     for (int u = 1; u < kPreRows; ++u)
       if (lane == u) a = acc[u];
-    const int64_t row = row0 + lane;
-    if (row < nrows) {
-      const RowIdx x = row_idx(row, p.Sq, p.H, small);
-      p.delta[((int64_t)x.b * p.H + x.h) * p.Sq + x.i] = a;
-    }
+    if (row0 + lane < nrows) p.delta[((int64_t)mine.b * p.H + mine.h) * p.Sq + mine.i] = a;
   }
 }
 
