@@ -287,26 +287,22 @@ __device__ __noinline__ float dk_quarter_rows(const BwdParams& P, const uint8_t*
       rsqrtf((((ex_ss[r] + ex_ss[kTile + r]) + ex_ss[2 * kTile + r]) + ex_ss[3 * kTile + r]) * (1.0f / kD) + c.eps);
   const float sc = c.scale;
   const float4* w4 = reinterpret_cast<const float4*>(sWk + 32 * cq);
-  float xg = 0.f, colsum = 0.f;
-#pragma unroll 1
-  for (int pass = 0; pass < 2; ++pass) {
-    if (pass == 1) {  // x . g' over the whole row
-      ex_xg[cq * kTile + r] = xg;
-      named_bar(kBarIdEpi, kEpiThreads);
-      xg = ((ex_xg[r] + ex_xg[kTile + r]) + ex_xg[2 * kTile + r]) + ex_xg[3 * kTile + r];
-    }
-    const float c3 = rr * rr * rr * xg * (1.0f / kD);
-    uint32_t v[32];
+  // g' = w R^T (scale dK') of the quarter, kept for dk; u gathers dy x r for dW_k
+  float gw[32], u[32];
+  float xg = 0.f;
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {  // 16 dims per TMEM load
+    uint32_t v[16];
     if (have) {
-      tmem_ld32(tacc, v);
+      tmem_ld16_issue(tacc + 16 * h2, v);
+      tmem_ld_wait16(v);
     } else {
 #pragma unroll
-      for (int t = 0; t < 32; ++t) v[t] = 0u;
+      for (int t = 0; t < 16; ++t) v[t] = 0u;
     }
-    float u[32];
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-      const int d0 = 8 * c8;  // dims d0 .. d0 + 7 of the quarter: pairs d0/2 .. d0/2 + 3
+    for (int c8 = 0; c8 < 2; ++c8) {
+      const int d0 = 16 * h2 + 8 * c8;  // dims d0 .. d0 + 7 of the quarter: pairs d0/2 .. d0/2 + 3
       float x8[8];
       load_x8(d0, x8);
       const float4 t0 = tab_chunk(d0 >> 2), t1 = tab_chunk((d0 >> 2) + 1);
@@ -315,24 +311,33 @@ __device__ __noinline__ float dk_quarter_rows(const BwdParams& P, const uint8_t*
       const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int t = d0 + 2 * e;
-        const float g0 = __uint_as_float(v[t]) * sc, g1 = __uint_as_float(v[t + 1]) * sc;
+        const int t = d0 + 2 * e, vi = 8 * c8 + 2 * e;
+        const float g0 = __uint_as_float(v[vi]) * sc, g1 = __uint_as_float(v[vi + 1]) * sc;
         const float cc = cs[2 * e], sn = cs[2 * e + 1];
         const float dy0 = fmaf(g0, cc, g1 * sn), dy1 = fmaf(g1, cc, -g0 * sn);
-        const float gw0 = wv[2 * e] * dy0, gw1 = wv[2 * e + 1] * dy1;
-        if (pass == 0) {
-          xg = fmaf(x8[2 * e], gw0, fmaf(x8[2 * e + 1], gw1, xg));
-          u[t] = key_ok ? dy0 * x8[2 * e] * rr : 0.f;
-          u[t + 1] = key_ok ? dy1 * x8[2 * e + 1] * rr : 0.f;
-        } else {
-          u[t] = fmaf(rr, gw0, -c3 * x8[2 * e]);
-          u[t + 1] = fmaf(rr, gw1, -c3 * x8[2 * e + 1]);
-        }
+        gw[t] = wv[2 * e] * dy0;
+        gw[t + 1] = wv[2 * e + 1] * dy1;
+        xg = fmaf(x8[2 * e], gw[t], fmaf(x8[2 * e + 1], gw[t + 1], xg));
+        u[t] = key_ok ? dy0 * x8[2 * e] * rr : 0.f;
+        u[t + 1] = key_ok ? dy1 * x8[2 * e + 1] * rr : 0.f;
       }
     }
-    if (pass == 0) {
-      colsum = warp_reduce_scatter32(u, lane);
-    } else if (QKT) {
+  }
+  const float colsum = warp_reduce_scatter32(u, lane);
+  // x . g' over the whole row
+  ex_xg[cq * kTile + r] = xg;
+  named_bar(kBarIdEpi, kEpiThreads);
+  xg = ((ex_xg[r] + ex_xg[kTile + r]) + ex_xg[2 * kTile + r]) + ex_xg[3 * kTile + r];
+  const float c3 = rr * rr * rr * xg * (1.0f / kD);
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {  // dk = r g' - (r^3 / D) x (x . g')
+    float x8[8];
+    load_x8(8 * c8, x8);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) u[8 * c8 + e] = fmaf(rr, gw[8 * c8 + e], -c3 * x8[e]);
+  }
+  {
+    if constexpr (QKT) {
       // 16-bit dk: chunks 4 (cq % 2) .. + 3 of the row's half cq / 2 in the staging tile
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4)
