@@ -374,7 +374,8 @@ cudaError_t launch_dq_post(const PostParams& p, cudaStream_t stream) {
 // so that the rows equal the ones a forward leaves in the workspace:
 // r = 1/sqrt(mean x^2 + eps) (16-bit q: the sum of squares of each 64-dim half
 // with separate even/odd accumulators, as the two lanes of a row do; fp32 q:
-// even/odd accumulators over the whole row), n = x w r,
+// the in-order sums of the four 32-dim quarters added as ((s0 + s1) + (s2 +
+// s3)), as the four lanes of a row do), n = x w r,
 // y = (n0 cos - n1 sin, n0 sin + n1 cos) with the fp16 (16-bit q) or fp32
 // (fp32 q) table, rounded once to the operand type.
 __global__ void __launch_bounds__(128) qprime_kernel(const __grid_constant__ QPrimeParams p) {
@@ -427,16 +428,21 @@ __global__ void __launch_bounds__(128) qprime_kernel(const __grid_constant__ QPr
     }
   } else {
     const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.q.p) + off);
-    float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll 4
-    for (int c = 0; c < kD / 4; ++c) {
-      const float4 v = __ldg(src + c);
-      ss0 = fmaf(v.x, v.x, ss0);
-      ss1 = fmaf(v.y, v.y, ss1);
-      ss0 = fmaf(v.z, v.z, ss0);
-      ss1 = fmaf(v.w, v.w, ss1);
+    float sq[4];  // sums of squares of the four 32-dim quarters, each in order
+#pragma unroll
+    for (int k4 = 0; k4 < 4; ++k4) {
+      float s4 = 0.f;
+#pragma unroll
+      for (int c = 8 * k4; c < 8 * k4 + 8; ++c) {
+        const float4 v = __ldg(src + c);
+        s4 = fmaf(v.x, v.x, s4);
+        s4 = fmaf(v.y, v.y, s4);
+        s4 = fmaf(v.z, v.z, s4);
+        s4 = fmaf(v.w, v.w, s4);
+      }
+      sq[k4] = s4;
     }
-    const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + p.eps);
+    const float r = rsqrtf(((sq[0] + sq[1]) + (sq[2] + sq[3])) * (1.0f / kD) + p.eps);
     const float4* t4 = reinterpret_cast<const float4*>(p.tab + trow);
 #pragma unroll 1
     for (int c = 0; c < kD / 8; ++c) {

@@ -789,16 +789,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
       // from global memory below
       ok = wait_bar(&bars[kBarKRaw], 0, abort_flag, budget);
       const bool cached = *reinterpret_cast<volatile uint32_t*>(scratch + 1) != 0u;
-      for (int row = p; ok && !cached && row < kTile; row += kProlThreads) {
-        const int jj = kt * kTile + row;
-        if constexpr (QKT) {
+      if constexpr (QKT) {
+        for (int row = p; ok && !cached && row < kTile; row += kProlThreads) {
+          const int jj = kt * kTile + row;
           if (jj < c.Skv)  // rows past S_kv stay TMA zeros
             rope_norm_inplace<F16>(sm + kOffK, row, c.wk, c.eps, c.tab16_k + b * c.tab_k_sb + (int64_t)jj * kPairs);
-        } else if (jj < c.Skv) {
-          rope_norm_global<F16>(c.k.p, b * c.k.sb + (int64_t)jj * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
-                           c.tab_k + b * c.tab_k_sb + (int64_t)jj * kPairs, sm + kOffK, row);
-        } else {
-          zero_row(sm + kOffK, row);
+        }
+      } else if (__all_sync(0xffffffffu, ok) && !cached) {
+        // fp32 rows from global memory, four lanes per row, as the forward
+        // builds them (every lane of the warp in every pass)
+#pragma unroll 1
+        for (int pass = 0; pass < kTile * 4 / kProlThreads; ++pass) {
+          const int row = pass * (kProlThreads / 4) + (p >> 2), jj = kt * kTile + row;
+          const bool valid = jj < c.Skv;
+          const int jv = valid ? jj : 0;
+          rope_norm_global_quad<F16>(c.k.p, b * c.k.sb + (int64_t)jv * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
+                                     c.tab_k + b * c.tab_k_sb + (int64_t)jv * kPairs, sm + kOffK, row, p & 3, valid,
+                                     kHalfBytes);
         }
       }
     }

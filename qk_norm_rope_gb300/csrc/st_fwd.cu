@@ -11,7 +11,7 @@
 //               kKStages-deep ring; bf16 rows arrive by TMA in the operand
 //               layout and are normalised and rotated in place, their (cos,
 //               sin) rows being fetched while the TMA is in flight (fp32 rows
-//               are read from global memory, one thread per row)
+//               are read from global memory, four lanes per row)
 //   warp 16     TMEM allocation + tcgen05.mma issue (one thread)
 //   warp 17     TMA: lane 0 raw Q and K rows, lane 1 V tiles (separate rings:
 //               a K stage is released once both score MMAs of its tile are
@@ -581,13 +581,18 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             hp.prefetch2(t16, hh);
           }
           hp.finish(tile, prow, hh, sW, c.eps, i < c.Sq);
-        } else if (p < kTile) {
-          const int i = (qt0 + ti) * kTile + p;
-          if (i < c.Sq)
-            rope_norm_global<F16>(c.q.p, b * c.q.sb + (int64_t)i * c.q.ss + h * c.q.sh, c.q.dt, c.wq, c.eps,
-                             c.tab_q + b * c.tab_q_sb + (int64_t)i * kPairs, tile, p);
-          else
-            zero_row(tile, p);
+        } else {
+          // fp32 rows from global memory, four lanes per row (every prologue
+          // thread in every pass: the row's sum of squares is a shuffle)
+#pragma unroll 1
+          for (int pass = 0; pass < kTile * 4 / (kProlWarps * 32); ++pass) {
+            const int row = pass * (kProlWarps * 8) + (p >> 2), i = (qt0 + ti) * kTile + row;
+            const bool valid = i < c.Sq;
+            const int iv = valid ? i : 0;
+            rope_norm_global_quad<F16>(c.q.p, b * c.q.sb + (int64_t)iv * c.q.ss + h * c.q.sh, c.q.dt, c.wq, c.eps,
+                                       c.tab_q + b * c.tab_q_sb + (int64_t)iv * kPairs, tile, row, p & 3, valid,
+                                       kHalfBytes);
+          }
         }
         // each tile is released as soon as it is final: S0 of the first key
         // tile does not wait for the second query tile
@@ -631,13 +636,16 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
             hp.prefetch2(t16, hh);
           }
           hp.finish(tile, prow, hh, sW + kD, c.eps, j < c.Skv);
-        } else if (p < kTile) {
-          const int j = kt * kTile + p;
-          if (j < c.Skv)
-            rope_norm_global<F16>(c.k.p, b * c.k.sb + (int64_t)j * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
-                             c.tab_k + b * c.tab_k_sb + (int64_t)j * kPairs, tile, p);
-          else
-            zero_row(tile, p);
+        } else {
+#pragma unroll 1
+          for (int pass = 0; pass < kTile * 4 / (kProlWarps * 32); ++pass) {
+            const int row = pass * (kProlWarps * 8) + (p >> 2), j = kt * kTile + row;
+            const bool valid = j < c.Skv;
+            const int jv = valid ? j : 0;
+            rope_norm_global_quad<F16>(c.k.p, b * c.k.sb + (int64_t)jv * c.k.ss + hk * c.k.sh, c.k.dt, c.wk, c.eps,
+                                       c.tab_k + b * c.tab_k_sb + (int64_t)jv * kPairs, tile, row, p & 3, valid,
+                                       kHalfBytes);
+          }
         }
         fence_proxy_async_smem();
       }

@@ -242,53 +242,13 @@ struct HalfRowPrologue {
   }
 };
 
-// Thread-per-row prologue reading the raw row (bf16 or fp32) from global
-// memory; used when q/k are fp32 (no in-place TMA staging) and for rows that
-// a TMA load does not cover. The raw row is read twice (sum of squares, then
-// transform), the second time from L1.
-template <bool F16>
-__device__ __forceinline__ void rope_norm_global(const void* base, int64_t off, int dt,
-                                                 const float* __restrict__ w, float eps,
-                                                 const float2* __restrict__ tab, uint8_t* tile, int row,
-                                                 uint32_t half = kHalfBytes) {
-  float ss0 = 0.f, ss1 = 0.f;
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {
-    float x[8];
-    load_chunk8(base, off, dt, c, x);
-#pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      ss0 = fmaf(x[e], x[e], ss0);
-      ss1 = fmaf(x[e + 1], x[e + 1], ss1);
-    }
-  }
-  const float r = rsqrtf((ss0 + ss1) * (1.0f / kD) + eps);
-  const float4* t4 = reinterpret_cast<const float4*>(tab);
-  const float4* w4 = reinterpret_cast<const float4*>(w);
-#pragma unroll
-  for (int c = 0; c < kD / 8; ++c) {
-    float x[8];
-    load_chunk8(base, off, dt, c, x);
-    uint32_t packed[4];
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const float4 cs = __ldg(t4 + 2 * c + hh);
-      const float4 ww = __ldg(w4 + 2 * c + hh);
-      const float n0 = x[4 * hh] * ww.x * r, n1 = x[4 * hh + 1] * ww.y * r;
-      const float n2 = x[4 * hh + 2] * ww.z * r, n3 = x[4 * hh + 3] * ww.w * r;
-      packed[2 * hh] = pack16<F16>(n0 * cs.x - n1 * cs.y, n0 * cs.y + n1 * cs.x);
-      packed[2 * hh + 1] = pack16<F16>(n2 * cs.z - n3 * cs.w, n2 * cs.w + n3 * cs.z);
-    }
-    *reinterpret_cast<uint4*>(tile + (c >> 3) * half + sw128_off(row, c & 7)) =
-        make_uint4(packed[0], packed[1], packed[2], packed[3]);
-  }
-}
-
-// Four-lanes-per-row form of rope_norm_global: lane `quarter` (0..3) of the
-// four lanes that share a row handles head dims [32 quarter, +32) (chunks
-// 4 quarter .. 4 quarter + 3); the row's sum of squares is reduced over the four
-// lanes with shuffles, so every lane of the warp calls it (valid: the row
-// exists; the four lanes of a row agree; an invalid row is written as zeros).
+// Prologue of a raw row (bf16 or fp32) read from global memory, used when q/k
+// are fp32 (no in-place TMA staging): four lanes per row, lane `quarter`
+// (0..3) handling head dims [32 quarter, +32) (chunks 4 quarter .. + 3). Each
+// lane sums its squares in order; the row's sum is ((s0 + s1) + (s2 + s3)) by
+// two shuffles, so every lane of the warp calls it (valid: the row exists; the
+// four lanes of a row agree; an invalid row is written as zeros). Then
+// n = x w r and the pair rotation with the fp32 table, rounded once.
 template <bool F16>
 __device__ __forceinline__ void rope_norm_global_quad(const void* base, int64_t off, int dt,
                                                       const float* __restrict__ w, float eps,
