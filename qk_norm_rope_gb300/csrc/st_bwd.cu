@@ -832,8 +832,27 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         dl_c = ldg_nc_f32(P.delta + ri);
       }
     };
+    // A mask that varies along the queries: the mask rows of a tile (this
+    // CTA's keys, the tile's 128 queries, one row per thread) are prefetched
+    // into L2 a tile ahead of the compute warps, whose loads of them are
+    // otherwise the backward's bottleneck.
+    auto prefetch_mask = [&](int qt, int h) {
+      if constexpr (ELEM) {
+        constexpr int es = MK == kMaskF32 ? 4 : (MK == kMaskBF16 ? 2 : 1);
+        const int iq = qt * kTile + p, j0 = kt * kTile;
+        if (iq < c.Sq && j0 < c.Skv) {
+          const uint8_t* row = static_cast<const uint8_t*>(c.mask) +
+                               ((int64_t)b * c.m_sb + (int64_t)h * c.m_sh + (int64_t)iq * c.m_sq + j0) * es;
+          const int nbytes = min(kTile, c.Skv - j0) * es;
+          for (int off = 0; off < nbytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + off));
+        }
+      }
+    };
     WPos m = next_pos<MK>(c, b, W, W.start(), kt0);
-    if (W.more(m)) load_stats(W.qt(m) * kTile, W.head(m));
+    if (W.more(m)) {
+      load_stats(W.qt(m) * kTile, W.head(m));
+      prefetch_mask(W.qt(m), W.head(m));
+    }
     int n = 0;
     for (; ok && W.more(m); ++n) {
       const WPos m_next = next_pos<MK>(c, b, W, W.step(m), kt0);
@@ -844,7 +863,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
         break;
       stat[sq * 2 * kTile + p] = l2;
       stat[sq * 2 * kTile + kTile + p] = dl;
-      if (W.more(m_next)) load_stats(W.qt(m_next) * kTile, W.head(m_next));
+      if (W.more(m_next)) {
+        load_stats(W.qt(m_next) * kTile, W.head(m_next));
+        prefetch_mask(W.qt(m_next), W.head(m_next));
+      }
       mbar_arrive(&bars[kBarQFull + sq]);
       m = m_next;
     }
