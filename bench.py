@@ -199,12 +199,18 @@ def run_ours(args, rank, world, dev):
                                                      for_backward=True), dtype=torch.uint8, device=dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    def step(q=q, k=k, v=v, do=do, wq=wq, wk=wk, ids=ids, mask=mask):
+    def fwd_call(q=q, k=k, v=v, wq=wq, wk=wk, ids=ids, mask=mask):
         api.st_rope_attn_fwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, mask=mask, causal=inp.causal,
                              o=o, lse=lse, workspace=ws)
+
+    def bwd_call(q=q, k=k, v=v, do=do, wq=wq, wk=wk, ids=ids, mask=mask):
         api.st_rope_attn_bwd(q, k, v, wq, wk, inp.eps, ids, inp.axes, inp.theta, o, lse, do, mask=mask,
                              causal=inp.causal, workspace=ws, dq=dq, dk=dk, dv=dv, dwq=dwq, dwk=dwk,
                              reuse_tables=True)
+
+    def step(q=q, k=k, v=v, do=do, wq=wq, wk=wk, ids=ids, mask=mask):
+        fwd_call(q, k, v, wq, wk, ids, mask)
+        bwd_call(q, k, v, do, wq, wk, ids, mask)
 
     def barrier():
         if world > 1:
@@ -281,14 +287,38 @@ def run_ours(args, rank, world, dev):
             h2d += hmask.numel() * hmask.element_size()
         d2h = sum(t.numel() * t.element_size() for t in outs)
 
+        # The forward's inputs are copied first; dO (an input of the backward
+        # only) follows on a copy stream while the forward runs, and O and LSE
+        # go back to the host while the backward runs. Every copy of the step
+        # completes before the step's end event (the compute stream joins the
+        # copy stream).
+        copy_stream = torch.cuda.Stream(device=dev)
+        ev_in, ev_do, ev_fwd = torch.cuda.Event(), torch.cuda.Event(), torch.cuda.Event()
+        bq, bk, bv, bdo, bwq, bwk, bids = dbuf
+
         def e2e_step():
-            for dst, src in zip(dbuf, (hq, hk, hv, hdo, hwq, hwk, hids)):
+            cur = torch.cuda.current_stream()
+            copy_stream.wait_stream(cur)  # the previous step is done with the buffers
+            for dst, src in ((bq, hq), (bk, hk), (bv, hv), (bwq, hwq), (bwk, hwk), (bids, hids)):
                 dst.copy_(src, non_blocking=True)
             if hmask is not None:
                 dmask.copy_(hmask, non_blocking=True)
-            step(*dbuf, mask=dmask)
-            for dst, src in zip(houts, outs):
+            ev_in.record(cur)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(ev_in)  # behind the forward's inputs on the copy engine
+                bdo.copy_(hdo, non_blocking=True)
+                ev_do.record(copy_stream)
+            fwd_call(bq, bk, bv, bwq, bwk, bids, dmask)
+            ev_fwd.record(cur)
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(ev_fwd)
+                houts[0].copy_(o, non_blocking=True)
+                houts[1].copy_(lse, non_blocking=True)
+            cur.wait_event(ev_do)
+            bwd_call(bq, bk, bv, bdo, bwq, bwk, bids, dmask)
+            for dst, src in zip(houts[2:], outs[2:]):
                 dst.copy_(src, non_blocking=True)
+            cur.wait_stream(copy_stream)
 
         for _ in range(2):
             e2e_step()
