@@ -409,6 +409,7 @@ void fill_common(const Plan& P, const st_tensor* qw, const st_tensor* kw, float 
   c->m_sq = P.m_sq;
   if (P.mask_kind == kMaskBool) {
     c->flags = ws + P.off_flags;
+    c->mask_any_false = reinterpret_cast<const unsigned*>(ws + P.off_ctrl) + kCtrlAnyFalse;
     c->f_sb = P.Bm > 1 ? (int64_t)P.Hm * P.nQtm * P.nKt : 0;
     c->f_sh = P.Hm > 1 ? (int64_t)P.nQtm * P.nKt : 0;
     c->f_sq = P.nQtm > 1 ? P.nKt : 0;

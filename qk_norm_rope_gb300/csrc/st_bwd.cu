@@ -487,9 +487,7 @@ __device__ __noinline__ void bwd_epilogue(const BwdParams& P, uint8_t* sm, int n
 // ELEM: the mask varies along the queries (per-element terms); a mask that is
 // broadcast over the queries reduces to one term per key.
 template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 1)
-    bwd_kernel(const __grid_constant__ BwdParams P) {
-  grid_dependency_wait();
+__device__ __forceinline__ void bwd_body(const BwdParams& P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   if (smem_u32(sm) & 1023u) {  // the layout has no slack: refuse an unaligned base (uniform over the grid)
@@ -1051,6 +1049,23 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int MK, bool CAUSAL, bool QKT, bool ELEM, bool F16>
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kBwdThreads, 1)
+    bwd_kernel(const __grid_constant__ BwdParams P) {
+  grid_dependency_wait();
+  if constexpr (MK == kMaskBool) {
+    // A bool mask whose every element is True (found by the classify kernel
+    // of this call or of the forward whose tables it reuses) masks nothing:
+    // the unmasked body computes the same results without the per-tile class
+    // lookups in every role's walk.
+    if (*P.c.mask_any_false == 0u) {
+      bwd_body<kMaskNone, CAUSAL, QKT, false, F16>(P);
+      return;
+    }
+  }
+  bwd_body<MK, CAUSAL, QKT, ELEM, F16>(P);
 }
 
 }  // namespace

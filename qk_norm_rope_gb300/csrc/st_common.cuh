@@ -51,6 +51,7 @@ struct Common {
   const void* mask;            // element (b,h,i,j) at b*m_sb + h*m_sh + i*m_sq + j
   int64_t m_sb, m_sh, m_sq;    // 0 on broadcast dims
   const uint8_t* flags;        // bool masks: tile classes
+  const unsigned* mask_any_false;  // bool masks: the classify kernel's word, 0 when every element is True
   int64_t f_sb, f_sh, f_sq;    // strides of the flag array (0 on broadcast dims)
   int causal;
   int f16;           // MMA operand type: 0 bf16, 1 fp16 (v's dtype; q/k of 16 bits have it too)

@@ -236,8 +236,7 @@ __device__ __forceinline__ void masked_scores32(const Common& c, const uint32_t 
 }
 
 template <int MK, bool CAUSAL, bool QKT, bool F16>
-__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
-  grid_dependency_wait();
+__device__ __forceinline__ void fwd_body(const FwdParams& P) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   if (smem_u32(sm) & 1023u) {  // the layout has no slack: refuse an unaligned base (uniform over the grid)
@@ -831,6 +830,22 @@ __global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_consta
     __syncwarp();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int MK, bool CAUSAL, bool QKT, bool F16>
+__global__ void __launch_bounds__(kFwdThreads, 1) fwd_kernel(const __grid_constant__ FwdParams P) {
+  grid_dependency_wait();
+  if constexpr (MK == kMaskBool) {
+    // A bool mask whose every element is True (found by the classify kernel,
+    // which completed before the wait above) masks nothing: the unmasked
+    // kernel body computes the same results without the per-tile class
+    // lookups.
+    if (*P.c.mask_any_false == 0u) {
+      fwd_body<kMaskNone, CAUSAL, QKT, F16>(P);
+      return;
+    }
+  }
+  fwd_body<MK, CAUSAL, QKT, F16>(P);
 }
 
 }  // namespace
